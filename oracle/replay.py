@@ -1,0 +1,125 @@
+"""Replay a workload script through the oracle — TEST INFRASTRUCTURE.
+
+Runs the host events of a workload (admit, fork, append) through the naive
+block manager, applying every copy-on-write copy and every key/value write to
+the oracle's own bit-level pools in the order the events happen, then runs the
+decode step (each batch entry appends its token, then attends over all of its
+cached tokens, its new one included) and the float64 attention.
+
+The only thing shared with the GPU side is the workload description and the
+seeded values; the bookkeeping, the data movement and the attention are all
+the oracle's own.
+"""
+import numpy as np
+
+from .attention import paged_decode
+from .block_manager import NaiveBlockManager
+from .kvcache import append_kv, copy_blocks
+
+
+def values_to_numpy(t):
+    """A torch tensor of seeded values as numpy: float32 stays float32,
+    bfloat16 becomes its raw bits (uint16)."""
+    import torch
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy().astype(np.float32, copy=False)
+
+
+class OracleState:
+    """Result of a replay: pools after the step, the step's device inputs as the
+    oracle derived them, and (optionally) the attention output."""
+
+    def __init__(self):
+        self.k_pool = self.v_pool = None
+        self.setup_pairs = []
+        self.step_pairs = []
+        self.step_slots = None
+        self.block_tables = None
+        self.context_lens = None
+        self.bm = None
+
+
+def replay(wl, values, *, run_step=True):
+    """Replay ``wl``'s setup script (and its decode-step appends if run_step)."""
+    st = OracleState()
+    bm = NaiveBlockManager(wl.num_blocks, wl.block_size, wl.free_order)
+    store = np.float32 if wl.dtype == "f32" else np.uint16
+    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    K = np.zeros(shape, store)
+    V = np.zeros(shape, store)
+    hk = values_to_numpy(values["hist_k"])
+    hv = values_to_numpy(values["hist_v"])
+    row = 0
+    pend_slots, pend_rows, pend_set = [], [], set()
+
+    def flush():
+        if pend_slots:
+            rows = np.asarray(pend_rows, dtype=np.int64)
+            append_kv(K, V, hk[rows], hv[rows], np.asarray(pend_slots, dtype=np.int64))
+            pend_slots.clear()
+            pend_rows.clear()
+            pend_set.clear()
+
+    for ev in wl.events:
+        kind = ev[0]
+        if kind == "add":
+            rid, _ = bm.add_request(ev[2], ev[3])
+            assert rid == ev[1]
+        elif kind == "fork":
+            rid = bm.fork(ev[2])
+            assert rid == ev[1]
+        elif kind == "extend":
+            for tok in np.asarray(ev[2]).tolist():
+                slot, src, dst = bm.append_slot(ev[1], tok)
+                if src >= 0:
+                    flush()                     # the copy must see every earlier write
+                    copy_blocks(K, V, [(src, dst)])
+                    st.setup_pairs.append((src, dst))
+                if slot in pend_set:            # a slot written twice: keep the order
+                    flush()
+                pend_slots.append(slot)
+                pend_set.add(slot)
+                pend_rows.append(row)
+                row += 1
+        else:
+            raise ValueError(kind)
+    flush()
+
+    if run_step:
+        nk = values_to_numpy(values["new_k"])
+        nv = values_to_numpy(values["new_v"])
+        slots = []
+        for i, rid in enumerate(wl.batch.tolist()):
+            slot, src, dst = bm.append_slot(rid, int(wl.step_tokens[i]))
+            if src >= 0:
+                copy_blocks(K, V, [(src, dst)])
+                st.step_pairs.append((src, dst))
+            append_kv(K, V, nk[i:i + 1], nv[i:i + 1], [slot])
+            slots.append(slot)
+        st.step_slots = np.asarray(slots, dtype=np.int64)
+
+    S = wl.num_seqs
+    tables = [bm.block_table(r) for r in wl.batch.tolist()]
+    width = max(1, max(len(t) for t in tables))
+    bt = np.full((S, width), -1, dtype=np.int32)
+    for i, t in enumerate(tables):
+        bt[i, :len(t)] = t
+    st.block_tables = bt
+    st.context_lens = np.asarray([bm.seq_len(r) for r in wl.batch.tolist()], dtype=np.int32)
+    st.k_pool, st.v_pool, st.bm = K, V, bm
+    return st
+
+
+def attention(wl, values, st, seqs=None, threads=1):
+    """float64 decode attention for all batch entries (or the listed ones)."""
+    q = values_to_numpy(values["q"])
+    if q.dtype == np.uint16:
+        q = (q.astype(np.uint32) << 16).view(np.float32)
+    bt, lens = st.block_tables, st.context_lens
+    if seqs is not None:
+        seqs = np.asarray(seqs, dtype=np.int64)
+        q, bt, lens = q[seqs], bt[seqs], lens[seqs]
+    return paged_decode(q, st.k_pool, st.v_pool, bt, lens, wl.scale, wl.num_kv_heads,
+                        threads=threads)
