@@ -1,0 +1,246 @@
+/*
+ * pa.h — C ABI of the paged KV-cache decode library (libpagedattn.so).
+ *
+ * What the calls compute comes from two web pages on PagedAttention:
+ *   [Z]  zenaique, "How does PagedAttention enable prefix sharing across
+ *        requests and what data structure makes it cheap?" (answer text;
+ *        "Most common mistake"; interviewer follow-ups)
+ *   [K]  kgptalkie, "Day 28: PagedAttention / vLLM" (sections named below)
+ *
+ * Conventions for every call
+ *   - Return value: PA_OK (0) on success, a negative PA_ERR_* code otherwise.
+ *     Errors a host check can see are returned at once and nothing is
+ *     launched.  Errors only the GPU can see (a block id or slot outside the
+ *     pool) make the kernel skip the offending access and record the first
+ *     such code in the pool's device error word; pa_get_error reports it.
+ *     No call traps or aborts.
+ *   - Device pointers: every tensor argument marked "device" is GPU memory
+ *     owned by the caller, on the device the pool was created on.  The
+ *     library never frees caller memory.
+ *   - Streams: `stream` is a cudaStream_t passed as void*.  NULL means the
+ *     legacy default stream.  Every GPU call is asynchronous on it.
+ *
+ * Pool layout (owned by the pool, created zeroed):
+ *   K: [num_blocks][kv_heads][block_size][head_dim]   keys, one row per token
+ *   V: [num_blocks][kv_heads][head_dim][block_size]   values, transposed inside
+ *                                                      each (block, head) tile
+ *   Each (block, head) tile of K and of V is block_size * head_dim elements,
+ *   contiguous (4 KiB at block_size 16, head_dim 128, bf16).  Values are
+ *   stored transposed so the decode kernel loads them directly as
+ *   tensor-core operand fragments.  A slot is physical_block * block_size +
+ *   offset ([K] "Follow One Token Address"); a negative slot means "skip".
+ */
+#ifndef PAGED_KV_CACHE_PA_H
+#define PAGED_KV_CACHE_PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pa_pool pa_pool;
+typedef struct pa_bm pa_bm;
+
+/* Element type of the pool, of q/k/v inputs and (for out) of the output. */
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1,     /* a size, pointer or enum out of range */
+    PA_ERR_DTYPE = -2,           /* unsupported dtype combination */
+    PA_ERR_CUDA = -3,            /* a CUDA runtime call failed */
+    PA_ERR_NO_FREE_BLOCK = -4,   /* the free pool is empty */
+    PA_ERR_BAD_BLOCK_ID = -5,    /* (device) block id outside [0, num_blocks) */
+    PA_ERR_BAD_SLOT = -6,        /* (device) slot outside the pool */
+    PA_ERR_REFCOUNT = -7,        /* reference count would go below zero */
+    PA_ERR_UNKNOWN_REQUEST = -8, /* request id not live in the block manager */
+    PA_ERR_OUT_OF_MEMORY = -9,   /* host or device allocation failed */
+    PA_ERR_UNSUPPORTED = -10,    /* shape outside what the kernels handle */
+    PA_ERR_OVERLAP = -11,        /* (device) a copy pair's block is also used by
+                                    another pair of the same call */
+    PA_ERR_BAD_LENGTH = -12      /* (device) context length beyond the table */
+};
+
+/* ---------------------------------------------------------------- pool --- */
+
+/* Create a KV pool of `num_blocks` physical blocks of `block_size` token
+ * positions each, for `kv_heads` heads of width `head_dim` ([K] "Split the
+ * Cache Into Fixed Blocks": a block holds a fixed number of positions; its
+ * bytes depend on heads, head width and dtype).  One pool holds one layer.
+ * Allocates and zeroes K and V on the current CUDA device (synchronously).
+ * Limits: block_size in [1, 1024]; head_dim in [1, 256]; kv_heads >= 1.
+ * On success *out owns the pool; release it with pa_pool_destroy. */
+int pa_pool_create(int num_blocks, int block_size, int kv_heads, int head_dim,
+                   pa_dtype dtype, pa_pool **out);
+
+/* Free the pool, its device arrays and its decode workspace.  NULL is a no-op. */
+int pa_pool_destroy(pa_pool *pool);
+
+/* Device addresses of the pool's K and V arrays (layout above), for tests
+ * and for callers that fill the cache themselves.  Either may be NULL. */
+int pa_pool_kv_ptrs(pa_pool *pool, void **k, void **v);
+
+/* Copy the whole pool out to (export) or in from (import) caller buffers of
+ * the pool's layout and size (num_blocks * kv_heads * block_size * head_dim
+ * elements each), device or host memory, asynchronously on `stream`.  For
+ * snapshots and tests; not on the decode path. */
+int pa_pool_export(pa_pool *pool, void *k_dst, void *v_dst, void *stream);
+int pa_pool_import(pa_pool *pool, const void *k_src, const void *v_src, void *stream);
+
+/* Geometry of the pool: any output pointer may be NULL. */
+int pa_pool_info(const pa_pool *pool, int *num_blocks, int *block_size, int *kv_heads,
+                 int *head_dim, int *dtype);
+
+/* Write each new token's keys and values into its slot ([Z] answer: a new
+ * token "is written there"; [K] "Growth Needs Only Another Free Block").
+ *   k, v          device [T][kv_heads][head_dim], pool dtype, row-major
+ *   slot_mapping  device int64 [T]; slot = block * block_size + offset;
+ *                 negative = skip; >= num_blocks * block_size records
+ *                 PA_ERR_BAD_SLOT and is skipped
+ * Slots of one call must be distinct (the host block manager guarantees it);
+ * two tokens aimed at one slot leave either one's data.  T == 0 is a no-op. */
+int pa_append_kv(pa_pool *pool, const void *k, const void *v, const int64_t *slot_mapping,
+                 int num_tokens, void *stream);
+
+/* Copy-on-write block copies ([K] "Shared Blocks Must Not Be Changed in
+ * Place": a private copy of the shared block is made before the diverging
+ * write; [Z] "only a divergent block is ever copied, and only that block").
+ *   pairs  device int64 [P][2] = (src, dst); each copies all kv_heads x
+ *          block_size x head_dim elements of K and of V, bit for bit.
+ * A pair whose block id is outside the pool records PA_ERR_BAD_BLOCK_ID; a
+ * pair whose dst equals its own src, or whose src or dst is another pair's
+ * dst (or whose dst is another pair's src), records PA_ERR_OVERLAP; such
+ * pairs copy nothing, the others proceed.  Issue it before the appends into
+ * the copied blocks on the same stream.  P == 0 is a no-op. */
+int pa_copy_blocks(pa_pool *pool, const int64_t *pairs, int num_pairs, void *stream);
+
+/* Decode attention through block tables ([K] "The Block Table Is the Map",
+ * "Follow One Token Address", "Batching Becomes More Flexible"; verification
+ * recipe under "A Tiny Block-Table Example").  For every sequence s and query
+ * head h, with G = num_q_heads / kv_heads and kv = h / G:
+ *   x_j = scale * <q[s][h], K_s[j][kv]>   for every cached position
+ *                                         j = 0 .. context_lens[s]-1, where
+ *   K_s[j] is the key in block block_tables[s][j / block_size] at offset
+ *   j % block_size;   out[s][h] = sum_j softmax(x)_j * V_s[j][kv].
+ *   q             device [S][num_q_heads][head_dim], pool dtype
+ *   block_tables  device int32 [S][max_blocks_per_seq]; entries past a
+ *                 sequence's last block are never read
+ *   context_lens  device int32 [S]; 0 gives an all-zero output row; larger
+ *                 than max_blocks_per_seq * block_size records
+ *                 PA_ERR_BAD_LENGTH and is clamped
+ *   out           device [S][num_q_heads][head_dim] of out_dtype
+ * Keys/values are read once per (sequence, KV head) for all G query heads;
+ * long contexts are split over block ranges and merged by log-sum-exp.
+ * Arithmetic: bf16 pools use bf16 tensor-core products with fp32
+ * accumulation and fp32 softmax (the probabilities enter the value product
+ * as a bf16 high part plus a bf16 low part); f32 pools use fp32 CUDA cores.
+ * Supported: num_q_heads a multiple of kv_heads with G <= 16; bf16 pools
+ * with head_dim in {64, 128, 256}, block_size a multiple of 16 and G <= 8
+ * take the tensor-core path, every other shape the fp32 CUDA-core path;
+ * S <= 16384.
+ * Workspace: the pool keeps a device workspace for the split partials; a
+ * call that needs more than it holds grows it (cudaMalloc, synchronous).
+ * pa_decode_reserve sizes it ahead of time. */
+int pa_decode(pa_pool *pool, const void *q, int num_seqs, int num_q_heads,
+              const int32_t *block_tables, int max_blocks_per_seq,
+              const int32_t *context_lens, float scale, void *out, pa_dtype out_dtype,
+              void *stream);
+
+/* Size the pool's decode workspace for batches up to these bounds. */
+int pa_decode_reserve(pa_pool *pool, int max_seqs, int max_q_heads);
+
+/* Synchronize `stream`, then return and clear the first error the pool's
+ * kernels recorded since the last call (PA_OK if none). */
+int pa_get_error(pa_pool *pool, void *stream);
+
+/* Static text for an error code. */
+const char *pa_error_string(int code);
+
+/* Number of kernels the library launched since it was loaded (all pools). */
+uint64_t pa_launch_count(void);
+
+/* ------------------------------------------------- host block manager --- */
+/* Plain host bookkeeping, not on the GPU ([K] "Growth Needs Only Another
+ * Free Block", "Shared Blocks Must Not Be Changed in Place"; [Z] answer and
+ * follow-ups on the parent-chained hash and the cache key):
+ *   - free pool: FIFO, initial order given; freed blocks join the tail in
+ *     table order;
+ *   - a request grows by one free block when its next token starts a block;
+ *   - reference count per block = number of live requests pointing at it;
+ *     a block returns to the free pool when its count reaches zero;
+ *   - copy-on-write: the next token of a request whose last block another
+ *     request also points at goes to a fresh block; the pair (old, fresh) is
+ *     returned for pa_copy_blocks and only this request's entry is repointed;
+ *   - prefix cache: each full block is hashed as FNV-1a-64 over (parent
+ *     block's hash, 8 bytes LE; salt, 8 bytes LE; its token ids, 4 bytes LE
+ *     each), the first block's parent hash being 0; a table maps hash to
+ *     physical block; admission reuses leading cached blocks while the
+ *     chain hits (token ids and parent block compared too) and stops at the
+ *     first miss.  A block leaves the hash table when freed.
+ * Not thread-safe: one manager per thread. */
+
+/* free_order: host int32 [num_blocks], a permutation of 0..num_blocks-1 giving
+ * the free pool's initial order; NULL means 0, 1, 2, ... */
+int pa_bm_create(int num_blocks, int block_size, const int32_t *free_order, pa_bm **out);
+int pa_bm_destroy(pa_bm *bm);
+
+/* Admit a request with prompt token ids tokens[0..n); reuses cached full
+ * blocks of the prompt's prefix.  *req = new request id, *cached_tokens =
+ * number of leading prompt tokens already in the cache.  The caller appends
+ * the remaining prompt tokens with pa_bm_append_slot(s). */
+int pa_bm_add_request(pa_bm *bm, const int32_t *tokens, int n, uint64_t salt, int *req,
+                      int *cached_tokens);
+
+/* A new request sharing every block of `parent` (parallel sampling). */
+int pa_bm_fork(pa_bm *bm, int parent, int *child);
+
+/* Reserve the slot of request `req`'s next token (token id `token`).
+ * *slot = block * block_size + offset.  *cow_src / *cow_dst = the copy pair
+ * when copy-on-write happened, else -1 / -1.  On error nothing changes. */
+int pa_bm_append_slot(pa_bm *bm, int req, int32_t token, int64_t *slot, int64_t *cow_src,
+                      int64_t *cow_dst);
+
+/* Batched form: for i in 0..n, append tokens[i] to reqs[i] in order.
+ * slots[i] receives each slot; copy pairs are written to cow_pairs
+ * ([*num_pairs][2], room for n pairs) in the order they arise.  Stops at the
+ * first error; *num_done = entries applied before it. */
+int pa_bm_append_slots(pa_bm *bm, int n, const int32_t *reqs, const int32_t *tokens,
+                       int64_t *slots, int64_t *cow_pairs, int *num_pairs, int *num_done);
+
+/* Release a finished request's blocks. */
+int pa_bm_free_request(pa_bm *bm, int req);
+
+/* Copy the request's block table into out[0..cap); *n = its length. */
+int pa_bm_block_table(pa_bm *bm, int req, int32_t *out, int cap, int *n);
+
+/* Fill tables [n][width] (host, int32) with the block tables of reqs[0..n),
+ * padding with -1, and lens[n] with their token counts. */
+int pa_bm_batch_tables(pa_bm *bm, int n, const int32_t *reqs, int width, int32_t *tables,
+                       int32_t *lens);
+
+/* Number of tokens of a request; -1 if unknown. */
+int pa_bm_seq_len(pa_bm *bm, int req);
+
+/* Reference count of a block (0 = free); -1 if out of range. */
+int pa_bm_refcount(pa_bm *bm, int block);
+
+/* Number of free blocks. */
+int pa_bm_num_free(pa_bm *bm);
+
+/* Copy the free pool in FIFO order into out[0..cap); *n = its length. */
+int pa_bm_free_list(pa_bm *bm, int32_t *out, int cap, int *n);
+
+/* 1 if the block is registered in the prefix hash table, 0 if not, -1 if out
+ * of range. */
+int pa_bm_is_cached(pa_bm *bm, int block);
+
+/* FNV-1a-64 of a byte string (exposed so the hash can be checked). */
+uint64_t pa_bm_fnv1a64(const uint8_t *data, size_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_CACHE_PA_H */

@@ -1,0 +1,305 @@
+// C-ABI front end of libpagedattn: pool lifetime, argument checks, decode
+// workspace and the device error word.  Semantics are documented in pa.h.
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include <cuda_runtime.h>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace pa_detail {
+
+static std::atomic<uint64_t> g_launch_counter{0};
+void count_launch() { g_launch_counter.fetch_add(1, std::memory_order_relaxed); }
+
+}  // namespace pa_detail
+
+namespace {
+
+constexpr double kLog2e = 1.4426950408889634;
+
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+size_t elem_size(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
+
+// Workspace: [counters S*Hkv ints, 256-aligned][part_acc][part_ml]
+size_t workspace_bytes(const pa_detail::DecodePlan& plan, int S, int Hkv, int G, int D,
+                       size_t* counters_bytes) {
+    const size_t cb = round256(static_cast<size_t>(S) * Hkv * sizeof(int));
+    const size_t acc = round256(plan.max_items * G * D * sizeof(float));
+    const size_t ml = round256(plan.max_items * G * 2 * sizeof(float));
+    if (counters_bytes) *counters_bytes = cb;
+    return cb + acc + ml;
+}
+
+// Grow the pool's workspace to at least `bytes`; new memory is zeroed (the
+// arrival counters must start at zero and are reset by the kernel after use).
+int ensure_workspace(pa_pool* pool, size_t bytes) {
+    if (pool->ws_bytes >= bytes) return PA_OK;
+    if (pool->ws) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+        cudaFree(pool->ws);
+        pool->ws = nullptr;
+        pool->ws_bytes = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_ERR_OUT_OF_MEMORY;
+    }
+    if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+        cudaFree(p);
+        return PA_ERR_CUDA;
+    }
+    pool->ws = p;
+    pool->ws_bytes = bytes;
+    return PA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int pa_pool_create(int num_blocks, int block_size, int kv_heads, int head_dim, pa_dtype dtype,
+                   pa_pool** out) {
+    if (!out || num_blocks <= 0 || block_size <= 0 || block_size > 1024 || kv_heads <= 0 ||
+        head_dim <= 0 || head_dim > 256)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+    *out = nullptr;
+    pa_pool* p = new (std::nothrow) pa_pool();
+    if (!p) return PA_ERR_OUT_OF_MEMORY;
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) !=
+            cudaSuccess) {
+        delete p;
+        return PA_ERR_CUDA;
+    }
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->kv_heads = kv_heads;
+    p->head_dim = head_dim;
+    p->dtype = dtype;
+    const size_t bytes =
+        static_cast<size_t>(num_blocks) * kv_heads * block_size * head_dim * elem_size(dtype);
+    if (cudaMalloc(&p->k, bytes) != cudaSuccess || cudaMalloc(&p->v, bytes) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void**>(&p->err), sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p->k);
+        cudaFree(p->v);
+        cudaFree(p->err);
+        delete p;
+        return PA_ERR_OUT_OF_MEMORY;
+    }
+    if (cudaMemset(p->k, 0, bytes) != cudaSuccess || cudaMemset(p->v, 0, bytes) != cudaSuccess ||
+        cudaMemset(p->err, 0, sizeof(int)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(p->k);
+        cudaFree(p->v);
+        cudaFree(p->err);
+        delete p;
+        return PA_ERR_CUDA;
+    }
+    *out = p;
+    return PA_OK;
+}
+
+int pa_pool_destroy(pa_pool* pool) {
+    if (!pool) return PA_OK;
+    DeviceGuard g(pool->device);
+    cudaDeviceSynchronize();
+    cudaFree(pool->k);
+    cudaFree(pool->v);
+    cudaFree(pool->err);
+    cudaFree(pool->ws);
+    delete pool;
+    return PA_OK;
+}
+
+int pa_pool_kv_ptrs(pa_pool* pool, void** k, void** v) {
+    if (!pool) return PA_ERR_INVALID_ARG;
+    if (k) *k = pool->k;
+    if (v) *v = pool->v;
+    return PA_OK;
+}
+
+static int pool_copy(pa_pool* pool, void* k_dst, const void* k_src, void* v_dst,
+                     const void* v_src, void* stream) {
+    DeviceGuard g(pool->device);
+    if (!g.ok) return PA_ERR_CUDA;
+    const size_t bytes = static_cast<size_t>(pool->num_blocks) * pool->kv_heads *
+                         pool->block_size * pool->head_dim * elem_size(pool->dtype);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(k_dst, k_src, bytes, cudaMemcpyDefault, st) != cudaSuccess ||
+        cudaMemcpyAsync(v_dst, v_src, bytes, cudaMemcpyDefault, st) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+int pa_pool_export(pa_pool* pool, void* k_dst, void* v_dst, void* stream) {
+    if (!pool || !k_dst || !v_dst) return PA_ERR_INVALID_ARG;
+    return pool_copy(pool, k_dst, pool->k, v_dst, pool->v, stream);
+}
+
+int pa_pool_import(pa_pool* pool, const void* k_src, const void* v_src, void* stream) {
+    if (!pool || !k_src || !v_src) return PA_ERR_INVALID_ARG;
+    return pool_copy(pool, pool->k, k_src, pool->v, v_src, stream);
+}
+
+int pa_pool_info(const pa_pool* pool, int* num_blocks, int* block_size, int* kv_heads,
+                 int* head_dim, int* dtype) {
+    if (!pool) return PA_ERR_INVALID_ARG;
+    if (num_blocks) *num_blocks = pool->num_blocks;
+    if (block_size) *block_size = pool->block_size;
+    if (kv_heads) *kv_heads = pool->kv_heads;
+    if (head_dim) *head_dim = pool->head_dim;
+    if (dtype) *dtype = pool->dtype;
+    return PA_OK;
+}
+
+int pa_append_kv(pa_pool* pool, const void* k, const void* v, const int64_t* slot_mapping,
+                 int num_tokens, void* stream) {
+    if (!pool || num_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !aligned(slot_mapping, 8)) return PA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_tokens) * pool->kv_heads * 32 > (int64_t{1} << 31) * 256)
+        return PA_ERR_UNSUPPORTED;
+    DeviceGuard g(pool->device);
+    if (!g.ok) return PA_ERR_CUDA;
+    return pa_detail::launch_append(pool, k, v, slot_mapping, num_tokens,
+                                    static_cast<cudaStream_t>(stream));
+}
+
+int pa_copy_blocks(pa_pool* pool, const int64_t* pairs, int num_pairs, void* stream) {
+    if (!pool || num_pairs < 0) return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!pairs || !aligned(pairs, 8)) return PA_ERR_INVALID_ARG;
+    DeviceGuard g(pool->device);
+    if (!g.ok) return PA_ERR_CUDA;
+    return pa_detail::launch_copy(pool, pairs, num_pairs, static_cast<cudaStream_t>(stream));
+}
+
+static int check_decode_args(const pa_pool* pool, const void* q, int S, int Hq,
+                             const int32_t* tables, int max_blocks, const int32_t* lens,
+                             const void* out, pa_dtype out_dtype) {
+    if (!pool || S < 0 || Hq <= 0 || max_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (Hq % pool->kv_heads != 0 || Hq / pool->kv_heads > 16) return PA_ERR_UNSUPPORTED;
+    if (out_dtype != PA_F32 && out_dtype != PA_BF16) return PA_ERR_DTYPE;
+    if (S > 16384) return PA_ERR_UNSUPPORTED;
+    if (S == 0) return PA_OK;
+    if (!q || !tables || !lens || !out || max_blocks == 0) return PA_ERR_INVALID_ARG;
+    if (!aligned(q, 16)) return PA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_blocks) * pool->block_size > (int64_t{1} << 30))
+        return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+int pa_decode_reserve(pa_pool* pool, int max_seqs, int max_q_heads) {
+    if (!pool || max_seqs <= 0 || max_q_heads <= 0 || max_q_heads % pool->kv_heads)
+        return PA_ERR_INVALID_ARG;
+    DeviceGuard g(pool->device);
+    if (!g.ok) return PA_ERR_CUDA;
+    pa_detail::DecodePlan plan;
+    // the fp32 path's partial count grows with the table width; reserve for the fast path
+    int rc = pa_detail::plan_decode(pool, max_seqs, max_q_heads, 1, &plan);
+    if (rc != PA_OK) return rc;
+    return ensure_workspace(pool, workspace_bytes(plan, max_seqs, pool->kv_heads,
+                                                  max_q_heads / pool->kv_heads, pool->head_dim,
+                                                  nullptr));
+}
+
+int pa_decode(pa_pool* pool, const void* q, int num_seqs, int num_q_heads,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              float scale, void* out, pa_dtype out_dtype, void* stream) {
+    int rc = check_decode_args(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                               context_lens, out, out_dtype);
+    if (rc != PA_OK || num_seqs == 0) return rc;
+    DeviceGuard g(pool->device);
+    if (!g.ok) return PA_ERR_CUDA;
+    const int G = num_q_heads / pool->kv_heads;
+    pa_detail::DecodePlan plan;
+    rc = pa_detail::plan_decode(pool, num_seqs, num_q_heads, max_blocks_per_seq, &plan);
+    if (rc != PA_OK) return rc;
+    size_t cb = 0;
+    const size_t need = workspace_bytes(plan, num_seqs, pool->kv_heads, G, pool->head_dim, &cb);
+    rc = ensure_workspace(pool, need);
+    if (rc != PA_OK) return rc;
+    DecodeParams p{};
+    p.q = q;
+    p.k = pool->k;
+    p.v = pool->v;
+    p.tables = block_tables;
+    p.lens = context_lens;
+    p.out = out;
+    p.counters = static_cast<int*>(pool->ws);
+    p.part_acc = reinterpret_cast<float*>(static_cast<char*>(pool->ws) + cb);
+    p.part_ml = reinterpret_cast<float*>(
+        static_cast<char*>(pool->ws) + cb + round256(plan.max_items * G * pool->head_dim * sizeof(float)));
+    p.err = pool->err;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    p.S = num_seqs;
+    p.Hq = num_q_heads;
+    p.Hkv = pool->kv_heads;
+    p.G = G;
+    p.D = pool->head_dim;
+    p.B = pool->block_size;
+    p.num_blocks = pool->num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.out_bf16 = out_dtype == PA_BF16;
+    return pa_detail::launch_decode(plan, p, static_cast<cudaStream_t>(stream));
+}
+
+int pa_get_error(pa_pool* pool, void* stream) {
+    if (!pool) return PA_ERR_INVALID_ARG;
+    DeviceGuard g(pool->device);
+    if (!g.ok) return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+    int code = 0;
+    if (cudaMemcpy(&code, pool->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (code != 0 && cudaMemset(pool->err, 0, sizeof(int)) != cudaSuccess) return PA_ERR_CUDA;
+    return code;
+}
+
+const char* pa_error_string(int code) {
+    switch (code) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_DTYPE: return "unsupported dtype";
+        case PA_ERR_CUDA: return "CUDA runtime error";
+        case PA_ERR_NO_FREE_BLOCK: return "no free block in the pool";
+        case PA_ERR_BAD_BLOCK_ID: return "block id outside the pool";
+        case PA_ERR_BAD_SLOT: return "slot outside the pool";
+        case PA_ERR_REFCOUNT: return "reference count underflow";
+        case PA_ERR_UNKNOWN_REQUEST: return "unknown request";
+        case PA_ERR_OUT_OF_MEMORY: return "out of memory";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape";
+        case PA_ERR_OVERLAP: return "copy pairs overlap";
+        case PA_ERR_BAD_LENGTH: return "context length beyond the block table";
+        default: return "unknown error";
+    }
+}
+
+uint64_t pa_launch_count(void) {
+    return pa_detail::g_launch_counter.load(std::memory_order_relaxed);
+}
+
+}  // extern "C"

@@ -1,0 +1,128 @@
+// KV append and copy-on-write block copy kernels.
+//
+// append: each new token's keys and values go to its (physical block,
+// offset) slot (kgptalkie "Day 28: PagedAttention / vLLM", "Follow One Token
+// Address", "Growth Needs Only Another Free Block"; zenaique prefix-sharing
+// answer: the new token "is written there").
+// copy:   copy-on-write duplicates a whole shared block before the diverging
+// write (kgptalkie "Shared Blocks Must Not Be Changed in Place"; zenaique
+// "Most common mistake": only the divergent block is copied).
+//
+// Both are pure data movement: elements are moved as raw bits.
+#include <cstdint>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace {
+
+// One warp per (token, KV head).  The key row is contiguous in the pool and is
+// written with whole-row vector stores; the value row lands in a column of the
+// transposed (head_dim x block_size) value tile, one element per dimension.
+template <typename E>
+__global__ void __launch_bounds__(256) append_kv_kernel(
+    E* __restrict__ kpool, E* __restrict__ vpool, const E* __restrict__ k,
+    const E* __restrict__ v, const int64_t* __restrict__ slots, int T, int Hkv, int D, int B,
+    int64_t num_slots, int* err) {
+    const int warp = static_cast<int>((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp >= T * Hkv) return;
+    const int t = warp / Hkv;
+    const int h = warp - t * Hkv;
+    const int64_t slot = slots[t];
+    if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (lane == 0) pa_dev::record_error(err, PA_ERR_BAD_SLOT);
+        return;
+    }
+    const int64_t blk = slot / B;
+    const int off = static_cast<int>(slot - blk * B);
+    const int64_t tile = (blk * Hkv + h) * static_cast<int64_t>(B) * D;
+    const E* ksrc = k + (static_cast<int64_t>(t) * Hkv + h) * D;
+    const E* vsrc = v + (static_cast<int64_t>(t) * Hkv + h) * D;
+    E* kdst = kpool + tile + static_cast<int64_t>(off) * D;
+    constexpr int kVec = 16 / sizeof(E);
+    const bool vec = (D % kVec == 0) &&
+                     ((reinterpret_cast<uintptr_t>(ksrc) | reinterpret_cast<uintptr_t>(kdst)) % 16 == 0);
+    if (vec) {
+        for (int i = lane; i < D / kVec; i += 32)
+            reinterpret_cast<uint4*>(kdst)[i] = reinterpret_cast<const uint4*>(ksrc)[i];
+    } else {
+        for (int d = lane; d < D; d += 32) kdst[d] = ksrc[d];
+    }
+    E* vdst = vpool + tile + off;
+    for (int d = lane; d < D; d += 32) vdst[static_cast<int64_t>(d) * B] = vsrc[d];
+}
+
+// One CTA per (src, dst) pair.  The pair is checked against every other pair
+// of the call first; a conflicting or out-of-range pair copies nothing.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(
+    uint8_t* __restrict__ kpool, uint8_t* __restrict__ vpool, const int64_t* __restrict__ pairs,
+    int P, int64_t num_blocks, int64_t block_bytes, int* err) {
+    const int i = blockIdx.x;
+    const int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+    const bool range_bad = src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks;
+    int conflict = (src == dst);
+    for (int j = threadIdx.x; j < P; j += blockDim.x) {
+        if (j == i) continue;
+        const int64_t s2 = pairs[2 * j], d2 = pairs[2 * j + 1];
+        conflict |= (dst == s2) | (dst == d2) | (src == d2);
+    }
+    conflict = __syncthreads_or(conflict);
+    if (range_bad || conflict) {
+        if (threadIdx.x == 0)
+            pa_dev::record_error(err, range_bad ? PA_ERR_BAD_BLOCK_ID : PA_ERR_OVERLAP);
+        return;
+    }
+    for (int which = 0; which < 2; ++which) {
+        uint8_t* base = which == 0 ? kpool : vpool;
+        const uint8_t* s = base + src * block_bytes;
+        uint8_t* d = base + dst * block_bytes;
+        if (block_bytes % 16 == 0) {
+            const int64_t n = block_bytes / 16;
+            for (int64_t e = threadIdx.x; e < n; e += blockDim.x)
+                reinterpret_cast<uint4*>(d)[e] = reinterpret_cast<const uint4*>(s)[e];
+        } else {
+            const int64_t n = block_bytes / 2;      // elements are 2 or 4 bytes
+            for (int64_t e = threadIdx.x; e < n; e += blockDim.x)
+                reinterpret_cast<uint16_t*>(d)[e] = reinterpret_cast<const uint16_t*>(s)[e];
+        }
+    }
+}
+
+}  // namespace
+
+namespace pa_detail {
+
+int launch_append(const pa_pool* p, const void* k, const void* v, const int64_t* slots, int T,
+                  cudaStream_t st) {
+    const int64_t warps = static_cast<int64_t>(T) * p->kv_heads;
+    const int threads = 256;
+    const int64_t grid = (warps * 32 + threads - 1) / threads;
+    const int64_t num_slots = static_cast<int64_t>(p->num_blocks) * p->block_size;
+    if (p->dtype == PA_BF16)
+        append_kv_kernel<uint16_t><<<static_cast<unsigned>(grid), threads, 0, st>>>(
+            static_cast<uint16_t*>(p->k), static_cast<uint16_t*>(p->v),
+            static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), slots, T,
+            p->kv_heads, p->head_dim, p->block_size, num_slots, p->err);
+    else
+        append_kv_kernel<uint32_t><<<static_cast<unsigned>(grid), threads, 0, st>>>(
+            static_cast<uint32_t*>(p->k), static_cast<uint32_t*>(p->v),
+            static_cast<const uint32_t*>(k), static_cast<const uint32_t*>(v), slots, T,
+            p->kv_heads, p->head_dim, p->block_size, num_slots, p->err);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int launch_copy(const pa_pool* p, const int64_t* pairs, int P, cudaStream_t st) {
+    const int64_t esz = p->dtype == PA_BF16 ? 2 : 4;
+    const int64_t block_bytes =
+        static_cast<int64_t>(p->kv_heads) * p->block_size * p->head_dim * esz;
+    copy_blocks_kernel<<<P, 256, 0, st>>>(static_cast<uint8_t*>(p->k),
+                                          static_cast<uint8_t*>(p->v), pairs, P,
+                                          p->num_blocks, block_bytes, p->err);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa_detail
