@@ -1,0 +1,367 @@
+"""Benchmark of one paged decode step on GB300.
+
+A step is one pass of the hot path over one batch: copy-on-write block copies
+(when the step has any), KV append of every sequence's new token, and paged
+decode attention over every cached token, new one included.
+
+Default workload: the decode batch (64 sequences, context lengths U[128, 2048],
+block_size 16, 32 query / 8 KV heads, head_dim 128, bf16, pool 1.25x the
+blocks needed, scattered block tables).  Other workloads: --workload
+{prefix,long,mixed,tiny}.
+
+value      = unique KV bytes the decode reads per step / device step time (GB/s),
+             inputs resident in HBM, L2 flushed (256 MiB write) between steps.
+e2e        = the same bytes / step time through the public API with host
+             buffers: pinned host->device copies of the step's inputs, the
+             three library calls, device->host copy of the output.
+roofline   = the decode kernel alone: algorithmic bytes per launch / its
+             CUDA-event time, against the measured HBM copy bandwidth.
+cpu_baseline = the float64 oracle on the host cores on a bounded sample.
+
+--impl reference times the oracle (the only other implementation there is)
+on the same workload, a bounded sample of sequences per step.
+N > 1 (torchrun): every rank runs its own replica (decode needs no exchange);
+value sums all ranks' bytes over the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode KV GB/s (% of GB300 HBM peak) and decode tokens/s per step"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _workload_desc(wl):
+    return (f"{wl.name}: {wl.description}; block_size {wl.block_size}, {wl.num_q_heads} q / "
+            f"{wl.num_kv_heads} KV heads, head_dim {wl.head_dim}, {wl.dtype}, "
+            f"{wl.num_blocks} physical blocks")
+
+
+def _kv_bytes(wl, lens, shared_blocks=0):
+    """Unique key+value bytes the decode reads: every cached token of every
+    sequence, K and V, all KV heads (blocks shared by several sequences are
+    counted once per sequence here unless the step reads them once)."""
+    per_tok = wl.num_kv_heads * wl.head_dim * 2 * wl.elem_bytes
+    return int(sum(int(x) for x in lens)) * per_tok
+
+
+def _algo_bytes(wl, lens):
+    """Everything the decode kernel must move: KV + q + out + tables + lens."""
+    S = wl.num_seqs
+    q = S * wl.num_q_heads * wl.head_dim * wl.elem_bytes
+    out = S * wl.num_q_heads * wl.head_dim * 4
+    blocks = sum(-(-int(x) // wl.block_size) for x in lens)
+    return _kv_bytes(wl, lens) + q + out + blocks * 4 + S * 4
+
+
+def _traffic_from_profile():
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged."""
+    src = os.path.join(ROOT, "paged_kv_cache_253_gb300", "csrc", "pa_decode.cu")
+    prof = os.path.join(ROOT, "profiles", "decode_kernel_decode_batch.md")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        text = open(prof).read()
+        m_hash = re.search(r"source sha256\[:16\]:\s*`?([0-9a-f]{16})", text)
+        m_tr = re.search(r"dram bytes per launch:\s*`?([0-9]+)", text)
+        if m_hash and m_tr and m_hash.group(1) == digest:
+            return int(m_tr.group(1))
+    except OSError:
+        pass
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        except OSError:
+            pass
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _oracle_sample(wl, values, target_s=12.0, threads=None):
+    """Time the oracle (step appends + float64 decode) on a bounded sample of
+    sequences; returns (GB/s of KV processed, tokens/s, threads, description)."""
+    import numpy as np
+    from oracle import replay as orp
+    from oracle.attention import default_threads
+    threads = threads or default_threads()
+    st = orp.replay(wl, values)
+    lens = st.context_lens
+    order = np.random.default_rng(wl.seed).permutation(wl.num_seqs)
+    # grow the sample until it takes about target_s
+    n, spent, done_tok, done_seq, calls = 1, 0.0, 0, 0, 0
+    pos = 0
+    while spent < target_s and pos < len(order):
+        pick = order[pos:pos + n]
+        t0 = time.perf_counter()
+        orp.attention(wl, values, st, seqs=pick, threads=threads)
+        dt = time.perf_counter() - t0
+        spent += dt
+        done_tok += int(lens[pick].sum())
+        done_seq += len(pick)
+        pos += len(pick)
+        calls += 1
+        n = max(1, min(len(order) - pos, int(n * 2)))
+    per_tok = wl.num_kv_heads * wl.head_dim * 2 * wl.elem_bytes
+    gbs = done_tok * per_tok / spent / 1e9
+    desc = (f"{done_seq} of {wl.num_seqs} sequences ({done_tok} cached tokens) of the same "
+            f"workload, float64 oracle, {threads} threads, {spent:.1f} s")
+    return gbs, done_seq / spent, threads, desc
+
+
+def run_reference(args):
+    world, rank, local = _dist()
+    if rank != 0:
+        return 0
+    from paged_kv_cache_253_gb300 import workloads as wls
+    wl = wls.make_workload(args.workload)
+    values = wls.generate_values(wl, "cpu")
+    per_step = max(2.0, 40.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _oracle_sample(wl, values, target_s=per_step / 4)
+    vals, toks, descs = [], [], []
+    for _ in range(args.steps):
+        gbs, tps, threads, desc = _oracle_sample(wl, values, target_s=per_step)
+        vals.append(gbs)
+        toks.append(tps)
+        descs.append(desc)
+    v = sum(vals) / len(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": _workload_desc(wl)},
+        "tokens_per_s": round(sum(toks) / len(toks), 3),
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": descs[-1]},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import torch
+    from paged_kv_cache_253_gb300 import api, runtime
+    from paged_kv_cache_253_gb300 import workloads as wls
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    wl = wls.make_workload(args.workload)
+    values = wls.generate_values(wl, f"cuda:{local}", seed=wl.seed + 1000 * rank)
+    pool, bm, _ = runtime.replay_setup(wl, values, f"cuda:{local}")
+    step = runtime.prepare_step(wl, values, pool, bm)
+    lens = step.context_lens.cpu().numpy()
+    kv_bytes = _kv_bytes(wl, lens)
+    algo_bytes = _algo_bytes(wl, lens)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    if pool.get_error():
+        raise RuntimeError("device error during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = api.launch_count()
+    with Clocks(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)                       # evict L2 between steps
+            a, b, c = ev[i]
+            a.record(stream)
+            if step.num_pairs:
+                pool.copy_blocks(step.pairs)
+            pool.append_kv(step.new_k, step.new_v, step.slots)
+            b.record(stream)
+            pool.decode(step.q, step.block_tables, step.context_lens, step.scale, out=step.out)
+            c.record(stream)
+        torch.cuda.synchronize()
+    launches = api.launch_count() - launches0
+    if dist:
+        dist.barrier()
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    dec_ms = [b.elapsed_time(c) for a, b, c in ev]
+    ms = sum(step_ms) / len(step_ms)
+    dms = sum(dec_ms) / len(dec_ms)
+    if dist:
+        t = torch.tensor([ms, dms], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, dms = t.tolist()
+    if pool.get_error():
+        raise RuntimeError("device error during the timed steps")
+
+    # ---- end to end: host buffers, pinned, through the public API ----
+    host = {k: getattr(step, k).cpu().pin_memory() for k in
+            ("q", "new_k", "new_v", "slots", "pairs", "block_tables", "context_lens")}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    dev = {k: torch.empty_like(v, device=f"cuda:{local}") for k, v in host.items()}
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(i & 0xFF)
+        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in dev:
+            dev[k].copy_(host[k], non_blocking=True)
+        if dev["pairs"].shape[0]:
+            pool.copy_blocks(dev["pairs"])
+        pool.append_kv(dev["new_k"], dev["new_v"], dev["slots"])
+        pool.decode(dev["q"], dev["block_tables"], dev["context_lens"], step.scale, out=step.out)
+        out_host.copy_(step.out, non_blocking=True)
+        c.record(stream)
+        c.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(c))
+    ems = sum(e2e_ms) / len(e2e_ms)
+    if dist:
+        t = torch.tensor([ems], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ems = t.item()
+
+    peak, peak_kind = _peaks()
+    achieved = algo_bytes / (dms * 1e-3) / 1e9
+    value = world * kv_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic",
+        "config": {"workload": _workload_desc(wl),
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "kv_bytes_per_step": kv_bytes, "copy_pairs_per_step": step.num_pairs,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "hbm_frac_of_" + peak_kind: round(value / world / peak, 4),
+        "tokens_per_s": round(world * wl.num_seqs / (ms * 1e-3), 1),
+        "decode_ms": round(dms, 5),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": _traffic_from_profile(), "kernel": "decode (pa_decode)",
+                     "algorithmic_bytes_per_launch": algo_bytes},
+        "e2e": {"value": round(world * kv_bytes / (ems * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(ems, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, tps, threads, desc = _oracle_sample(wl, {k: v.cpu() for k, v in values.items()},
+                                                 target_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode",
+                    choices=["tiny", "decode", "prefix", "long", "mixed"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    from paged_kv_cache_253_gb300 import build
+    build.build()
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

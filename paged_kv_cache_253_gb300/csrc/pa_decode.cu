@@ -401,7 +401,8 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(const DecodePar
     float* res = sc + p.G * PTm;                              // [G][OS]
     float* res_m = res + p.G * OS;                            // [16]
     float* res_l = res_m + 16;                                // [16]
-    long long* s_red = reinterpret_cast<long long*>(res_l + 16);
+    const int used = p.G * p.D + p.G * PTm + p.G * OS + 32;   // floats so far
+    long long* s_red = reinterpret_cast<long long*>(qs + (used + 3) / 4 * 4);
     int* s_flag = reinterpret_cast<int*>(s_red + kWarps);
     int* s_start = s_flag + 4;
 
@@ -481,7 +482,7 @@ size_t fast_smem(int D, int S) {
 }
 
 size_t simple_smem(int G, int D, int PT, int S) {
-    return static_cast<size_t>(G * D + G * PT + G * (D + 4) + 32) * sizeof(float) +
+    return static_cast<size_t>((G * D + G * PT + G * (D + 4) + 32 + 3) / 4 * 4) * sizeof(float) +
            kWarps * sizeof(long long) + 4 * sizeof(int) + static_cast<size_t>(S + 1) * sizeof(int);
 }
 

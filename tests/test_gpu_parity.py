@@ -1,0 +1,208 @@
+"""GPU parity: the library (C++ block manager + CUDA kernels, called through the
+C ABI) against the oracle (naive bookkeeping + float64 loops), on the same
+seeded inputs.
+
+* bookkeeping (slots, copy pairs, block tables, lengths) — bit-exact;
+* pool contents after every copy-on-write copy and append — bit-exact;
+* attention output — max-abs error <= 1e-5 (fp32 pool) or <= 5e-3 (bf16).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import replay as orp
+from paged_kv_cache_253_gb300 import workloads as wls
+
+from gpu_common import assert_pools_equal, run_library, tol
+
+pytestmark = pytest.mark.gpu
+
+D128 = dict(num_q_heads=32, num_kv_heads=8, head_dim=128)
+
+SMALL = [
+    ("tiny", dict()),
+    ("decode", dict(num_seqs=6, min_len=1, max_len=300, **D128)),
+    ("decode", dict(num_seqs=5, min_len=1, max_len=200, num_q_heads=64, num_kv_heads=8,
+                    head_dim=128)),                                     # G = 8
+    ("decode", dict(num_seqs=4, min_len=1, max_len=150, num_q_heads=8, num_kv_heads=8,
+                    head_dim=128)),                                     # G = 1
+    ("decode", dict(num_seqs=4, min_len=1, max_len=150, num_q_heads=10, num_kv_heads=2,
+                    head_dim=128)),                                     # G = 5
+    ("decode", dict(num_seqs=4, min_len=1, max_len=200, num_q_heads=16, num_kv_heads=4,
+                    head_dim=64)),
+    ("decode", dict(num_seqs=3, min_len=1, max_len=200, num_q_heads=8, num_kv_heads=2,
+                    head_dim=256)),
+    ("decode", dict(num_seqs=4, min_len=1, max_len=200, block_size=32, **D128)),
+    ("decode", dict(num_seqs=4, min_len=1, max_len=100, block_size=8, **D128)),   # fp32 path
+    ("decode", dict(num_seqs=4, min_len=1, max_len=100, dtype="f32", **D128)),
+    ("decode", dict(num_seqs=3, min_len=1, max_len=100, num_q_heads=32, num_kv_heads=2,
+                    head_dim=128)),                                     # G = 16
+    ("decode", dict(lengths=[0, 1, 15, 16, 17, 33], **D128)),
+    ("prefix", dict(num_seqs=6, prefix_len=41, suffix_min=1, suffix_max=40, **D128)),
+    ("mixed", dict(num_seqs=24, median=60, min_len=1, max_len=400, prefix_min=20,
+                   prefix_max=90, num_q_heads=64, num_kv_heads=8, head_dim=128)),
+    ("long", dict(num_seqs=2, min_len=3000, max_len=9000, **D128)),
+]
+
+
+def _ids():
+    out = []
+    for name, kw in SMALL:
+        tag = "-".join(f"{k}{v}" for k, v in kw.items() if k not in ("num_q_heads",))
+        out.append(f"{name}-{tag}"[:60])
+    return out
+
+
+def _check(wl, values, seqs=None, threads=1):
+    pool, bm, setup_pairs, step = run_library(wl, values)
+    assert pool.get_error() == 0
+    st = orp.replay(wl, values)
+    # bookkeeping, bit-exact
+    assert setup_pairs == st.setup_pairs
+    assert step.slots.cpu().numpy().tolist() == st.step_slots.tolist()
+    assert [tuple(p) for p in step.pairs.cpu().numpy().tolist()] == st.step_pairs
+    assert np.array_equal(step.block_tables.cpu().numpy(), st.block_tables)
+    assert np.array_equal(step.context_lens.cpu().numpy(), st.context_lens)
+    # pool contents, bit-exact
+    assert_pools_equal(pool, st)
+    # attention
+    ref = orp.attention(wl, values, st, seqs=seqs, threads=threads)
+    got = step.out.double().cpu().numpy()
+    if seqs is not None:
+        got = got[np.asarray(seqs)]
+    err = np.abs(got - ref).max() if ref.size else 0.0
+    assert err <= tol(wl), f"max-abs {err:.3g} > {tol(wl)}"
+    return err, pool, step
+
+
+@pytest.mark.parametrize("name,kw", SMALL, ids=_ids())
+def test_small_parity(name, kw):
+    wl = wls.make_workload(name, **kw)
+    values = wls.generate_values(wl, "cpu")
+    err, pool, step = _check(wl, values)
+    print(f"{name} {kw}: max-abs {err:.3g}")
+
+
+def test_repeated_step_is_idempotent():
+    wl = wls.make_workload("prefix", num_seqs=5, prefix_len=37, suffix_min=0, suffix_max=0,
+                           **D128)
+    values = wls.generate_values(wl, "cpu")
+    pool, bm, _, step = run_library(wl, values)
+    first = step.out.clone()
+    assert step.num_pairs == 4          # every fork but the last copies the partial block
+    for _ in range(3):
+        step.run()
+    torch.cuda.synchronize()
+    assert torch.equal(first, step.out)
+    assert pool.get_error() == 0
+
+
+def test_moving_physical_blocks_leaves_output_unchanged():
+    wl = wls.make_workload("decode", num_seqs=6, min_len=1, max_len=400, **D128)
+    values = wls.generate_values(wl, "cpu")
+    pool, bm, _, step = run_library(wl, values)
+    base = step.out.clone()
+    k, v = pool.export()
+    move = torch.randperm(wl.num_blocks, generator=torch.Generator().manual_seed(5)).cuda()
+    k2, v2 = torch.empty_like(k), torch.empty_like(v)
+    k2[move] = k
+    v2[move] = v
+    pool.import_(k2, v2)
+    t = step.block_tables
+    t2 = torch.where(t >= 0, move[t.clamp(min=0).long()].int(), t).contiguous()
+    out = pool.decode(step.q, t2, step.context_lens, step.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, base)
+    assert pool.get_error() == 0
+
+
+def test_sorted_tables_change_the_output():
+    wl = wls.make_workload("decode", lengths=[40, 70], **D128)
+    values = wls.generate_values(wl, "cpu")
+    pool, bm, _, step = run_library(wl, values)
+    t = step.block_tables.clone()
+    n = (t >= 0).sum(1)
+    for i in range(t.shape[0]):
+        t[i, :n[i]] = t[i, :n[i]].sort(descending=True).values
+    out = pool.decode(step.q, t.contiguous(), step.context_lens, step.scale)
+    torch.cuda.synchronize()
+    assert (out - step.out).abs().max().item() > 1e-3
+
+
+def test_bf16_output_dtype():
+    wl = wls.make_workload("decode", num_seqs=4, min_len=1, max_len=300, **D128)
+    values = wls.generate_values(wl, "cpu")
+    pool, bm, _, step = run_library(wl, values)
+    out16 = pool.decode(step.q, step.block_tables, step.context_lens, step.scale,
+                        out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(out16, step.out.to(torch.bfloat16))
+
+
+def test_device_errors_are_reported_not_faulted():
+    from paged_kv_cache_253_gb300._lib import (PA_ERR_BAD_BLOCK_ID, PA_ERR_BAD_LENGTH,
+                                               PA_ERR_BAD_SLOT, PA_ERR_OVERLAP)
+    wl = wls.make_workload("decode", num_seqs=3, min_len=20, max_len=60, **D128)
+    values = wls.generate_values(wl, "cpu")
+    pool, bm, _, step = run_library(wl, values)
+    assert pool.get_error() == 0
+    bad = step.block_tables.clone()
+    bad[1, 0] = wl.num_blocks + 5
+    pool.decode(step.q, bad, step.context_lens, step.scale)
+    assert pool.get_error() == PA_ERR_BAD_BLOCK_ID
+    assert pool.get_error() == 0                       # cleared by the read
+    long_lens = step.context_lens.clone()
+    long_lens[0] = bad.shape[1] * wl.block_size + 100
+    pool.decode(step.q, step.block_tables, long_lens, step.scale)
+    assert pool.get_error() == PA_ERR_BAD_LENGTH
+    slots = torch.tensor([wl.num_blocks * wl.block_size + 3, -1, 0], dtype=torch.int64,
+                         device="cuda")
+    pool.append_kv(step.new_k, step.new_v, slots)
+    assert pool.get_error() == PA_ERR_BAD_SLOT
+    pairs = torch.tensor([[1, 2], [2, 3]], dtype=torch.int64, device="cuda")
+    pool.copy_blocks(pairs)
+    assert pool.get_error() == PA_ERR_OVERLAP
+    pairs = torch.tensor([[1, wl.num_blocks]], dtype=torch.int64, device="cuda")
+    pool.copy_blocks(pairs)
+    assert pool.get_error() == PA_ERR_BAD_BLOCK_ID
+
+
+def test_copy_blocks_skips_only_conflicting_pairs():
+    wl = wls.make_workload("decode", num_seqs=2, min_len=40, max_len=60, **D128)
+    values = wls.generate_values(wl, "cpu")
+    pool, bm, _, step = run_library(wl, values)
+    k0, v0 = pool.export()
+    pairs = torch.tensor([[0, 5], [7, 9], [9, 11]], dtype=torch.int64, device="cuda")
+    pool.copy_blocks(pairs)
+    torch.cuda.synchronize()
+    k1, v1 = pool.export()
+    torch.cuda.synchronize()
+    assert torch.equal(k1[5], k0[0]) and torch.equal(v1[5], v0[0])
+    assert torch.equal(k1[9], k0[9]) and torch.equal(k1[11], k0[11])   # conflicting: untouched
+    assert pool.get_error() != 0
+
+
+# ---------------------------------------------------------- full sizes ---
+
+FULL = ["decode", "prefix", "long", "mixed"]
+
+
+def _sample(wl, n=10):
+    """Batch entries whose outputs the oracle recomputes: longest, shortest,
+    shared ones, and a seeded spread."""
+    rng = np.random.default_rng(wl.seed)
+    S = wl.num_seqs
+    pick = set(rng.choice(S, size=min(n, S), replace=False).tolist())
+    pick |= {0, S - 1}
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_parity(name):
+    wl = wls.make_workload(name)
+    values = wls.generate_values(wl, "cuda")
+    seqs = _sample(wl)
+    if name == "long":
+        seqs = list(range(wl.num_seqs))
+    err, pool, step = _check(wl, values, seqs=seqs, threads=8)
+    print(f"{name}: max-abs over {len(seqs)} sampled sequences {err:.3g}")
