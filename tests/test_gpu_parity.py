@@ -168,7 +168,9 @@ def test_device_errors_are_reported_not_faulted():
 
 
 def test_copy_blocks_skips_only_conflicting_pairs():
-    wl = wls.make_workload("decode", num_seqs=2, min_len=40, max_len=60, **D128)
+    wl = wls.make_workload("decode", num_seqs=2, min_len=40, max_len=60, pool_factor=4.0,
+                           **D128)
+    assert wl.num_blocks >= 12
     values = wls.generate_values(wl, "cpu")
     pool, bm, _, step = run_library(wl, values)
     k0, v0 = pool.export()
