@@ -151,6 +151,29 @@ int pa_decode(pa_pool *pool, const void *q, int num_seqs, int num_q_heads,
 /* Size the pool's decode workspace for batches up to these bounds. */
 int pa_decode_reserve(pa_pool *pool, int max_seqs, int max_q_heads);
 
+/* Decode without allocating: the same computation, arguments and result as
+ * pa_decode, for callers that cannot let the library call cudaMalloc — a
+ * process whose device memory is owned by another allocator (a framework's
+ * caching allocator that has reserved the GPU, or a fixed memory budget set
+ * by the application), or a serving loop that cannot pay for cudaMalloc's
+ * implicit device-wide synchronisation.  The pages have no counterpart: this
+ * is an interface choice of this library, not part of the method.
+ * The split partials and arrival counters live in a fixed 32 MiB array inside
+ * the library image that every GPU loading the library holds until the
+ * process exits; nothing is allocated or freed by the call (it clears the
+ * counters with cudaMemsetAsync on `stream`).  A batch whose partials do not
+ * fit returns PA_ERR_UNSUPPORTED before launching anything (roughly: up to
+ * 16384 sequences x KV heads at head_dim 128, G 4, on a 152-SM GB300).
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture
+ * begins.  All calls on a device share the one array, which keeps the last
+ * call's contents: calls that overlap on the GPU (other streams, other pools,
+ * other threads) race and give wrong results; serialise them. */
+int pa_decode_noalloc(pa_pool *pool, const void *q, int num_seqs, int num_q_heads,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, float scale, void *out,
+                      pa_dtype out_dtype, void *stream);
+
 /* Synchronize `stream`, then return and clear the first error the pool's
  * kernels recorded since the last call (PA_OK if none). */
 int pa_get_error(pa_pool *pool, void *stream);

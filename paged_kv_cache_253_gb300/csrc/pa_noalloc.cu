@@ -1,0 +1,122 @@
+// pa_decode_noalloc: the decode entry point for callers that must not allocate
+// device memory.
+//
+// pa_decode keeps its split partials and arrival counters in a workspace that
+// the pool grows with cudaMalloc on demand.  Some callers cannot let a library
+// do that: processes whose device memory is already owned by another allocator
+// (a framework's caching allocator that has reserved the GPU, or a fixed
+// memory budget the application enforces), and serving loops that cannot pay
+// for cudaMalloc's implicit device-wide synchronisation.  This variant runs the
+// same decode kernel with its scratch in a fixed array that is part of the
+// library image itself, so the call never allocates.
+//
+// The array is a file-scope __device__ object: every GPU that loads this
+// library holds its kScratchBytes until the process exits.  Host code cannot
+// use the array's name as a device address; the address is looked up once per
+// device with cudaGetSymbolAddress (on the first call made on that device) and
+// cached.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = size_t{32} << 20;   // 32 MiB per device
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+size_t round_up256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Device address of this device's copy of g_decode_scratch (looked up once,
+// with that device current).
+int scratch_address(int device, void** out) {
+    if (device < 0 || device >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[device]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess || !p) {
+            cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
+        g_scratch_ptr[device] = p;
+    }
+    *out = g_scratch_ptr[device];
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_decode_noalloc(pa_pool* pool, const void* q, int num_seqs, int num_q_heads,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, float scale, void* out,
+                                 pa_dtype out_dtype, void* stream) {
+    if (!pool || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % pool->kv_heads != 0 || num_q_heads / pool->kv_heads > 16)
+        return PA_ERR_UNSUPPORTED;
+    if (out_dtype != PA_F32 && out_dtype != PA_BF16) return PA_ERR_DTYPE;
+    if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!q || !block_tables || !context_lens || !out || max_blocks_per_seq == 0)
+        return PA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(q) % 16 != 0) return PA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_blocks_per_seq) * pool->block_size > (int64_t{1} << 30))
+        return PA_ERR_UNSUPPORTED;
+
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) return PA_ERR_CUDA;
+    if (prev != pool->device && cudaSetDevice(pool->device) != cudaSuccess) return PA_ERR_CUDA;
+    struct Restore {
+        int dev, was;
+        ~Restore() { if (dev != was) cudaSetDevice(was); }
+    } restore{pool->device, prev};
+
+    const int Hkv = pool->kv_heads, D = pool->head_dim;
+    const int G = num_q_heads / Hkv;
+    pa_detail::DecodePlan plan;
+    int rc = pa_detail::plan_decode(pool, num_seqs, num_q_heads, max_blocks_per_seq, &plan);
+    if (rc != PA_OK) return rc;
+    const size_t counters = round_up256(static_cast<size_t>(num_seqs) * Hkv * sizeof(int));
+    const size_t acc = round_up256(plan.max_items * G * D * sizeof(float));
+    const size_t ml = round_up256(plan.max_items * G * 2 * sizeof(float));
+    if (counters + acc + ml > kScratchBytes) return PA_ERR_UNSUPPORTED;   // batch too large
+
+    void* base = nullptr;
+    rc = scratch_address(pool->device, &base);
+    if (rc != PA_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the arrival counters must start at zero; the array keeps the previous call's bytes
+    if (cudaMemsetAsync(base, 0, counters, st) != cudaSuccess) return PA_ERR_CUDA;
+
+    DecodeParams p{};
+    p.q = q;
+    p.k = pool->k;
+    p.v = pool->v;
+    p.tables = block_tables;
+    p.lens = context_lens;
+    p.out = out;
+    p.counters = static_cast<int*>(base);
+    p.part_acc = reinterpret_cast<float*>(static_cast<char*>(base) + counters);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(base) + counters + acc);
+    p.err = pool->err;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.S = num_seqs;
+    p.Hq = num_q_heads;
+    p.Hkv = Hkv;
+    p.G = G;
+    p.D = D;
+    p.B = pool->block_size;
+    p.num_blocks = pool->num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.out_bf16 = out_dtype == PA_BF16;
+    return pa_detail::launch_decode(plan, p, st);
+}
