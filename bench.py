@@ -165,10 +165,12 @@ def _oracle_sample(wl, values, target_s=12.0, threads=None):
     st = orp.replay(wl, values)
     lens = st.context_lens
     order = np.random.default_rng(wl.seed).permutation(wl.num_seqs)
-    # grow the sample until it takes about target_s
+    # grow the sample until it takes about target_s (cycling over the batch)
     n, spent, done_tok, done_seq, calls = 1, 0.0, 0, 0, 0
     pos = 0
-    while spent < target_s and pos < len(order):
+    while spent < target_s:
+        if pos >= len(order):
+            pos = 0
         pick = order[pos:pos + n]
         t0 = time.perf_counter()
         orp.attention(wl, values, st, seqs=pick, threads=threads)
@@ -178,11 +180,11 @@ def _oracle_sample(wl, values, target_s=12.0, threads=None):
         done_seq += len(pick)
         pos += len(pick)
         calls += 1
-        n = max(1, min(len(order) - pos, int(n * 2)))
+        n = max(1, min(len(order), int(n * 2)))
     per_tok = wl.num_kv_heads * wl.head_dim * 2 * wl.elem_bytes
     gbs = done_tok * per_tok / spent / 1e9
-    desc = (f"{done_seq} of {wl.num_seqs} sequences ({done_tok} cached tokens) of the same "
-            f"workload, float64 oracle, {threads} threads, {spent:.1f} s")
+    desc = (f"{done_seq} sequence decodes ({done_tok} cached tokens) drawn from the same "
+            f"{wl.num_seqs}-sequence batch, float64 oracle, {threads} threads, {spent:.1f} s")
     return gbs, done_seq / spent, threads, desc
 
 
@@ -247,29 +249,30 @@ def run_ours(args):
     if pool.get_error():
         raise RuntimeError("device error during warm-up")
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    def timed(body, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for i in range(n):
+            flush.fill_(i & 0xFF)                       # evict L2 between steps
+            evs[i][0].record(stream)
+            body()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def decode_only():
+        pool.decode(step.q, step.block_tables, step.context_lens, step.scale, out=step.out)
+
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = api.launch_count()
     with Clocks(local) as clk:
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)                       # evict L2 between steps
-            a, b, c = ev[i]
-            a.record(stream)
-            if step.num_pairs:
-                pool.copy_blocks(step.pairs)
-            pool.append_kv(step.new_k, step.new_v, step.slots)
-            b.record(stream)
-            pool.decode(step.q, step.block_tables, step.context_lens, step.scale, out=step.out)
-            c.record(stream)
-        torch.cuda.synchronize()
+        step_ms = timed(step.run, args.steps)
     launches = api.launch_count() - launches0
+    dec_ms = timed(decode_only, args.steps)             # the decode call alone, for the roofline
     if dist:
         dist.barrier()
-    step_ms = [a.elapsed_time(c) for a, b, c in ev]
-    dec_ms = [b.elapsed_time(c) for a, b, c in ev]
     ms = sum(step_ms) / len(step_ms)
     dms = sum(dec_ms) / len(dec_ms)
     if dist:
@@ -323,6 +326,7 @@ def run_ours(args):
         "hbm_frac_of_" + peak_kind: round(value / world / peak, 4),
         "tokens_per_s": round(world * wl.num_seqs / (ms * 1e-3), 1),
         "decode_ms": round(dms, 5),
+        "launches_per_step": step.launches() + 1,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": _traffic_from_profile(), "kernel": "decode (pa_decode)",

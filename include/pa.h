@@ -70,7 +70,8 @@ enum {
  * Cache Into Fixed Blocks": a block holds a fixed number of positions; its
  * bytes depend on heads, head width and dtype).  One pool holds one layer.
  * Allocates and zeroes K and V on the current CUDA device (synchronously).
- * Limits: block_size in [1, 1024]; head_dim in [1, 256]; kv_heads >= 1.
+ * Limits: block_size in [1, 1024]; head_dim in [4, 256], a multiple of 4;
+ * kv_heads >= 1.
  * On success *out owns the pool; release it with pa_pool_destroy. */
 int pa_pool_create(int num_blocks, int block_size, int kv_heads, int head_dim,
                    pa_dtype dtype, pa_pool **out);
@@ -132,7 +133,8 @@ int pa_copy_blocks(pa_pool *pool, const int64_t *pairs, int num_pairs, void *str
  *                 PA_ERR_BAD_LENGTH and is clamped
  *   out           device [S][num_q_heads][head_dim] of out_dtype
  * Keys/values are read once per (sequence, KV head) for all G query heads;
- * long contexts are split over block ranges and merged by log-sum-exp.
+ * long contexts are split over block ranges and merged by log-sum-exp in a
+ * second kernel (two launches per call).
  * Arithmetic: bf16 pools use bf16 tensor-core products with fp32
  * accumulation and fp32 softmax (the probabilities enter the value product
  * as a bf16 high part plus a bf16 low part); f32 pools use fp32 CUDA cores.

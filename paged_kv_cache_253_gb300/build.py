@@ -42,7 +42,8 @@ def _compile(src, verbose_ptxas=False):
     obj = os.path.join(OUT_DIR, name + ".o")
     if src.endswith(".cu"):
         cmd = [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-               "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+               "-I", INCLUDE, "-I", CSRC, *os.environ.get("PA_NVCC_FLAGS", "").split(),
+               "-c", src, "-o", obj]
         if verbose_ptxas:
             cmd.insert(1, "-Xptxas=-v")
     else:

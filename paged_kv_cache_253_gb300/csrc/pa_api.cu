@@ -38,10 +38,11 @@ struct DeviceGuard {
 
 size_t elem_size(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
 
-// Workspace: [counters S*Hkv ints, 256-aligned][part_acc][part_ml]
+// Workspace: [header: ticket + schedule, 256-aligned][part_acc][part_ml]
 size_t workspace_bytes(const pa_detail::DecodePlan& plan, int S, int Hkv, int G, int D,
                        size_t* counters_bytes) {
-    const size_t cb = round256(static_cast<size_t>(S) * Hkv * sizeof(int));
+    (void)Hkv;
+    const size_t cb = decode_header_bytes(S);
     const size_t acc = round256(plan.max_items * G * D * sizeof(float));
     const size_t ml = round256(plan.max_items * G * 2 * sizeof(float));
     if (counters_bytes) *counters_bytes = cb;
@@ -49,7 +50,7 @@ size_t workspace_bytes(const pa_detail::DecodePlan& plan, int S, int Hkv, int G,
 }
 
 // Grow the pool's workspace to at least `bytes`; new memory is zeroed (the
-// arrival counters must start at zero and are reset by the kernel after use).
+// work ticket must start at zero; the kernel resets it after use).
 int ensure_workspace(pa_pool* pool, size_t bytes) {
     if (pool->ws_bytes >= bytes) return PA_OK;
     if (pool->ws) {
@@ -81,7 +82,7 @@ extern "C" {
 int pa_pool_create(int num_blocks, int block_size, int kv_heads, int head_dim, pa_dtype dtype,
                    pa_pool** out) {
     if (!out || num_blocks <= 0 || block_size <= 0 || block_size > 1024 || kv_heads <= 0 ||
-        head_dim <= 0 || head_dim > 256)
+        head_dim <= 0 || head_dim > 256 || head_dim % 4 != 0)
         return PA_ERR_INVALID_ARG;
     if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
     *out = nullptr;
@@ -249,7 +250,8 @@ int pa_decode(pa_pool* pool, const void* q, int num_seqs, int num_q_heads,
     p.tables = block_tables;
     p.lens = context_lens;
     p.out = out;
-    p.counters = static_cast<int*>(pool->ws);
+    p.ticket = static_cast<int*>(pool->ws);
+    p.sched = p.ticket + 4;
     p.part_acc = reinterpret_cast<float*>(static_cast<char*>(pool->ws) + cb);
     p.part_ml = reinterpret_cast<float*>(
         static_cast<char*>(pool->ws) + cb + round256(plan.max_items * G * pool->head_dim * sizeof(float)));

@@ -40,9 +40,29 @@
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
+// Tuning knobs (compile-time; the defaults are the measured best on GB300).
+#ifndef PA_ITEMS_PER_CTA
+#define PA_ITEMS_PER_CTA 4      // target work items per resident CTA
+#endif
+#ifndef PA_PREFETCH
+#define PA_PREFETCH 0           // stream an item's K/V tiles into L2 when it starts
+#endif                          // (measured slower on GB300; kept as an option)
+#ifndef PA_DYNAMIC
+#define PA_DYNAMIC 1            // CTAs take items from a global counter, not round-robin
+#endif
+#ifndef PA_WARPS
+#define PA_WARPS 4              // warps per CTA sharing one item
+#endif
+#ifndef PA_MIN_CTAS
+#define PA_MIN_CTAS 3           // resident CTAs per SM the register budget aims at
+#endif
+#ifndef PA_STAGES
+#define PA_STAGES 0             // cp.async ring depth per warp (0/1: direct register loads)
+#endif
+
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = PA_WARPS;
 constexpr int kThreads = kWarps * 32;
 
 using pa_dev::record_error;
@@ -124,6 +144,40 @@ __device__ __forceinline__ int find_seq(const int* s_start, int S, int item) {
     return lo;
 }
 
+// Next item for this CTA.  Dynamic: every CTA starts at blockIdx.x and then
+// takes gridDim.x + (a global ticket), so CTAs that finish early keep working
+// and the launch ends about one item after the average CTA.  The ticket
+// counter lives in the workspace header.
+__device__ __forceinline__ int next_item(const DecodeParams& p, int item, int* s_next) {
+#if PA_DYNAMIC
+    if (threadIdx.x == 0) *s_next = static_cast<int>(gridDim.x) + atomicAdd(p.ticket, 1);
+    __syncthreads();
+    const int it = *s_next;
+    __syncthreads();
+    return it;
+#else
+    (void)p;
+    (void)s_next;
+    return item + static_cast<int>(gridDim.x);
+#endif
+}
+
+// The last CTA to stop resets the ticket counters for the next launch.  Every
+// other CTA has taken its last ticket before it counts itself out, so nothing
+// reads the counters after the reset.
+__device__ __forceinline__ void retire_cta(const DecodeParams& p) {
+#if PA_DYNAMIC
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.ticket + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+            p.ticket[0] = 0;
+            p.ticket[1] = 0;
+            __threadfence();
+        }
+    }
+#endif
+}
+
 // --------------------------------------------------------- item results ---
 
 __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, float x) {
@@ -134,13 +188,15 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, flo
 }
 
 // res_m/res_l: [G] (log2-domain running max, sum); res_acc: [G][stride].
+// A sequence with one partition gets its normalised output here; otherwise the
+// item's partial goes to the workspace for the merge kernel.
 __device__ void finish_item(const DecodeParams& p, int item, int s, int h, int nP,
-                            int seq_item0, const float* res_m, const float* res_l,
-                            const float* res_acc, int stride, int* s_flag) {
+                            const float* res_m, const float* res_l, const float* res_acc,
+                            int stride) {
     const int tid = threadIdx.x;
     const int GD = p.G * p.D;
-    const size_t out0 = (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G) * p.D;
     if (nP == 1) {
+        const size_t out0 = (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G) * p.D;
         for (int idx = tid; idx < GD; idx += kThreads) {
             const int n = idx / p.D, d = idx - n * p.D;
             const float l = res_l[n];
@@ -157,33 +213,17 @@ __device__ void finish_item(const DecodeParams& p, int item, int s, int h, int n
         p.part_ml[(static_cast<size_t>(item) * p.G + tid) * 2 + 0] = res_m[tid];
         p.part_ml[(static_cast<size_t>(item) * p.G + tid) * 2 + 1] = res_l[tid];
     }
-    __threadfence();
-    __syncthreads();
-    int* counter = p.counters + static_cast<size_t>(s) * p.Hkv + h;
-    if (tid == 0) *s_flag = (atomicAdd(counter, 1) == nP - 1);
-    __syncthreads();
-    if (!*s_flag) return;
-    __threadfence();
-    for (int idx = tid; idx < GD; idx += kThreads) {
-        const int n = idx / p.D;
-        float M = -INFINITY;
-        for (int q = 0; q < nP; ++q) {
-            const size_t it = static_cast<size_t>(seq_item0) + static_cast<size_t>(q) * p.Hkv + h;
-            M = fmaxf(M, __ldcg(p.part_ml + (it * p.G + n) * 2));
-        }
-        float acc = 0.f, l = 0.f;
-        if (M != -INFINITY) {
-            for (int q = 0; q < nP; ++q) {
-                const size_t it = static_cast<size_t>(seq_item0) + static_cast<size_t>(q) * p.Hkv + h;
-                const float mq = __ldcg(p.part_ml + (it * p.G + n) * 2);
-                const float f = pa_dev::ex2(mq - M);
-                l += f * __ldcg(p.part_ml + (it * p.G + n) * 2 + 1);
-                acc += f * __ldcg(p.part_acc + it * GD + idx);
-            }
-        }
-        store_out(p, out0 + idx, l > 0.f ? acc / l : 0.f);
+}
+
+// CTA 0 publishes the schedule (PT, item count, first item of each sequence)
+// for the merge kernel.
+__device__ void publish_schedule(const DecodeParams& p, const Sched& sc, const int* s_start) {
+    if (blockIdx.x != 0) return;
+    if (threadIdx.x == 0) {
+        p.sched[0] = sc.PT;
+        p.sched[1] = sc.total_items;
     }
-    if (tid == 0) *counter = 0;
+    for (int i = threadIdx.x; i <= p.S; i += kThreads) p.sched[2 + i] = s_start[i];
 }
 
 // ------------------------------------------------ bf16 tensor-core item ---
@@ -197,45 +237,216 @@ __device__ void finish_item(const DecodeParams& p, int item, int s, int h, int n
 //   c, c+4, ... of each row; chunk elements 0-1 / 2-3 feed the low / high k
 //   half of one k-step and elements 4-7 the next k-step, identically for K
 //   and Q, so every product q[d]*k[d] is formed exactly once.
+
+template <int D>
+struct WarpAcc {
+    static constexpr int NJ = D / 32;     // 16-byte chunks per thread per row
+    static constexpr int NT = D / 16;     // m-tiles of the value product
+    uint4 qf[NJ];                         // Q^T B-fragments (bf16 pairs)
+    float o[NT][4];                       // O^T accumulators: rows d, columns heads 2c, 2c+1
+    float m0, m1, l0, l1;                 // running max / sum (log2 units), heads 2c, 2c+1
+};
+
+// One 16-token tile: scores, online-softmax update, value product.
+template <int D>
+__device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D / 32],
+                                            const uint4 (&k1)[D / 32], uint2 (&v0)[D / 16],
+                                            uint2 (&v1)[D / 16], int nvalid, float sl, int r0,
+                                            int r1, int c) {
+    constexpr int NJ = D / 32, NT = D / 16;
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        pa_dev::mma_bf16_16816(sc, k0[j].x, k1[j].x, k0[j].y, k1[j].y, a.qf[j].x, a.qf[j].y);
+        pa_dev::mma_bf16_16816(sc, k0[j].z, k1[j].z, k0[j].w, k1[j].w, a.qf[j].z, a.qf[j].w);
+    }
+    float x0 = sc[0] * sl, x1 = sc[1] * sl, x2 = sc[2] * sl, x3 = sc[3] * sl;
+    if (nvalid < 16) {                        // partly filled last tile
+        if (r0 >= nvalid) x0 = x1 = -INFINITY;
+        if (r1 >= nvalid) x2 = x3 = -INFINITY;
+        const uint32_t mlo = (4 * c < nvalid ? 0x0000ffffu : 0u) |
+                             (4 * c + 1 < nvalid ? 0xffff0000u : 0u);
+        const uint32_t mhi = (4 * c + 2 < nvalid ? 0x0000ffffu : 0u) |
+                             (4 * c + 3 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            v0[t].x &= mlo; v0[t].y &= mhi;
+            v1[t].x &= mlo; v1[t].y &= mhi;
+        }
+    }
+    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(a.m0, mx0), mn1 = fmaxf(a.m1, mx1);
+    const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float cr0 = pa_dev::ex2(a.m0 - ms0), cr1 = pa_dev::ex2(a.m1 - ms1);
+    const float p0 = pa_dev::ex2(x0 - ms0), p1 = pa_dev::ex2(x1 - ms1);
+    const float p2 = pa_dev::ex2(x2 - ms0), p3 = pa_dev::ex2(x3 - ms1);
+    a.l0 = a.l0 * cr0 + (p0 + p2);
+    a.l1 = a.l1 * cr1 + (p1 + p3);
+    a.m0 = mn0;
+    a.m1 = mn1;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        a.o[t][0] *= cr0; a.o[t][1] *= cr1;
+        a.o[t][2] *= cr0; a.o[t][3] *= cr1;
+    }
+    const uint32_t h01 = pa_dev::pack_bf16(p0, p1), h23 = pa_dev::pack_bf16(p2, p3);
+    const uint32_t e01 = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(h01), p1 - pa_dev::bf16_hi(h01));
+    const uint32_t e23 = pa_dev::pack_bf16(p2 - pa_dev::bf16_lo(h23), p3 - pa_dev::bf16_hi(h23));
+    const uint32_t bh0 = pa_dev::movmatrix_trans(h01), bh1 = pa_dev::movmatrix_trans(h23);
+    const uint32_t be0 = pa_dev::movmatrix_trans(e01), be1 = pa_dev::movmatrix_trans(e23);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, bh0, bh1);
+        pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, be0, be1);
+    }
+}
+
+#if PA_STAGES > 1
+__device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+#endif
+
+// The warp's share of one item: blocks lb0 + warp + kWarps*i of the
+// partition, each block cut into 16-token units.  With PA_STAGES > 1 every
+// unit's K tile (16 rows) and V^T tile (D rows of 16 tokens) are copied into
+// a per-warp ring of shared-memory stages with cp.async, PA_STAGES - 1 units
+// ahead of the unit being computed, so each warp keeps several tiles in
+// flight.  K rows are stored with 16-byte chunk c of odd rows at c ^ 4, which
+// makes the fragment reads below bank-conflict free.
 template <int D>
 __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, int tok0,
-                                          int tok1, int L, float* sm_o, float* sm_m,
-                                          float* sm_l) {
-    constexpr int NJ = D / 32;        // 16-byte chunks per thread per row
-    constexpr int NT = D / 16;        // m-tiles of the value product
-    constexpr int OS = D + 4;         // padded row stride of the merge buffer
+                                          int tok1, int L, unsigned char* ring, float* sm_o,
+                                          float* sm_m, float* sm_l) {
+    constexpr int NJ = D / 32, NT = D / 16;
+    constexpr int OS = D + 4;             // padded row stride of the merge buffer
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
-    const int B = p.B;
+    const int B = p.B, nsub = B / 16;
 
-    uint4 qf[NJ];
+    WarpAcc<D> a;
     {
         const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
                                (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G + g) * D;
 #pragma unroll
         for (int j = 0; j < NJ; ++j)
-            qf[j] = g < p.G ? __ldg(reinterpret_cast<const uint4*>(qrow + (4 * j + c) * 8))
-                            : make_uint4(0u, 0u, 0u, 0u);
+            a.qf[j] = g < p.G ? __ldg(reinterpret_cast<const uint4*>(qrow + (4 * j + c) * 8))
+                              : make_uint4(0u, 0u, 0u, 0u);
     }
-    float o[NT][4];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    for (int t = 0; t < NT; ++t) a.o[t][0] = a.o[t][1] = a.o[t][2] = a.o[t][3] = 0.f;
+    a.m0 = a.m1 = -INFINITY;
+    a.l0 = a.l1 = 0.f;
     const float sl = p.scale_log2;
     const int r0 = 4 * (g >> 1) + (g & 1), r1 = r0 + 2;
     const int lb0 = tok0 / B, lb1 = (tok1 + B - 1) / B;
     const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
     const uint16_t* kpool = static_cast<const uint16_t*>(p.k);
     const uint16_t* vpool = static_cast<const uint16_t*>(p.v);
+    const size_t tile_elems = static_cast<size_t>(B) * D;
+    const int nblk = lb1 > lb0 + warp ? (lb1 - lb0 - warp + kWarps - 1) / kWarps : 0;
 
-    for (int lb = lb0 + warp; lb < lb1; lb += kWarps) {
-        const int phys = __ldg(table + lb);
+#if PA_STAGES > 1
+    constexpr int S = PA_STAGES;
+    constexpr int UNIT = 64 * D;          // bytes per stage: K 16 x D + V^T D x 16, bf16
+    const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+    const int nunits = nblk * nsub;
+    int my_phys = -1;
+    unsigned valid = 0;                   // bit (u % S): stage holds unit u
+    auto issue = [&](int u) {
+        const int i = u / nsub, sub = u - i * nsub;
+        if (sub == 0 && (i & 31) == 0) {
+            const int mine = lb0 + warp + kWarps * (i + lane);
+            my_phys = mine < lb1 ? __ldg(table + mine) : -1;
+        }
+        const int phys = __shfl_sync(0xffffffffu, my_phys, i & 31);
+        const int lb = lb0 + warp + kWarps * i;
+        const int nv = L - (lb * B + sub * 16);
+        const int st = u % S;
+        valid &= ~(1u << st);
+        if (phys < 0 || phys >= p.num_blocks) {
+            if (lane == 0 && nv > 0) record_error(p.err, PA_ERR_BAD_BLOCK_ID);
+        } else if (nv > 0) {
+            const size_t tile = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems;
+            const uint16_t* kg = kpool + tile + static_cast<size_t>(sub) * 16 * D;
+            const uint16_t* vg = vpool + tile + sub * 16;
+            const uint32_t ks = ring_s + st * UNIT;
+            const uint32_t vs = ks + 32 * D;
+#pragma unroll
+            for (int q = lane; q < 2 * D; q += 32) {          // K: 16 rows x D/8 chunks
+                const int r = q / (D / 8), ch = q - r * (D / 8);
+                cp_async16(ks + r * (2 * D) + ((ch ^ ((r & 1) << 2)) << 4), kg + r * D + ch * 8);
+            }
+#pragma unroll
+            for (int q = lane; q < 2 * D; q += 32) {          // V^T: D rows x 2 chunks
+                const int d = q >> 1, half = q & 1;
+                cp_async16(vs + d * 32 + half * 16, vg + static_cast<size_t>(d) * B + half * 8);
+            }
+            valid |= 1u << st;
+        }
+        cp_async_commit();
+    };
+    for (int u = 0; u < S - 1; ++u) {
+        if (u < nunits) issue(u);
+        else cp_async_commit();
+    }
+    for (int u = 0; u < nunits; ++u) {
+        if (u + S - 1 < nunits) issue(u + S - 1);
+        else cp_async_commit();
+        cp_async_wait<S - 1>();
+        __syncwarp();
+        const int st = u % S;
+        const int i = u / nsub, sub = u - i * nsub;
+        const int nvalid = min(16, L - ((lb0 + warp + kWarps * i) * B + sub * 16));
+        if ((valid >> st) & 1u) {
+            const unsigned char* ks = ring + st * UNIT;
+            const unsigned char* vs = ks + 32 * D;
+            uint4 k0[NJ], k1[NJ];
+            uint2 v0[NT], v1[NT];
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int ch = 4 * j + c;
+                k0[j] = *reinterpret_cast<const uint4*>(ks + r0 * (2 * D) + ((ch ^ ((r0 & 1) << 2)) << 4));
+                k1[j] = *reinterpret_cast<const uint4*>(ks + r1 * (2 * D) + ((ch ^ ((r1 & 1) << 2)) << 4));
+            }
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                v0[t] = *reinterpret_cast<const uint2*>(vs + (16 * t + g) * 32 + 8 * c);
+                v1[t] = *reinterpret_cast<const uint2*>(vs + (16 * t + g + 8) * 32 + 8 * c);
+            }
+            tile_update<D>(a, k0, k1, v0, v1, nvalid, sl, r0, r1, c);
+        }
+        __syncwarp();
+    }
+    cp_async_wait<0>();
+#else
+    int my_phys = -1;
+    for (int i = 0; i < nblk; ++i) {
+        const int lb = lb0 + warp + kWarps * i;
+        if ((i & 31) == 0) {
+            const int mine = lb + lane * kWarps;
+            my_phys = mine < lb1 ? __ldg(table + mine) : -1;
+        }
+        const int phys = __shfl_sync(0xffffffffu, my_phys, i & 31);
         if (phys < 0 || phys >= p.num_blocks) {
             if (lane == 0) record_error(p.err, PA_ERR_BAD_BLOCK_ID);
             continue;
         }
-        const size_t tile = (static_cast<size_t>(phys) * p.Hkv + h) * static_cast<size_t>(B) * D;
-        for (int sub = 0; sub * 16 < B; ++sub) {
+        const size_t tile = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems;
+        for (int sub = 0; sub < nsub; ++sub) {
             const int nvalid = min(16, L - (lb * B + sub * 16));
             if (nvalid <= 0) break;
             const uint16_t* kt = kpool + tile + static_cast<size_t>(sub) * 16 * D;
@@ -252,86 +463,58 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
                 v0[t] = pa_dev::ld_stream8(vt + static_cast<size_t>(16 * t + g) * B);
                 v1[t] = pa_dev::ld_stream8(vt + static_cast<size_t>(16 * t + g + 8) * B);
             }
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                pa_dev::mma_bf16_16816(sc, k0[j].x, k1[j].x, k0[j].y, k1[j].y, qf[j].x, qf[j].y);
-                pa_dev::mma_bf16_16816(sc, k0[j].z, k1[j].z, k0[j].w, k1[j].w, qf[j].z, qf[j].w);
-            }
-            float x0 = sc[0] * sl, x1 = sc[1] * sl, x2 = sc[2] * sl, x3 = sc[3] * sl;
-            if (nvalid < 16) {                        // partly filled last tile
-                if (r0 >= nvalid) x0 = x1 = -INFINITY;
-                if (r1 >= nvalid) x2 = x3 = -INFINITY;
-                const uint32_t mlo = (4 * c < nvalid ? 0x0000ffffu : 0u) |
-                                     (4 * c + 1 < nvalid ? 0xffff0000u : 0u);
-                const uint32_t mhi = (4 * c + 2 < nvalid ? 0x0000ffffu : 0u) |
-                                     (4 * c + 3 < nvalid ? 0xffff0000u : 0u);
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    v0[t].x &= mlo; v0[t].y &= mhi;
-                    v1[t].x &= mlo; v1[t].y &= mhi;
-                }
-            }
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
-            const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float cr0 = pa_dev::ex2(m0 - ms0), cr1 = pa_dev::ex2(m1 - ms1);
-            const float p0 = pa_dev::ex2(x0 - ms0), p1 = pa_dev::ex2(x1 - ms1);
-            const float p2 = pa_dev::ex2(x2 - ms0), p3 = pa_dev::ex2(x3 - ms1);
-            l0 = l0 * cr0 + (p0 + p2);
-            l1 = l1 * cr1 + (p1 + p3);
-            m0 = mn0;
-            m1 = mn1;
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                o[t][0] *= cr0; o[t][1] *= cr1;
-                o[t][2] *= cr0; o[t][3] *= cr1;
-            }
-            const uint32_t h01 = pa_dev::pack_bf16(p0, p1), h23 = pa_dev::pack_bf16(p2, p3);
-            const uint32_t e01 = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(h01), p1 - pa_dev::bf16_hi(h01));
-            const uint32_t e23 = pa_dev::pack_bf16(p2 - pa_dev::bf16_lo(h23), p3 - pa_dev::bf16_hi(h23));
-            const uint32_t bh0 = pa_dev::movmatrix_trans(h01), bh1 = pa_dev::movmatrix_trans(h23);
-            const uint32_t be0 = pa_dev::movmatrix_trans(e01), be1 = pa_dev::movmatrix_trans(e23);
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                pa_dev::mma_bf16_16816(o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, bh0, bh1);
-                pa_dev::mma_bf16_16816(o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, be0, be1);
-            }
+            tile_update<D>(a, k0, k1, v0, v1, nvalid, sl, r0, r1, c);
         }
     }
+#endif
+    float l0 = a.l0, l1 = a.l1;
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
+#if PA_STAGES > 1
+    __syncthreads();                      // every warp is done with its ring: the merge buffer aliases it
+#endif
     float* mo = sm_o + warp * 8 * OS;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        mo[(2 * c) * OS + 16 * t + g] = o[t][0];
-        mo[(2 * c + 1) * OS + 16 * t + g] = o[t][1];
-        mo[(2 * c) * OS + 16 * t + g + 8] = o[t][2];
-        mo[(2 * c + 1) * OS + 16 * t + g + 8] = o[t][3];
+        mo[(2 * c) * OS + 16 * t + g] = a.o[t][0];
+        mo[(2 * c + 1) * OS + 16 * t + g] = a.o[t][1];
+        mo[(2 * c) * OS + 16 * t + g + 8] = a.o[t][2];
+        mo[(2 * c + 1) * OS + 16 * t + g + 8] = a.o[t][3];
     }
     if (g == 0) {
-        sm_m[warp * 8 + 2 * c] = m0;
-        sm_m[warp * 8 + 2 * c + 1] = m1;
+        sm_m[warp * 8 + 2 * c] = a.m0;
+        sm_m[warp * 8 + 2 * c + 1] = a.m1;
         sm_l[warp * 8 + 2 * c] = l0;
         sm_l[warp * 8 + 2 * c + 1] = l1;
     }
 }
 
+// Bytes at the front of the fast kernel's shared memory: the cp.async rings
+// of all warps, which the merge buffer reuses between items.
+__host__ __device__ constexpr size_t fast_front_bytes(int D) {
+    return PA_STAGES > 1
+               ? (static_cast<size_t>(kWarps) * PA_STAGES * 64 * D >
+                          static_cast<size_t>(kWarps) * 8 * (D + 4) * 4
+                      ? static_cast<size_t>(kWarps) * PA_STAGES * 64 * D
+                      : static_cast<size_t>(kWarps) * 8 * (D + 4) * 4)
+               : static_cast<size_t>(kWarps) * 8 * (D + 4) * 4;
+}
+
+__device__ __forceinline__ size_t warp_ring_offset(int D) {
+    return static_cast<size_t>(threadIdx.x >> 5) * PA_STAGES * 64 * D;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 3) decode_fast_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, PA_MIN_CTAS) decode_fast_kernel(const DecodeParams p) {
     constexpr int OS = D + 4;
     extern __shared__ __align__(16) unsigned char smem_raw[];
+    // [ring | merge buffer (aliases the ring when there is one)][m, l, ...][s_start]
+    unsigned char* ring = smem_raw;
     float* sm_o = reinterpret_cast<float*>(smem_raw);        // [kWarps][8][OS]
-    float* sm_m = sm_o + kWarps * 8 * OS;                     // [kWarps][8]
+    float* sm_m = reinterpret_cast<float*>(smem_raw + fast_front_bytes(D));   // [kWarps][8]
     float* sm_l = sm_m + kWarps * 8;                          // [kWarps][8]
     float* res_m = sm_l + kWarps * 8;                         // [8]
     float* res_l = res_m + 8;                                 // [8]
@@ -339,15 +522,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fast_kernel(const DecodePa
     int* s_flag = reinterpret_cast<int*>(s_red + kWarps);
     int* s_start = s_flag + 4;                                // [S + 1]
 
+    pa_dev::wait_prior_grid();
     const Sched sc = build_schedule(p, s_start, s_red);
-    for (int item = blockIdx.x; item < sc.total_items; item += gridDim.x) {
+    publish_schedule(p, sc, s_start);
+    for (int item = blockIdx.x; item < sc.total_items; item = next_item(p, item, s_flag + 1)) {
         const int s = find_seq(s_start, p.S, item);
         const int local = item - s_start[s];
         const int part = local / p.Hkv, h = local - part * p.Hkv;
         const int L = seq_len(p, s, false);
         const int nP = max(1, (L + sc.PT - 1) / sc.PT);
         const int tok0 = part * sc.PT, tok1 = min(L, tok0 + sc.PT);
-        fast_item<D>(p, s, h, tok0, tok1, L, sm_o, sm_m, sm_l);
+        fast_item<D>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
         __syncthreads();
         // merge the warps' softmax states (in place into warp 0's buffer)
         for (int idx = threadIdx.x; idx < p.G * D; idx += kThreads) {
@@ -371,9 +556,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fast_kernel(const DecodePa
             }
         }
         __syncthreads();
-        finish_item(p, item, s, h, nP, s_start[s], res_m, res_l, sm_o, OS, s_flag);
+        finish_item(p, item, s, h, nP, res_m, res_l, sm_o, OS);
         __syncthreads();
     }
+    pa_dev::allow_next_grid();
+    retire_cta(p);
 }
 
 // ------------------------------------------------ fp32 CUDA-core item ---
@@ -410,8 +597,10 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(const DecodePar
     const E* q = static_cast<const E*>(p.q);
     const E* kp = static_cast<const E*>(p.k);
     const E* vp = static_cast<const E*>(p.v);
+    pa_dev::wait_prior_grid();
     const Sched sched = build_schedule(p, s_start, s_red);
-    for (int item = blockIdx.x; item < sched.total_items; item += gridDim.x) {
+    publish_schedule(p, sched, s_start);
+    for (int item = blockIdx.x; item < sched.total_items; item = next_item(p, item, s_flag + 1)) {
         const int s = find_seq(s_start, p.S, item);
         const int local = item - s_start[s];
         const int part = local / p.Hkv, h = local - part * p.Hkv;
@@ -471,13 +660,76 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(const DecodePar
             res[n * OS + d] = acc;
         }
         __syncthreads();
-        finish_item(p, item, s, h, nP, s_start[s], res_m, res_l, res, OS, s_flag);
+        finish_item(p, item, s, h, nP, res_m, res_l, res, OS);
         __syncthreads();
+    }
+    pa_dev::allow_next_grid();
+    retire_cta(p);
+}
+
+// --------------------------------------------------------------- merge ---
+//
+// One CTA per (sequence, KV head) with more than one partition: combine the
+// partitions' (acc, max, sum) by log-sum-exp,
+//   M = max_q m_q,  L = sum_q l_q 2^(m_q - M),  out = sum_q acc_q 2^(m_q - M) / L.
+// Launched as a programmatic dependent of the split kernel: it may start while
+// the split kernel drains and waits (griddepcontrol.wait) for it to finish.
+__global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodeParams p) {
+    __shared__ float s_M[16], s_L[16];
+    pa_dev::wait_prior_grid();
+    pa_dev::allow_next_grid();
+    const int s = blockIdx.x / p.Hkv, h = blockIdx.x - s * p.Hkv;
+    const int PT = p.sched[0];
+    const int L = seq_len(p, s, false);
+    const int nP = max(1, (L + PT - 1) / PT);
+    if (nP == 1) return;                                    // written by the split kernel
+    const int item0 = p.sched[2 + s] + h;                   // item of partition q: item0 + q*Hkv
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int n = warp; n < p.G; n += kWarps) {
+        float M = -INFINITY;
+        for (int q = lane; q < nP; q += 32)
+            M = fmaxf(M, p.part_ml[((static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv) * p.G + n) * 2]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float l = 0.f;
+        if (M != -INFINITY) {
+            for (int q = lane; q < nP; q += 32) {
+                const float* ml = p.part_ml + ((static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv) * p.G + n) * 2;
+                l += ml[1] * pa_dev::ex2(ml[0] - M);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+            s_M[n] = M;
+            s_L[n] = l;
+        }
+    }
+    __syncthreads();
+    const int GD = p.G * p.D;
+    const size_t out0 = (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G) * p.D;
+    for (int e = threadIdx.x * 4; e < GD; e += kThreads * 4) {   // D % 4 == 0: never splits a head
+        const int n = e / p.D;
+        const float M = s_M[n], Lsum = s_L[n];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+            for (int q = 0; q < nP; ++q) {
+                const size_t it = static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv;
+                const float f = pa_dev::ex2(p.part_ml[(it * p.G + n) * 2] - M);
+                const float4 a = *reinterpret_cast<const float4*>(p.part_acc + it * GD + e);
+                acc.x += f * a.x; acc.y += f * a.y; acc.z += f * a.z; acc.w += f * a.w;
+            }
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        store_out(p, out0 + e + 0, acc.x * inv);
+        store_out(p, out0 + e + 1, acc.y * inv);
+        store_out(p, out0 + e + 2, acc.z * inv);
+        store_out(p, out0 + e + 3, acc.w * inv);
     }
 }
 
 size_t fast_smem(int D, int S) {
-    return static_cast<size_t>(kWarps * 8 * (D + 4) + kWarps * 16 + 16) * sizeof(float) +
+    return fast_front_bytes(D) + static_cast<size_t>(kWarps * 16 + 16) * sizeof(float) +
            kWarps * sizeof(long long) + 4 * sizeof(int) + static_cast<size_t>(S + 1) * sizeof(int);
 }
 
@@ -528,7 +780,7 @@ int plan_decode(const pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* 
     if (occ <= 0) return PA_ERR_UNSUPPORTED;
     plan->grid = pool->num_sms * occ;
     if (fast) {
-        plan->items_target = plan->grid * 4;
+        plan->items_target = plan->grid * PA_ITEMS_PER_CTA;
         plan->max_items = static_cast<size_t>(plan->items_target) + static_cast<size_t>(Hkv) * S;
     } else {
         plan->items_target = 0;
@@ -545,17 +797,23 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
     p.items_target = plan.items_target;
     p.pt_min = plan.pt_min;
     p.pt_fixed = plan.pt_fixed;
+    const dim3 grid(plan.grid), block(plan.threads);
+    cudaError_t e;
     if (plan.fast) {
-        if (p.D == 64) decode_fast_kernel<64><<<plan.grid, plan.threads, plan.smem, st>>>(p);
-        else if (p.D == 128) decode_fast_kernel<128><<<plan.grid, plan.threads, plan.smem, st>>>(p);
-        else decode_fast_kernel<256><<<plan.grid, plan.threads, plan.smem, st>>>(p);
+        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64>, grid, block, plan.smem, st, p);
+        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128>, grid, block, plan.smem, st, p);
+        else e = launch_pdl(decode_fast_kernel<256>, grid, block, plan.smem, st, p);
     } else if (plan.bf16) {
-        decode_simple_kernel<uint16_t><<<plan.grid, plan.threads, plan.smem, st>>>(p);
+        e = launch_pdl(decode_simple_kernel<uint16_t>, grid, block, plan.smem, st, p);
     } else {
-        decode_simple_kernel<float><<<plan.grid, plan.threads, plan.smem, st>>>(p);
+        e = launch_pdl(decode_simple_kernel<float>, grid, block, plan.smem, st, p);
     }
     count_launch();
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    e = launch_pdl(decode_merge_kernel, dim3(static_cast<unsigned>(p.S) * static_cast<unsigned>(p.Hkv)),
+                   dim3(kThreads), 0, st, p);
+    count_launch();
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa_detail

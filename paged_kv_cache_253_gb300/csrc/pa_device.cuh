@@ -30,6 +30,24 @@ __device__ __forceinline__ uint2 ld_stream8(const void* p) {
     return r;
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialisation attribute may start while the previous kernel in the
+// stream drains.  wait_prior_grid() blocks until that kernel has completed and
+// its writes are visible, so it must precede every global read of inputs;
+// allow_next_grid() lets the next kernel begin launching.
+__device__ __forceinline__ void wait_prior_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_next_grid() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Fire-and-forget bulk prefetch of `bytes` (multiple of 16, 16-byte aligned)
+// into L2: starts the HBM read early without holding registers or shared memory.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3, uint32_t b0,

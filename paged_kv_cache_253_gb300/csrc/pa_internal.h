@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -31,7 +32,8 @@ struct DecodeParams {
     void* out;                  // [S][Hq][D]
     float* part_acc;            // [max_items][G][D]  un-normalised partial sums
     float* part_ml;             // [max_items][G][2]  (running max, sum) in log2 units
-    int* counters;              // [S][Hkv] arrival counters, zero between launches
+    int* ticket;                // [2] work ticket and retired-CTA count, zero between launches
+    int* sched;                 // [S + 3] PT, item count, first item of each sequence
     int* err;
     float scale_log2;           // scale * log2(e)
     int S, Hq, Hkv, G, D, B, num_blocks, max_blocks;
@@ -48,9 +50,33 @@ struct DecodeWorkspace {
     size_t bytes;               // total
 };
 
+// Decode workspace header: ticket[2], 2 spare ints, then the published
+// schedule (PT, item count, S + 1 item offsets); zeroed before first use.
+inline size_t decode_header_bytes(int S) {
+    return ((static_cast<size_t>(S) + 8) * sizeof(int) + 255) / 256 * 256;
+}
+
 namespace pa_detail {
 
 void count_launch();
+
+// Launch `kernel` on `st` allowing programmatic dependent launch (the kernel
+// must call pa_dev::wait_prior_grid() before reading any input).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launchers; each returns PA_OK or PA_ERR_CUDA (launch failure).
 int launch_append(const pa_pool* p, const void* k, const void* v, const int64_t* slots,

@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(256) append_kv_kernel(
     E* __restrict__ kpool, E* __restrict__ vpool, const E* __restrict__ k,
     const E* __restrict__ v, const int64_t* __restrict__ slots, int T, int Hkv, int D, int B,
     int64_t num_slots, int* err) {
+    pa_dev::wait_prior_grid();
+    pa_dev::allow_next_grid();
     const int warp = static_cast<int>((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (warp >= T * Hkv) return;
@@ -59,6 +61,8 @@ __global__ void __launch_bounds__(256) append_kv_kernel(
 __global__ void __launch_bounds__(256) copy_blocks_kernel(
     uint8_t* __restrict__ kpool, uint8_t* __restrict__ vpool, const int64_t* __restrict__ pairs,
     int P, int64_t num_blocks, int64_t block_bytes, int* err) {
+    pa_dev::wait_prior_grid();
+    pa_dev::allow_next_grid();
     const int i = blockIdx.x;
     const int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
     const bool range_bad = src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks;
@@ -100,29 +104,31 @@ int launch_append(const pa_pool* p, const void* k, const void* v, const int64_t*
     const int threads = 256;
     const int64_t grid = (warps * 32 + threads - 1) / threads;
     const int64_t num_slots = static_cast<int64_t>(p->num_blocks) * p->block_size;
+    cudaError_t e;
     if (p->dtype == PA_BF16)
-        append_kv_kernel<uint16_t><<<static_cast<unsigned>(grid), threads, 0, st>>>(
-            static_cast<uint16_t*>(p->k), static_cast<uint16_t*>(p->v),
-            static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), slots, T,
-            p->kv_heads, p->head_dim, p->block_size, num_slots, p->err);
+        e = launch_pdl(append_kv_kernel<uint16_t>, dim3(static_cast<unsigned>(grid)), dim3(threads),
+                       0, st, static_cast<uint16_t*>(p->k), static_cast<uint16_t*>(p->v),
+                       static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), slots, T,
+                       p->kv_heads, p->head_dim, p->block_size, num_slots, p->err);
     else
-        append_kv_kernel<uint32_t><<<static_cast<unsigned>(grid), threads, 0, st>>>(
-            static_cast<uint32_t*>(p->k), static_cast<uint32_t*>(p->v),
-            static_cast<const uint32_t*>(k), static_cast<const uint32_t*>(v), slots, T,
-            p->kv_heads, p->head_dim, p->block_size, num_slots, p->err);
+        e = launch_pdl(append_kv_kernel<uint32_t>, dim3(static_cast<unsigned>(grid)), dim3(threads),
+                       0, st, static_cast<uint32_t*>(p->k), static_cast<uint32_t*>(p->v),
+                       static_cast<const uint32_t*>(k), static_cast<const uint32_t*>(v), slots, T,
+                       p->kv_heads, p->head_dim, p->block_size, num_slots, p->err);
     count_launch();
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int launch_copy(const pa_pool* p, const int64_t* pairs, int P, cudaStream_t st) {
     const int64_t esz = p->dtype == PA_BF16 ? 2 : 4;
     const int64_t block_bytes =
         static_cast<int64_t>(p->kv_heads) * p->block_size * p->head_dim * esz;
-    copy_blocks_kernel<<<P, 256, 0, st>>>(static_cast<uint8_t*>(p->k),
-                                          static_cast<uint8_t*>(p->v), pairs, P,
-                                          p->num_blocks, block_bytes, p->err);
+    const cudaError_t e = launch_pdl(copy_blocks_kernel, dim3(P), dim3(256), 0, st,
+                                     static_cast<uint8_t*>(p->k), static_cast<uint8_t*>(p->v),
+                                     pairs, P, static_cast<int64_t>(p->num_blocks), block_bytes,
+                                     p->err);
     count_launch();
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa_detail

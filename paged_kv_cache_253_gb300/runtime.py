@@ -132,6 +132,7 @@ class DecodeStep:
         return self.out
 
     def launches(self):
+        """Library calls per step (pa_decode itself launches two kernels)."""
         return 2 + (1 if self.num_pairs else 0)
 
 
