@@ -62,12 +62,17 @@ def _workload_desc(wl):
             f"{wl.num_blocks} physical blocks")
 
 
-def _kv_bytes(wl, lens, shared_blocks=0):
+def _kv_bytes(wl, lens, groups=None):
     """Unique key+value bytes the decode reads: every cached token of every
-    sequence, K and V, all KV heads (blocks shared by several sequences are
-    counted once per sequence here unless the step reads them once)."""
+    sequence, K and V, all KV heads, with a shared span counted once for its
+    whole group when the step reads it once (pa_decode_shared)."""
     per_tok = wl.num_kv_heads * wl.head_dim * 2 * wl.elem_bytes
-    return int(sum(int(x) for x in lens)) * per_tok
+    tokens = int(sum(int(x) for x in lens))
+    if groups is not None:
+        offs, seqs, nsh = groups
+        for g in range(len(nsh)):
+            tokens -= (int(offs[g + 1]) - int(offs[g]) - 1) * int(nsh[g]) * wl.block_size
+    return tokens * per_tok
 
 
 def _algo_bytes(wl, lens):
@@ -238,8 +243,9 @@ def run_ours(args):
     pool, bm, _ = runtime.replay_setup(wl, values, f"cuda:{local}")
     step = runtime.prepare_step(wl, values, pool, bm)
     lens = step.context_lens.cpu().numpy()
-    kv_bytes = _kv_bytes(wl, lens)
-    algo_bytes = _algo_bytes(wl, lens)
+    kv_bytes = _kv_bytes(wl, lens, step.groups)
+    logical_kv_bytes = _kv_bytes(wl, lens)
+    algo_bytes = _algo_bytes(wl, lens) - logical_kv_bytes + kv_bytes
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{local}")
     stream = torch.cuda.current_stream()
 
@@ -261,7 +267,7 @@ def run_ours(args):
         return [a.elapsed_time(b) for a, b in evs]
 
     def decode_only():
-        pool.decode(step.q, step.block_tables, step.context_lens, step.scale, out=step.out)
+        step.decode()
 
     if dist:
         dist.barrier()
@@ -299,7 +305,12 @@ def run_ours(args):
         if dev["pairs"].shape[0]:
             pool.copy_blocks(dev["pairs"])
         pool.append_kv(dev["new_k"], dev["new_v"], dev["slots"])
-        pool.decode(dev["q"], dev["block_tables"], dev["context_lens"], step.scale, out=step.out)
+        if step.groups is not None and len(step.groups[2]):
+            pool.decode_shared(dev["q"], dev["block_tables"], dev["context_lens"], step.scale,
+                               step.groups, out=step.out)
+        else:
+            pool.decode(dev["q"], dev["block_tables"], dev["context_lens"], step.scale,
+                        out=step.out)
         out_host.copy_(step.out, non_blocking=True)
         c.record(stream)
         c.synchronize()
@@ -321,7 +332,9 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": _workload_desc(wl),
                    "l2": "flushed between steps (256 MiB write, outside the timed events)",
-                   "kv_bytes_per_step": kv_bytes, "copy_pairs_per_step": step.num_pairs,
+                   "kv_bytes_per_step": kv_bytes, "logical_kv_bytes_per_step": logical_kv_bytes,
+                   "shared_groups": int(len(step.groups[2])) if step.groups is not None else 0,
+                   "copy_pairs_per_step": step.num_pairs,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_frac_of_" + peak_kind: round(value / world / peak, 4),
         "tokens_per_s": round(world * wl.num_seqs / (ms * 1e-3), 1),

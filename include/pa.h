@@ -153,6 +153,35 @@ int pa_decode(pa_pool *pool, const void *q, int num_seqs, int num_q_heads,
 /* Size the pool's decode workspace for batches up to these bounds. */
 int pa_decode_reserve(pa_pool *pool, int max_seqs, int max_q_heads);
 
+/* Decode attention for batches whose requests share leading blocks, reading
+ * each shared block once for all the queries that point at it ([Z] answer:
+ * requests with one prefix point at one copy; [K] "Prefix Sharing Is a
+ * Natural Extension").  Same arguments and result as pa_decode, plus a host
+ * description of the sharing (pa_bm_prefix_groups produces it):
+ *   group_seq_offsets   host int32 [num_groups + 1], offsets[0] == 0: group g
+ *                       owns batch entries group_seqs[offsets[g] .. offsets[g+1])
+ *   group_seqs          host int32: batch indices; each in at most one group
+ *   group_shared_blocks host int32 [num_groups]: number of leading table
+ *                       entries that are the same physical blocks for every
+ *                       member and lie wholly inside every member's context
+ * For each group and KV head, tiles of up to 64 query rows (members x their G
+ * heads) attend to the shared span together on the tensor cores; each
+ * member's private suffix goes through the ordinary split path, and the
+ * partials are merged by log-sum-exp.  Groups with fewer than two members
+ * or no shared block are ignored; shapes outside the bf16 tensor-core path
+ * (see pa_decode) fall back to pa_decode.  The device checks that members'
+ * leading entries agree and that their contexts cover the shared span, and
+ * records PA_ERR_INVALID_ARG otherwise (the result is then undefined).
+ * The description is uploaded to the device when it differs from the
+ * previous call's (a synchronous copy); repeated steps with the same sharing
+ * reuse it.  Calls on one pool must not overlap on the GPU. */
+int pa_decode_shared(pa_pool *pool, const void *q, int num_seqs, int num_q_heads,
+                     const int32_t *block_tables, int max_blocks_per_seq,
+                     const int32_t *context_lens, float scale, void *out,
+                     pa_dtype out_dtype, const int32_t *group_seq_offsets,
+                     const int32_t *group_seqs, const int32_t *group_shared_blocks,
+                     int num_groups, void *stream);
+
 /* Decode without allocating: the same computation, arguments and result as
  * pa_decode, for callers that cannot let the library call cudaMalloc — a
  * process whose device memory is owned by another allocator (a framework's
@@ -256,6 +285,16 @@ int pa_bm_num_free(pa_bm *bm);
 
 /* Copy the free pool in FIFO order into out[0..cap); *n = its length. */
 int pa_bm_free_list(pa_bm *bm, int32_t *out, int cap, int *n);
+
+/* Sharing description of a decode batch for pa_decode_shared: batch entries
+ * i (requests reqs[i]) whose tables start with the same physical block form
+ * a group (in order of first appearance; singletons dropped); its shared
+ * span is the longest run of leading entries that are the same physical
+ * block for all members and full in every member.  Outputs (host, room for
+ * n + 1 / n / n entries): group_offsets, group_seqs (batch indices),
+ * group_shared_blocks; *num_groups = number of groups. */
+int pa_bm_prefix_groups(pa_bm *bm, int n, const int32_t *reqs, int32_t *group_offsets,
+                        int32_t *group_seqs, int32_t *group_shared_blocks, int *num_groups);
 
 /* 1 if the block is registered in the prefix hash table, 0 if not, -1 if out
  * of range. */

@@ -47,6 +47,9 @@ SIGNATURES = {
     "pa_decode": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_void_p, c_float,
                           c_void_p, c_int, c_void_p]),
     "pa_decode_reserve": (c_int, [c_void_p, c_int, c_int]),
+    "pa_decode_shared": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_void_p,
+                                 c_float, c_void_p, c_int, c_i32p, c_i32p, c_i32p, c_int,
+                                 c_void_p]),
     "pa_decode_noalloc": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_void_p,
                                   c_float, c_void_p, c_int, c_void_p]),
     "pa_get_error": (c_int, [c_void_p, c_void_p]),
@@ -67,6 +70,7 @@ SIGNATURES = {
     "pa_bm_num_free": (c_int, [c_void_p]),
     "pa_bm_free_list": (c_int, [c_void_p, c_i32p, c_int, c_intp]),
     "pa_bm_is_cached": (c_int, [c_void_p, c_int]),
+    "pa_bm_prefix_groups": (c_int, [c_void_p, c_int, c_i32p, c_i32p, c_i32p, c_i32p, c_intp]),
     "pa_bm_fnv1a64": (ctypes.c_uint64, [c_u8p, c_size_t]),
 }
 

@@ -106,6 +106,32 @@ class KVPool:
                             _CODE[out.dtype], _stream()), "pa_decode")
         return out
 
+    def decode_shared(self, q, block_tables, context_lens, scale, groups, out=None,
+                      out_dtype=torch.float32):
+        """Decode with shared leading blocks read once per group.
+
+        groups = (offsets, seqs, shared_blocks) host int32 arrays, as returned by
+        BlockManager.prefix_groups.
+        """
+        offs, seqs, nsh = (np.ascontiguousarray(a, dtype=np.int32) for a in groups)
+        S, hq, d = q.shape
+        if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+            raise ValueError("block_tables [S, max_blocks] / context_lens [S]")
+        if out is None:
+            out = torch.empty((S, hq, d), dtype=out_dtype, device=self.device)
+        ng = len(nsh)
+        if len(offs) != ng + 1:
+            raise ValueError("group offsets must have num_groups + 1 entries")
+        L.check(L.pa_decode_shared(self.handle, _dev(q, self.dtype, "q", self.device), S, hq,
+                                   _dev(block_tables, torch.int32, "block_tables", self.device),
+                                   int(block_tables.shape[1]),
+                                   _dev(context_lens, torch.int32, "context_lens", self.device),
+                                   float(scale), _dev(out, out.dtype, "out", self.device),
+                                   _CODE[out.dtype], _i32p(offs), _i32p(seqs) if len(seqs) else None,
+                                   _i32p(nsh) if ng else None, ng, _stream()),
+                "pa_decode_shared")
+        return out
+
     def reserve(self, max_seqs, max_q_heads):
         L.check(L.pa_decode_reserve(self.handle, int(max_seqs), int(max_q_heads)),
                 "pa_decode_reserve")
@@ -230,6 +256,19 @@ class BlockManager:
         L.check(L.pa_bm_free_list(self.handle, _i32p(out), self.num_blocks, ctypes.byref(n)),
                 "pa_bm_free_list")
         return out[:n.value].tolist()
+
+    def prefix_groups(self, reqs):
+        """(offsets, seqs, shared_blocks) of the batch's sharing groups."""
+        r = np.ascontiguousarray(reqs, dtype=np.int32)
+        n = len(r)
+        offs = np.zeros(n + 1, dtype=np.int32)
+        seqs = np.zeros(max(n, 1), dtype=np.int32)
+        nsh = np.zeros(max(n, 1), dtype=np.int32)
+        ng = ctypes.c_int()
+        L.check(L.pa_bm_prefix_groups(self.handle, n, _i32p(r), _i32p(offs), _i32p(seqs),
+                                      _i32p(nsh), ctypes.byref(ng)), "pa_bm_prefix_groups")
+        g = ng.value
+        return offs[:g + 1].copy(), seqs[:offs[g]].copy(), nsh[:g].copy()
 
     def is_cached(self, block):
         return L.pa_bm_is_cached(self.handle, int(block)) == 1

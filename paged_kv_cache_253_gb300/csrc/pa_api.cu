@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -131,6 +132,7 @@ int pa_pool_destroy(pa_pool* pool) {
     cudaFree(pool->v);
     cudaFree(pool->err);
     cudaFree(pool->ws);
+    cudaFree(pool->desc_dev);
     delete pool;
     return PA_OK;
 }
@@ -227,9 +229,20 @@ int pa_decode_reserve(pa_pool* pool, int max_seqs, int max_q_heads) {
                                                   nullptr));
 }
 
-int pa_decode(pa_pool* pool, const void* q, int num_seqs, int num_q_heads,
-              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-              float scale, void* out, pa_dtype out_dtype, void* stream) {
+// Host plan of the shared-prefix items (see pa_decode_shared).
+struct SharedPlan {
+    int num_groups = 0;
+    int K = 0;                  // items before expanding over KV heads
+    int slots = 0;              // shared-partial slots (members x chunks)
+    int chunk_tokens = 0, members_per_tile = 0;
+    std::vector<int> desc;      // packed device descriptor
+    size_t off_items, off_sgroup, off_smember, off_sstart, off_goff, off_gmem, off_gnc, off_gbase, off_gtok;
+};
+
+static int decode_impl(pa_pool* pool, const void* q, int num_seqs, int num_q_heads,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, float scale, void* out, pa_dtype out_dtype,
+                       void* stream, const SharedPlan* sh) {
     int rc = check_decode_args(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
                                context_lens, out, out_dtype);
     if (rc != PA_OK || num_seqs == 0) return rc;
@@ -237,13 +250,57 @@ int pa_decode(pa_pool* pool, const void* q, int num_seqs, int num_q_heads,
     if (!g.ok) return PA_ERR_CUDA;
     const int G = num_q_heads / pool->kv_heads;
     pa_detail::DecodePlan plan;
+    plan.shared = sh != nullptr;
     rc = pa_detail::plan_decode(pool, num_seqs, num_q_heads, max_blocks_per_seq, &plan);
     if (rc != PA_OK) return rc;
+    if (sh && !plan.fast) return PA_ERR_UNSUPPORTED;
     size_t cb = 0;
-    const size_t need = workspace_bytes(plan, num_seqs, pool->kv_heads, G, pool->head_dim, &cb);
+    size_t need = workspace_bytes(plan, num_seqs, pool->kv_heads, G, pool->head_dim, &cb);
+    const size_t sacc_off = need;
+    const size_t sacc_bytes = sh ? round256(static_cast<size_t>(sh->slots) * pool->kv_heads * G *
+                                            pool->head_dim * sizeof(float)) : 0;
+    const size_t sml_bytes = sh ? round256(static_cast<size_t>(sh->slots) * pool->kv_heads * G * 2 *
+                                           sizeof(float)) : 0;
+    need += sacc_bytes + sml_bytes;
     rc = ensure_workspace(pool, need);
     if (rc != PA_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (sh && sh->desc != pool->desc_host) {       // upload only a changed description
+        if (sh->desc.size() > pool->desc_cap) {
+            if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+            cudaFree(pool->desc_dev);
+            pool->desc_dev = nullptr;
+            pool->desc_cap = 0;
+            if (cudaMalloc(&pool->desc_dev, sh->desc.size() * sizeof(int)) != cudaSuccess) {
+                cudaGetLastError();
+                return PA_ERR_OUT_OF_MEMORY;
+            }
+            pool->desc_cap = sh->desc.size();
+        }
+        // pageable source: the runtime stages it before returning, after prior work on st
+        if (cudaMemcpyAsync(pool->desc_dev, sh->desc.data(), sh->desc.size() * sizeof(int),
+                            cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return PA_ERR_CUDA;
+        pool->desc_host = sh->desc;
+    }
     DecodeParams p{};
+    if (sh) {
+        const int* d = pool->desc_dev;
+        p.n_shared_items = sh->K * pool->kv_heads;
+        p.chunk_tokens = sh->chunk_tokens;
+        p.members_per_tile = sh->members_per_tile;
+        p.sh_items = d + sh->off_items;
+        p.seq_group = d + sh->off_sgroup;
+        p.seq_member = d + sh->off_smember;
+        p.seq_start = d + sh->off_sstart;
+        p.g_members_off = d + sh->off_goff;
+        p.g_members = d + sh->off_gmem;
+        p.g_nchunks = d + sh->off_gnc;
+        p.g_spart_base = d + sh->off_gbase;
+        p.g_shared_tokens = d + sh->off_gtok;
+        p.spart_acc = reinterpret_cast<float*>(static_cast<char*>(pool->ws) + sacc_off);
+        p.spart_ml = reinterpret_cast<float*>(static_cast<char*>(pool->ws) + sacc_off + sacc_bytes);
+    }
     p.q = q;
     p.k = pool->k;
     p.v = pool->v;
@@ -266,7 +323,103 @@ int pa_decode(pa_pool* pool, const void* q, int num_seqs, int num_q_heads,
     p.num_blocks = pool->num_blocks;
     p.max_blocks = max_blocks_per_seq;
     p.out_bf16 = out_dtype == PA_BF16;
-    return pa_detail::launch_decode(plan, p, static_cast<cudaStream_t>(stream));
+    return pa_detail::launch_decode(plan, p, st);
+}
+
+int pa_decode(pa_pool* pool, const void* q, int num_seqs, int num_q_heads,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              float scale, void* out, pa_dtype out_dtype, void* stream) {
+    return decode_impl(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                       context_lens, scale, out, out_dtype, stream, nullptr);
+}
+
+int pa_decode_shared(pa_pool* pool, const void* q, int num_seqs, int num_q_heads,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, float scale, void* out, pa_dtype out_dtype,
+                     const int32_t* group_seq_offsets, const int32_t* group_seqs,
+                     const int32_t* group_shared_blocks, int num_groups, void* stream) {
+    int rc = check_decode_args(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                               context_lens, out, out_dtype);
+    if (rc != PA_OK || num_seqs == 0) return rc;
+    if (num_groups < 0 || (num_groups > 0 && (!group_seq_offsets || !group_seqs ||
+                                               !group_shared_blocks)))
+        return PA_ERR_INVALID_ARG;
+    const int Hkv = pool->kv_heads, G = num_q_heads / Hkv, B = pool->block_size;
+    const bool tensor_path = pool->dtype == PA_BF16 && B % 16 == 0 && G <= 8 &&
+                             (pool->head_dim == 64 || pool->head_dim == 128 || pool->head_dim == 256);
+    // validate and keep groups of at least two members with a shared span
+    std::vector<char> seen(num_seqs, 0);
+    std::vector<int> keep;
+    if (num_groups > 0 && group_seq_offsets[0] != 0) return PA_ERR_INVALID_ARG;
+    for (int gi = 0; gi < num_groups; ++gi) {
+        const int a = group_seq_offsets[gi], b = group_seq_offsets[gi + 1];
+        if (b < a) return PA_ERR_INVALID_ARG;
+        if (group_shared_blocks[gi] < 0 || group_shared_blocks[gi] > max_blocks_per_seq)
+            return PA_ERR_INVALID_ARG;
+        for (int i = a; i < b; ++i) {
+            const int s = group_seqs[i];
+            if (s < 0 || s >= num_seqs || seen[s]) return PA_ERR_INVALID_ARG;
+            seen[s] = 1;
+        }
+        if (b - a >= 2 && group_shared_blocks[gi] > 0) keep.push_back(gi);
+    }
+    if (keep.empty() || !tensor_path)
+        return decode_impl(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                           context_lens, scale, out, out_dtype, stream, nullptr);
+    SharedPlan sh;
+    sh.num_groups = static_cast<int>(keep.size());
+    sh.members_per_tile = std::max(1, 64 / G);
+    sh.chunk_tokens = std::max(B, 512 / B * B);
+    const int Ng = sh.num_groups;
+    std::vector<int> items, sgroup(num_seqs, -1), smember(num_seqs, 0), sstart(num_seqs, 0);
+    std::vector<int> goff(Ng + 1, 0), gmem, gnc(Ng), gbase(Ng), gtok(Ng);
+    int slots = 0;
+    for (int k = 0; k < Ng; ++k) {
+        const int gi = keep[k];
+        const int a = group_seq_offsets[gi], b = group_seq_offsets[gi + 1], M = b - a;
+        const int tok = group_shared_blocks[gi] * B;
+        const int nc = (tok + sh.chunk_tokens - 1) / sh.chunk_tokens;
+        const int tiles = (M + sh.members_per_tile - 1) / sh.members_per_tile;
+        for (int i = a; i < b; ++i) {
+            const int s = group_seqs[i];
+            sgroup[s] = k;
+            smember[s] = i - a;
+            sstart[s] = tok;
+            gmem.push_back(s);
+        }
+        goff[k + 1] = goff[k] + M;
+        gnc[k] = nc;
+        gbase[k] = slots;
+        gtok[k] = tok;
+        slots += M * nc;
+        for (int c = 0; c < nc; ++c)          // chunk-major: spread a group's tiles over CTAs
+            for (int t = 0; t < tiles; ++t) {
+                items.push_back(k);
+                items.push_back(t);
+                items.push_back(c);
+                items.push_back(0);
+            }
+    }
+    sh.K = static_cast<int>(items.size() / 4);
+    sh.slots = slots;
+    auto& d = sh.desc;
+    auto put = [&d](const std::vector<int>& v) {
+        const size_t off = d.size();
+        d.insert(d.end(), v.begin(), v.end());
+        while (d.size() % 4) d.push_back(0);        // keep int4 alignment of each section
+        return off;
+    };
+    sh.off_items = put(items);
+    sh.off_sgroup = put(sgroup);
+    sh.off_smember = put(smember);
+    sh.off_sstart = put(sstart);
+    sh.off_goff = put(goff);
+    sh.off_gmem = put(gmem);
+    sh.off_gnc = put(gnc);
+    sh.off_gbase = put(gbase);
+    sh.off_gtok = put(gtok);
+    return decode_impl(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                       context_lens, scale, out, out_dtype, stream, &sh);
 }
 
 int pa_get_error(pa_pool* pool, void* stream) {

@@ -8,6 +8,7 @@
 // Plain C++ bookkeeping that runs on the host between decode steps and hands
 // the GPU three small arrays: the slot of each new token, the block tables,
 // and the (src, dst) pairs to copy.  Semantics are spelled out in pa.h.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <deque>
@@ -295,6 +296,56 @@ int pa_bm_free_list(pa_bm* bm, int32_t* out, int cap, int* n) {
         if (i >= cap) break;
         out[i++] = b;
     }
+    return PA_OK;
+}
+
+int pa_bm_prefix_groups(pa_bm* bm, int n, const int32_t* reqs, int32_t* group_offsets,
+                        int32_t* group_seqs, int32_t* group_shared_blocks, int* num_groups) {
+    if (!bm || n < 0 || !num_groups || (n > 0 && (!reqs || !group_offsets || !group_seqs ||
+                                                   !group_shared_blocks)))
+        return PA_ERR_INVALID_ARG;
+    std::vector<Request*> r(n);
+    for (int i = 0; i < n; ++i) {
+        r[i] = bm->find(reqs[i]);
+        if (!r[i]) return PA_ERR_UNKNOWN_REQUEST;
+    }
+    // batch entries keyed by their first physical block, in batch order
+    std::unordered_map<int32_t, std::vector<int>> by_first;
+    std::vector<int32_t> order;
+    for (int i = 0; i < n; ++i) {
+        if (r[i]->table.empty() || static_cast<int>(r[i]->tokens.size()) < bm->block_size) continue;
+        const int32_t b0 = r[i]->table[0];
+        auto it = by_first.find(b0);
+        if (it == by_first.end()) {
+            order.push_back(b0);
+            by_first[b0] = {i};
+        } else {
+            it->second.push_back(i);
+        }
+    }
+    int ng = 0, pos = 0;
+    group_offsets[0] = 0;
+    for (int32_t b0 : order) {
+        const std::vector<int>& m = by_first[b0];
+        if (m.size() < 2) continue;
+        // leading blocks that are the same physical block for every member and
+        // full in every member's context
+        size_t full = SIZE_MAX;
+        for (int i : m) full = std::min(full, r[i]->tokens.size() / bm->block_size);
+        size_t lcp = 0;
+        while (lcp < full) {
+            const int32_t b = r[m[0]]->table[lcp];
+            bool same = true;
+            for (int i : m) same = same && r[i]->table[lcp] == b;
+            if (!same) break;
+            ++lcp;
+        }
+        if (lcp == 0) continue;
+        for (int i : m) group_seqs[pos++] = i;
+        group_shared_blocks[ng] = static_cast<int32_t>(lcp);
+        group_offsets[++ng] = pos;
+    }
+    *num_groups = ng;
     return PA_OK;
 }
 

@@ -60,9 +60,20 @@
 #define PA_STAGES 0             // cp.async ring depth per warp (0/1: direct register loads)
 #endif
 
+#ifndef PA_SHARED_STAGES
+#define PA_SHARED_STAGES 8      // staged 16-token tiles per CTA for shared-prefix items
+#endif
+#ifndef PA_SHARED_UNITS_PER_SYNC
+#define PA_SHARED_UNITS_PER_SYNC 2
+#endif
+
 namespace {
 
 constexpr int kWarps = PA_WARPS;
+constexpr int kSharedStages = PA_SHARED_STAGES;
+constexpr int kSharedUnitsPerSync = PA_SHARED_UNITS_PER_SYNC;
+static_assert(kSharedStages > kSharedUnitsPerSync, "shared pipeline needs copies in flight");
+static_assert(kSharedUnitsPerSync % 2 == 0, "shared items consume 32-token tiles");
 constexpr int kThreads = kWarps * 32;
 
 using pa_dev::record_error;
@@ -79,20 +90,35 @@ __device__ __forceinline__ int seq_len(const DecodeParams& p, int s, bool report
     return L;
 }
 
+// First token of a sequence's private span: tokens before it are a shared
+// prefix that pa_decode_shared serves with its shared items.
+__device__ __forceinline__ int priv_start(const DecodeParams& p, int s) {
+    return p.seq_start ? __ldg(p.seq_start + s) : 0;
+}
+
+__device__ __forceinline__ int priv_len(const DecodeParams& p, int s, bool report) {
+    return max(0, seq_len(p, s, report) - priv_start(p, s));
+}
+
+__device__ __forceinline__ bool in_group(const DecodeParams& p, int s) {
+    return p.seq_group && __ldg(p.seq_group + s) >= 0;
+}
+
 struct Sched {
     int PT;
-    int total_items;
+    int total_items;    // private items (the shared ones come first in the item order)
 };
 
-// Every CTA derives the same item list: per sequence nP = max(1, ceil(L/PT))
-// partitions, each of Hkv items; s_start[s] = first item of sequence s.
+// Every CTA derives the same private item list: per sequence nP =
+// max(1, ceil(Lp/PT)) partitions of its private span (length Lp), each of Hkv
+// items; s_start[s] = first private item of sequence s.
 __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* s_red) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per = (p.S + kThreads - 1) / kThreads;
     const int lo = min(p.S, tid * per), hi = min(p.S, lo + per);
     const bool report = blockIdx.x == 0;
     long long tok = 0;
-    for (int s = lo; s < hi; ++s) tok += seq_len(p, s, report);
+    for (int s = lo; s < hi; ++s) tok += priv_len(p, s, report);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tok += __shfl_xor_sync(0xffffffffu, tok, o);
     if (lane == 0) s_red[warp] = tok;
@@ -110,7 +136,7 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
     }
     int cnt = 0;
     for (int s = lo; s < hi; ++s) {
-        const int L = seq_len(p, s, false);
+        const int L = priv_len(p, s, false);
         cnt += max(1, (L + PT - 1) / PT) * p.Hkv;
     }
     int inc = cnt;                                  // inclusive scan over the block
@@ -128,7 +154,7 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
     for (int w = 0; w < kWarps; ++w) total_items += static_cast<int>(s_red[w]);
     for (int s = lo; s < hi; ++s) {
         s_start[s] = base;
-        base += max(1, (seq_len(p, s, false) + PT - 1) / PT) * p.Hkv;
+        base += max(1, (priv_len(p, s, false) + PT - 1) / PT) * p.Hkv;
     }
     if (tid == 0) s_start[p.S] = total_items;
     __syncthreads();
@@ -195,7 +221,7 @@ __device__ void finish_item(const DecodeParams& p, int item, int s, int h, int n
                             int stride) {
     const int tid = threadIdx.x;
     const int GD = p.G * p.D;
-    if (nP == 1) {
+    if (nP == 1 && !in_group(p, s)) {
         const size_t out0 = (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G) * p.D;
         for (int idx = tid; idx < GD; idx += kThreads) {
             const int n = idx / p.D, d = idx - n * p.D;
@@ -254,12 +280,14 @@ __device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D /
                                             uint2 (&v1)[D / 16], int nvalid, float sl, int r0,
                                             int r1, int c) {
     constexpr int NJ = D / 32, NT = D / 16;
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};   // two chains
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
         pa_dev::mma_bf16_16816(sc, k0[j].x, k1[j].x, k0[j].y, k1[j].y, a.qf[j].x, a.qf[j].y);
-        pa_dev::mma_bf16_16816(sc, k0[j].z, k1[j].z, k0[j].w, k1[j].w, a.qf[j].z, a.qf[j].w);
+        pa_dev::mma_bf16_16816(sd, k0[j].z, k1[j].z, k0[j].w, k1[j].w, a.qf[j].z, a.qf[j].w);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[i] += sd[i];
     float x0 = sc[0] * sl, x1 = sc[1] * sl, x2 = sc[2] * sl, x3 = sc[3] * sl;
     if (nvalid < 16) {                        // partly filled last tile
         if (r0 >= nvalid) x0 = x1 = -INFINITY;
@@ -307,7 +335,6 @@ __device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D /
     }
 }
 
-#if PA_STAGES > 1
 __device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gmem) : "memory");
 }
@@ -318,7 +345,6 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-#endif
 
 // The warp's share of one item: blocks lb0 + warp + kWarps*i of the
 // partition, each block cut into 16-token units.  With PA_STAGES > 1 every
@@ -492,29 +518,258 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
     }
 }
 
+// ------------------------------------------------- shared-prefix item ---
+//
+// One item = (group, KV head, tile of members, chunk of the shared span).  The
+// CTA's 4 warps each own 16 query rows (row r = member r / G, head r % G of
+// the tile); the chunk's 16-token K and V^T tiles are staged once in shared
+// memory (cp.async, double-buffered, all threads copying) and read by every
+// warp, so each shared block is read from memory once per item for up to 64
+// queries instead of once per query.  Per 16-token tile and warp:
+//   S[16 rows x 16 tokens] = Q[16 x D] . K^T   (2 n-tiles x D/16 k-steps)
+//   O[16 x D] += P[16 x 16] . V[16 x D]         (D/8 n-tiles, P as bf16 hi+lo)
+// with the same token permutation and d-chunk split as the private path, so
+// K and V^T fragments are read with 16-byte / 8-byte loads.  The item's
+// (acc, max, sum) per (member, head) go to the shared-partial slots.
+template <int D>
+__device__ void shared_item(const DecodeParams& p, int grp, int h, int tile, int chunk,
+                            unsigned char* stage_mem) {
+    constexpr int NJ = D / 32, NT = D / 16, ND = D / 8;
+    constexpr int UNIT = 64 * D;                    // bytes per staged tile pair
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gi = lane >> 2, c = lane & 3;
+    const int G = p.G, B = p.B;
+    const int moff = p.g_members_off[grp];
+    const int M = p.g_members_off[grp + 1] - moff;
+    const int m0 = tile * p.members_per_tile, m1 = min(M, m0 + p.members_per_tile);
+    const int shared_tok = p.g_shared_tokens[grp];
+    const int t0 = chunk * p.chunk_tokens, t1 = min(shared_tok, t0 + p.chunk_tokens);
+    const int nunits = (t1 - t0) / 16;
+    const int nC = p.g_nchunks[grp];
+
+    // every member must have these leading blocks in its context
+    if (chunk == 0 && tid < m1 - m0 && seq_len(p, p.g_members[moff + m0 + tid], false) < shared_tok)
+        record_error(p.err, PA_ERR_INVALID_ARG);
+    static_assert(kThreads >= 64, "one thread per member of a tile");
+
+    // query rows of this warp
+    const int rA = warp * 16 + gi, rB = rA + 8;
+    const int memA = m0 + rA / G, memB = m0 + rB / G;
+    const bool okA = memA < m1, okB = memB < m1;
+    uint4 qa[NJ], qb[NJ];
+    {
+        const uint16_t* q = static_cast<const uint16_t*>(p.q);
+        const uint16_t* rowA = okA ? q + (static_cast<size_t>(p.g_members[moff + memA]) * p.Hq +
+                                          static_cast<size_t>(h) * G + rA % G) * D : nullptr;
+        const uint16_t* rowB = okB ? q + (static_cast<size_t>(p.g_members[moff + memB]) * p.Hq +
+                                          static_cast<size_t>(h) * G + rB % G) * D : nullptr;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            qa[j] = okA ? __ldg(reinterpret_cast<const uint4*>(rowA + (4 * j + c) * 8)) : make_uint4(0u, 0u, 0u, 0u);
+            qb[j] = okB ? __ldg(reinterpret_cast<const uint4*>(rowB + (4 * j + c) * 8)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    float o[ND][4];
+#pragma unroll
+    for (int t = 0; t < ND; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb_ = 0.f;
+    const float sl = p.scale_log2;
+    const int r0 = 4 * (gi >> 1) + (gi & 1), r1 = r0 + 2;
+
+    const int32_t* table = p.tables + static_cast<size_t>(p.g_members[moff]) * p.max_blocks;
+    const uint16_t* kpool = static_cast<const uint16_t*>(p.k);
+    const uint16_t* vpool = static_cast<const uint16_t*>(p.v);
+    const size_t tile_elems = static_cast<size_t>(B) * D;
+    const uint32_t stage_s = static_cast<uint32_t>(__cvta_generic_to_shared(stage_mem));
+    constexpr int NS = kSharedStages, CH = kSharedUnitsPerSync;
+    unsigned valid = 0;
+    // the chunk's block ids, one per lane (a chunk spans at most 32 blocks)
+    const int lbc = t0 / B, nbc = (t1 - t0) / B;
+    const int chunk_phys = lane < nbc ? __ldg(table + lbc + lane) : -1;
+    auto issue = [&](int u) {
+        const int tok = t0 + u * 16, lb = tok / B, sub = (tok - lb * B) / 16;
+        const int phys = __shfl_sync(0xffffffffu, chunk_phys, lb - lbc);
+        const int st = u % NS;
+        valid &= ~(1u << st);
+        (void)sub;
+        if (phys < 0 || phys >= p.num_blocks) {
+            if (tid == 0) record_error(p.err, PA_ERR_BAD_BLOCK_ID);
+        } else {
+            const size_t tl = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems;
+            const uint16_t* kg = kpool + tl + static_cast<size_t>(sub) * 16 * D;
+            const uint16_t* vg = vpool + tl + sub * 16;
+            const uint32_t ks = stage_s + st * UNIT, vs = ks + 32 * D;
+            for (int q = tid; q < 2 * D; q += kThreads) {
+                const int r = q / (D / 8), ch = q - r * (D / 8);
+                cp_async16(ks + r * (2 * D) + ((ch ^ ((r & 1) << 2)) << 4), kg + r * D + ch * 8);
+            }
+            for (int q = tid; q < 2 * D; q += kThreads) {
+                const int d = q >> 1, half = q & 1;
+                cp_async16(vs + d * 32 + half * 16, vg + static_cast<size_t>(d) * B + half * 8);
+            }
+            valid |= 1u << st;
+        }
+        cp_async_commit();
+    };
+    // NS stages; each step consumes CH units after one barrier, while the
+    // copies of the next NS - CH units are in flight.
+    for (int u = 0; u < NS - CH; ++u) {
+        if (u < nunits) issue(u);
+        else cp_async_commit();
+    }
+    // every member's table must hold the same blocks here (checked once per
+    // item while the first copies are in flight)
+    for (int e = tid; e < (m1 - m0) * nbc; e += kThreads) {
+        const int mi = e / nbc, bi = e - mi * nbc;
+        const int32_t* mt = p.tables + static_cast<size_t>(p.g_members[moff + m0 + mi]) * p.max_blocks;
+        if (__ldg(mt + lbc + bi) != __ldg(table + lbc + bi)) record_error(p.err, PA_ERR_INVALID_ARG);
+    }
+    for (int u0 = 0; u0 < nunits; u0 += CH) {
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            if (u0 + NS - CH + k < nunits) issue(u0 + NS - CH + k);
+            else cp_async_commit();
+        }
+        cp_async_wait<NS - CH>();
+        __syncthreads();
+      for (int u = u0; u < min(nunits, u0 + CH); u += 2) {
+        // two 16-token units form one 32-token tile: 4 token n-tiles
+        const bool v0ok = (valid >> (u % NS)) & 1u;
+        const bool v1ok = u + 1 < nunits && ((valid >> ((u + 1) % NS)) & 1u);
+        float sA[4][4], sB[4][4];                   // [n-tile][frag], even / odd k-step chains
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sA[nt][i] = sB[nt][i] = 0.f;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            if (!(w == 0 ? v0ok : v1ok)) continue;
+            const unsigned char* ks = stage_mem + ((u + w) % NS) * UNIT;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int ch = 4 * j + c;
+                const uint4 ka = *reinterpret_cast<const uint4*>(ks + r0 * (2 * D) + ((ch ^ ((r0 & 1) << 2)) << 4));
+                const uint4 kb = *reinterpret_cast<const uint4*>(ks + r1 * (2 * D) + ((ch ^ ((r1 & 1) << 2)) << 4));
+                pa_dev::mma_bf16_16816(sA[2 * w], qa[j].x, qb[j].x, qa[j].y, qb[j].y, ka.x, ka.y);
+                pa_dev::mma_bf16_16816(sB[2 * w], qa[j].z, qb[j].z, qa[j].w, qb[j].w, ka.z, ka.w);
+                pa_dev::mma_bf16_16816(sA[2 * w + 1], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kb.x, kb.y);
+                pa_dev::mma_bf16_16816(sB[2 * w + 1], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kb.z, kb.w);
+            }
+        }
+        // rows gi ([0], [1]) and gi + 8 ([2], [3]) of each n-tile
+        float xa[8], xb[8];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const bool ok = (nt < 2) ? v0ok : v1ok;
+            xa[2 * nt] = ok ? (sA[nt][0] + sB[nt][0]) * sl : -INFINITY;
+            xa[2 * nt + 1] = ok ? (sA[nt][1] + sB[nt][1]) * sl : -INFINITY;
+            xb[2 * nt] = ok ? (sA[nt][2] + sB[nt][2]) * sl : -INFINITY;
+            xb[2 * nt + 1] = ok ? (sA[nt][3] + sB[nt][3]) * sl : -INFINITY;
+        }
+        float mxa = xa[0], mxb = xb[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+            mxa = fmaxf(mxa, xa[i]);
+            mxb = fmaxf(mxb, xb[i]);
+        }
+#pragma unroll
+        for (int off = 1; off < 4; off <<= 1) {
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
+        }
+        const float na = fmaxf(ma, mxa), nb = fmaxf(mb, mxb);
+        const float sa = na == -INFINITY ? 0.f : na, sb = nb == -INFINITY ? 0.f : nb;
+        const float cra = pa_dev::ex2(ma - sa), crb = pa_dev::ex2(mb - sb);
+        float pa[8], pb[8], suma = 0.f, sumb = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            pa[i] = pa_dev::ex2(xa[i] - sa);
+            pb[i] = pa_dev::ex2(xb[i] - sb);
+            suma += pa[i];
+            sumb += pb[i];
+        }
+        la = la * cra + suma;
+        lb_ = lb_ * crb + sumb;
+        ma = na;
+        mb = nb;
+        // A fragments of P for the two 16-token k-steps (bf16 high and low parts)
+        uint32_t ah[2][4], al[2][4];
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            const int n0 = 2 * w, n1 = 2 * w + 1;
+            ah[w][0] = pa_dev::pack_bf16(pa[2 * n0], pa[2 * n0 + 1]);
+            ah[w][1] = pa_dev::pack_bf16(pb[2 * n0], pb[2 * n0 + 1]);
+            ah[w][2] = pa_dev::pack_bf16(pa[2 * n1], pa[2 * n1 + 1]);
+            ah[w][3] = pa_dev::pack_bf16(pb[2 * n1], pb[2 * n1 + 1]);
+            al[w][0] = pa_dev::pack_bf16(pa[2 * n0] - pa_dev::bf16_lo(ah[w][0]), pa[2 * n0 + 1] - pa_dev::bf16_hi(ah[w][0]));
+            al[w][1] = pa_dev::pack_bf16(pb[2 * n0] - pa_dev::bf16_lo(ah[w][1]), pb[2 * n0 + 1] - pa_dev::bf16_hi(ah[w][1]));
+            al[w][2] = pa_dev::pack_bf16(pa[2 * n1] - pa_dev::bf16_lo(ah[w][2]), pa[2 * n1 + 1] - pa_dev::bf16_hi(ah[w][2]));
+            al[w][3] = pa_dev::pack_bf16(pb[2 * n1] - pa_dev::bf16_lo(ah[w][3]), pb[2 * n1 + 1] - pa_dev::bf16_hi(ah[w][3]));
+        }
+#pragma unroll
+        for (int t = 0; t < ND; ++t) {
+            o[t][0] *= cra; o[t][1] *= cra; o[t][2] *= crb; o[t][3] *= crb;
+        }
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            if (!(w == 0 ? v0ok : v1ok)) continue;
+            const unsigned char* vs = stage_mem + ((u + w) % NS) * UNIT + 32 * D;
+#pragma unroll
+            for (int t = 0; t < ND; ++t) {
+                const uint2 v = *reinterpret_cast<const uint2*>(vs + (8 * t + gi) * 32 + 8 * c);
+                pa_dev::mma_bf16_16816(o[t], ah[w][0], ah[w][1], ah[w][2], ah[w][3], v.x, v.y);
+                pa_dev::mma_bf16_16816(o[t], al[w][0], al[w][1], al[w][2], al[w][3], v.x, v.y);
+            }
+        }
+      }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+        la += __shfl_xor_sync(0xffffffffu, la, off);
+        lb_ += __shfl_xor_sync(0xffffffffu, lb_, off);
+    }
+    const int GD = G * D;
+    auto write_row = [&](int mem, int n, int which, float m, float l) {
+        const size_t slot = (static_cast<size_t>(p.g_spart_base[grp]) + static_cast<size_t>(mem) * nC + chunk) * p.Hkv + h;
+        float* acc = p.spart_acc + slot * GD + static_cast<size_t>(n) * D;
+#pragma unroll
+        for (int t = 0; t < ND; ++t)
+            *reinterpret_cast<float2*>(acc + 8 * t + 2 * c) = make_float2(o[t][which], o[t][which + 1]);
+        if (c == 0) {
+            p.spart_ml[(slot * G + n) * 2] = m;
+            p.spart_ml[(slot * G + n) * 2 + 1] = l;
+        }
+    };
+    if (okA) write_row(memA, rA % G, 0, ma, la);
+    if (okB) write_row(memB, rB % G, 2, mb, lb_);
+    __syncthreads();                                // the stages are reused by the next item
+}
+
 // Bytes at the front of the fast kernel's shared memory: the cp.async rings
 // of all warps, which the merge buffer reuses between items.
-__host__ __device__ constexpr size_t fast_front_bytes(int D) {
-    return PA_STAGES > 1
-               ? (static_cast<size_t>(kWarps) * PA_STAGES * 64 * D >
-                          static_cast<size_t>(kWarps) * 8 * (D + 4) * 4
-                      ? static_cast<size_t>(kWarps) * PA_STAGES * 64 * D
-                      : static_cast<size_t>(kWarps) * 8 * (D + 4) * 4)
-               : static_cast<size_t>(kWarps) * 8 * (D + 4) * 4;
+// (With shared-prefix items they also hold those items' staged tiles.)
+__host__ __device__ constexpr size_t cmax(size_t a, size_t b) { return a > b ? a : b; }
+__host__ __device__ constexpr size_t fast_front_bytes(int D, bool shared) {
+    return cmax(cmax(PA_STAGES > 1 ? static_cast<size_t>(kWarps) * PA_STAGES * 64 * D : 0,
+                     static_cast<size_t>(kWarps) * 8 * (D + 4) * 4),
+                shared ? static_cast<size_t>(kSharedStages) * 64 * D : 0);
 }
 
 __device__ __forceinline__ size_t warp_ring_offset(int D) {
     return static_cast<size_t>(threadIdx.x >> 5) * PA_STAGES * 64 * D;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, PA_MIN_CTAS) decode_fast_kernel(const DecodeParams p) {
+template <int D, bool SHARED>
+__global__ void __launch_bounds__(kThreads, SHARED ? 2 : PA_MIN_CTAS)
+decode_fast_kernel(const DecodeParams p) {
     constexpr int OS = D + 4;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // [ring | merge buffer (aliases the ring when there is one)][m, l, ...][s_start]
     unsigned char* ring = smem_raw;
     float* sm_o = reinterpret_cast<float*>(smem_raw);        // [kWarps][8][OS]
-    float* sm_m = reinterpret_cast<float*>(smem_raw + fast_front_bytes(D));   // [kWarps][8]
+    float* sm_m = reinterpret_cast<float*>(smem_raw + fast_front_bytes(D, SHARED));  // [kWarps][8]
     float* sm_l = sm_m + kWarps * 8;                          // [kWarps][8]
     float* res_m = sm_l + kWarps * 8;                         // [8]
     float* res_l = res_m + 8;                                 // [8]
@@ -525,13 +780,22 @@ __global__ void __launch_bounds__(kThreads, PA_MIN_CTAS) decode_fast_kernel(cons
     pa_dev::wait_prior_grid();
     const Sched sc = build_schedule(p, s_start, s_red);
     publish_schedule(p, sc, s_start);
-    for (int item = blockIdx.x; item < sc.total_items; item = next_item(p, item, s_flag + 1)) {
-        const int s = find_seq(s_start, p.S, item);
-        const int local = item - s_start[s];
+    const int n_sh = SHARED ? p.n_shared_items : 0;
+    for (int item = blockIdx.x; item < n_sh + sc.total_items; item = next_item(p, item, s_flag + 1)) {
+        if (SHARED && item < n_sh) {
+            const int k = item / p.Hkv, hh = item - k * p.Hkv;
+            shared_item<D>(p, p.sh_items[4 * k], hh, p.sh_items[4 * k + 1], p.sh_items[4 * k + 2],
+                           ring);
+            continue;
+        }
+        const int pitem = item - n_sh;
+        const int s = find_seq(s_start, p.S, pitem);
+        const int local = pitem - s_start[s];
         const int part = local / p.Hkv, h = local - part * p.Hkv;
         const int L = seq_len(p, s, false);
-        const int nP = max(1, (L + sc.PT - 1) / sc.PT);
-        const int tok0 = part * sc.PT, tok1 = min(L, tok0 + sc.PT);
+        const int start = priv_start(p, s);
+        const int nP = max(1, (max(0, L - start) + sc.PT - 1) / sc.PT);
+        const int tok0 = start + part * sc.PT, tok1 = min(L, tok0 + sc.PT);
         fast_item<D>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
         __syncthreads();
         // merge the warps' softmax states (in place into warp 0's buffer)
@@ -556,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, PA_MIN_CTAS) decode_fast_kernel(cons
             }
         }
         __syncthreads();
-        finish_item(p, item, s, h, nP, res_m, res_l, sm_o, OS);
+        finish_item(p, pitem, s, h, nP, res_m, res_l, sm_o, OS);
         __syncthreads();
     }
     pa_dev::allow_next_grid();
@@ -680,21 +944,31 @@ __global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodePara
     pa_dev::allow_next_grid();
     const int s = blockIdx.x / p.Hkv, h = blockIdx.x - s * p.Hkv;
     const int PT = p.sched[0];
-    const int L = seq_len(p, s, false);
-    const int nP = max(1, (L + PT - 1) / PT);
-    if (nP == 1) return;                                    // written by the split kernel
+    const int nP = max(1, (priv_len(p, s, false) + PT - 1) / PT);
+    const int grp = p.seq_group ? p.seq_group[s] : -1;
+    if (nP == 1 && grp < 0) return;                        // written by the split kernel
     const int item0 = p.sched[2 + s] + h;                   // item of partition q: item0 + q*Hkv
+    // the sequence's shared-span partials (one per chunk of its group)
+    const int nC = grp >= 0 ? p.g_nchunks[grp] : 0;
+    const size_t slot0 = grp >= 0 ? (static_cast<size_t>(p.g_spart_base[grp]) +
+                                     static_cast<size_t>(p.seq_member[s]) * nC) * p.Hkv + h
+                                  : 0;
+    const int nAll = nP + nC;
+    // partial q < nP: private item; q >= nP: shared chunk q - nP
+    auto ml_of = [&](int q, int n) -> const float* {
+        return q < nP ? p.part_ml + ((static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv) * p.G + n) * 2
+                      : p.spart_ml + ((slot0 + static_cast<size_t>(q - nP) * p.Hkv) * p.G + n) * 2;
+    };
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int n = warp; n < p.G; n += kWarps) {
         float M = -INFINITY;
-        for (int q = lane; q < nP; q += 32)
-            M = fmaxf(M, p.part_ml[((static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv) * p.G + n) * 2]);
+        for (int q = lane; q < nAll; q += 32) M = fmaxf(M, ml_of(q, n)[0]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float l = 0.f;
         if (M != -INFINITY) {
-            for (int q = lane; q < nP; q += 32) {
-                const float* ml = p.part_ml + ((static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv) * p.G + n) * 2;
+            for (int q = lane; q < nAll; q += 32) {
+                const float* ml = ml_of(q, n);
                 l += ml[1] * pa_dev::ex2(ml[0] - M);
             }
         }
@@ -713,10 +987,12 @@ __global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodePara
         const float M = s_M[n], Lsum = s_L[n];
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (M != -INFINITY) {
-            for (int q = 0; q < nP; ++q) {
-                const size_t it = static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv;
-                const float f = pa_dev::ex2(p.part_ml[(it * p.G + n) * 2] - M);
-                const float4 a = *reinterpret_cast<const float4*>(p.part_acc + it * GD + e);
+            for (int q = 0; q < nAll; ++q) {
+                const float f = pa_dev::ex2(ml_of(q, n)[0] - M);
+                const float* src = q < nP
+                    ? p.part_acc + (static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv) * GD
+                    : p.spart_acc + (slot0 + static_cast<size_t>(q - nP) * p.Hkv) * GD;
+                const float4 a = *reinterpret_cast<const float4*>(src + e);
                 acc.x += f * a.x; acc.y += f * a.y; acc.z += f * a.z; acc.w += f * a.w;
             }
         }
@@ -728,8 +1004,8 @@ __global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodePara
     }
 }
 
-size_t fast_smem(int D, int S) {
-    return fast_front_bytes(D) + static_cast<size_t>(kWarps * 16 + 16) * sizeof(float) +
+size_t fast_smem(int D, int S, bool shared) {
+    return fast_front_bytes(D, shared) + static_cast<size_t>(kWarps * 16 + 16) * sizeof(float) +
            kWarps * sizeof(long long) + 4 * sizeof(int) + static_cast<size_t>(S + 1) * sizeof(int);
 }
 
@@ -763,12 +1039,18 @@ int plan_decode(const pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* 
     plan->threads = kThreads;
     int occ = 0;
     if (fast) {
-        plan->smem = fast_smem(D, S);
+        plan->smem = fast_smem(D, S, plan->shared);
         plan->pt_fixed = 0;
         plan->pt_min = std::max(B, (64 + B - 1) / B * B);
-        if (D == 64) occ = occupancy(decode_fast_kernel<64>, plan->smem);
-        else if (D == 128) occ = occupancy(decode_fast_kernel<128>, plan->smem);
-        else occ = occupancy(decode_fast_kernel<256>, plan->smem);
+        if (plan->shared) {
+            if (D == 64) occ = occupancy(decode_fast_kernel<64, true>, plan->smem);
+            else if (D == 128) occ = occupancy(decode_fast_kernel<128, true>, plan->smem);
+            else occ = occupancy(decode_fast_kernel<256, true>, plan->smem);
+        } else {
+            if (D == 64) occ = occupancy(decode_fast_kernel<64, false>, plan->smem);
+            else if (D == 128) occ = occupancy(decode_fast_kernel<128, false>, plan->smem);
+            else occ = occupancy(decode_fast_kernel<256, false>, plan->smem);
+        }
     } else {
         const int PT = B >= 256 ? B : (256 / B) * B;
         plan->pt_fixed = PT;
@@ -799,10 +1081,14 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
     p.pt_fixed = plan.pt_fixed;
     const dim3 grid(plan.grid), block(plan.threads);
     cudaError_t e;
-    if (plan.fast) {
-        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64>, grid, block, plan.smem, st, p);
-        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128>, grid, block, plan.smem, st, p);
-        else e = launch_pdl(decode_fast_kernel<256>, grid, block, plan.smem, st, p);
+    if (plan.fast && plan.shared) {
+        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, true>, grid, block, plan.smem, st, p);
+        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, true>, grid, block, plan.smem, st, p);
+        else e = launch_pdl(decode_fast_kernel<256, true>, grid, block, plan.smem, st, p);
+    } else if (plan.fast) {
+        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false>, grid, block, plan.smem, st, p);
+        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false>, grid, block, plan.smem, st, p);
+        else e = launch_pdl(decode_fast_kernel<256, false>, grid, block, plan.smem, st, p);
     } else if (plan.bf16) {
         e = launch_pdl(decode_simple_kernel<uint16_t>, grid, block, plan.smem, st, p);
     } else {

@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <utility>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -17,9 +18,13 @@ struct pa_pool {
     void* k = nullptr;          // K [num_blocks][kv_heads][block_size][head_dim]
     void* v = nullptr;          // V [num_blocks][kv_heads][head_dim][block_size]
     int* err = nullptr;         // device error word (first recorded PA_ERR_*)
-    void* ws = nullptr;         // decode workspace: counters, then partials
+    void* ws = nullptr;         // decode workspace: header, then partials
     size_t ws_bytes = 0;
     int num_sms = 0;
+    // shared-prefix descriptor last uploaded by pa_decode_shared (host copy + device copy)
+    std::vector<int> desc_host;
+    int* desc_dev = nullptr;
+    size_t desc_cap = 0;        // ints
 };
 
 // Everything one decode launch needs, passed by value to the kernels.
@@ -41,13 +46,21 @@ struct DecodeParams {
     int items_target;           // wanted number of work items (fast path)
     int pt_min;                 // smallest partition, tokens (multiple of B)
     int pt_fixed;               // > 0: use exactly this partition size
-};
-
-// Sizes of the decode workspace for a launch shape.
-struct DecodeWorkspace {
-    size_t counters_bytes;      // S * Hkv ints, rounded to 256
-    size_t max_items;
-    size_t bytes;               // total
+    // Shared-prefix description (pa_decode_shared); all zero / null otherwise.
+    int n_shared_items;         // shared work items, heads included (K * Hkv)
+    int chunk_tokens;           // shared tokens per item (multiple of B)
+    int members_per_tile;       // group members per item (16-row tiles of members x G)
+    const int* sh_items;        // [K][4] (group, member tile, chunk, 0)
+    const int* seq_group;       // [S] group of each sequence, -1 if none
+    const int* seq_member;      // [S] index of the sequence inside its group
+    const int* seq_start;       // [S] first private token (the shared span precedes it)
+    const int* g_members_off;   // [Ng + 1]
+    const int* g_members;       // batch indices, grouped
+    const int* g_nchunks;       // [Ng] shared chunks of each group
+    const int* g_spart_base;    // [Ng] first shared-partial slot of each group
+    const int* g_shared_tokens; // [Ng] shared tokens of each group
+    float* spart_acc;           // [slots][Hkv][G][D] shared-span partial sums
+    float* spart_ml;            // [slots][Hkv][G][2]
 };
 
 // Decode workspace header: ticket[2], 2 spare ints, then the published
@@ -85,6 +98,7 @@ int launch_copy(const pa_pool* p, const int64_t* pairs, int P, cudaStream_t st);
 
 // Decode: how the launch is shaped for a pool and batch.
 struct DecodePlan {
+    bool shared = false;        // shared-prefix items present (fast path only)
     bool fast;                  // bf16 tensor-core path
     bool bf16;                  // pool element type is bf16
     int grid, threads;

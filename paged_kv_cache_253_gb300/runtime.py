@@ -119,16 +119,24 @@ class DecodeStep:
     context_lens: torch.Tensor     # int32 [S], after the append
     scale: float
     out: torch.Tensor
+    groups: tuple = None           # (offsets, seqs, shared_blocks): decode with shared reads
 
     @property
     def num_pairs(self):
         return int(self.pairs.shape[0])
 
+    def decode(self):
+        if self.groups is not None and len(self.groups[2]):
+            return self.pool.decode_shared(self.q, self.block_tables, self.context_lens,
+                                           self.scale, self.groups, out=self.out)
+        return self.pool.decode(self.q, self.block_tables, self.context_lens, self.scale,
+                                out=self.out)
+
     def run(self):
         if self.num_pairs:
             self.pool.copy_blocks(self.pairs)
         self.pool.append_kv(self.new_k, self.new_v, self.slots)
-        self.pool.decode(self.q, self.block_tables, self.context_lens, self.scale, out=self.out)
+        self.decode()
         return self.out
 
     def launches(self):
@@ -136,11 +144,15 @@ class DecodeStep:
         return 2 + (1 if self.num_pairs else 0)
 
 
-def prepare_step(wl, values, pool, bm, out_dtype=torch.float32):
-    """Reserve the step's slots in the block manager and upload its inputs."""
+def prepare_step(wl, values, pool, bm, out_dtype=torch.float32, shared=True):
+    """Reserve the step's slots in the block manager and upload its inputs.
+
+    With ``shared`` the step decodes through pa_decode_shared whenever the block
+    manager finds batch entries that share leading blocks."""
     dev = pool.device
     slots, pairs = bm.append_slots(wl.batch, wl.step_tokens)
     tables, lens = bm.batch_tables(wl.batch)
+    groups = bm.prefix_groups(wl.batch) if shared else None
     S = wl.num_seqs
     return DecodeStep(
         pool=pool,
@@ -152,4 +164,5 @@ def prepare_step(wl, values, pool, bm, out_dtype=torch.float32):
         block_tables=torch.as_tensor(tables, device=dev),
         context_lens=torch.as_tensor(lens, device=dev),
         scale=wl.scale,
-        out=torch.empty((S, wl.num_q_heads, wl.head_dim), dtype=out_dtype, device=dev))
+        out=torch.empty((S, wl.num_q_heads, wl.head_dim), dtype=out_dtype, device=dev),
+        groups=groups)

@@ -22,9 +22,9 @@ def bits(t):
     return t.numpy()
 
 
-def run_library(wl, values, out_dtype=torch.float32):
+def run_library(wl, values, out_dtype=torch.float32, shared=True):
     pool, bm, setup_pairs = runtime.replay_setup(wl, values, "cuda")
-    step = runtime.prepare_step(wl, values, pool, bm, out_dtype=out_dtype)
+    step = runtime.prepare_step(wl, values, pool, bm, out_dtype=out_dtype, shared=shared)
     step.run()
     torch.cuda.synchronize()
     return pool, bm, setup_pairs, step

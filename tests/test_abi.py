@@ -154,3 +154,28 @@ def test_batch_tables_and_errors(lib):
         bm.append_slot(b, 0)
     assert e.value.code == lib.PA_ERR_NO_FREE_BLOCK
     assert bm.seq_len(b) == 12 and bm.num_free() == 0
+
+
+def test_prefix_groups_follow_the_tables(lib):
+    from paged_kv_cache_253_gb300.api import BlockManager
+    B = 4
+    bm = BlockManager(64, B)
+    root, _ = bm.add_request([])
+    for t in range(11):                       # 2 full blocks + 3 tokens
+        bm.append_slot(root, t)
+    kids = [bm.fork(root) for _ in range(3)]
+    other, _ = bm.add_request([])
+    for t in range(9):
+        bm.append_slot(other, t)
+    batch = [kids[0], other, root, kids[1], kids[2]]
+    for r in batch:                           # each diverges: the partial block is copied
+        bm.append_slot(r, 99)
+    offs, seqs, nsh = bm.prefix_groups(batch)
+    assert offs.tolist() == [0, 4] and seqs.tolist() == [0, 2, 3, 4] and nsh.tolist() == [2]
+    tables = [bm.block_table(r) for r in batch]
+    for i in seqs.tolist():
+        assert tables[i][:2] == tables[0][:2]
+    assert len({tables[i][2] for i in seqs.tolist()}) == 4
+    # no sharing at all: no groups
+    offs, seqs, nsh = bm.prefix_groups([other])
+    assert offs.tolist() == [0] and len(nsh) == 0

@@ -53,8 +53,8 @@ def _ids():
     return out
 
 
-def _check(wl, values, seqs=None, threads=1):
-    pool, bm, setup_pairs, step = run_library(wl, values)
+def _check(wl, values, seqs=None, threads=1, shared=True):
+    pool, bm, setup_pairs, step = run_library(wl, values, shared=shared)
     assert pool.get_error() == 0
     st = orp.replay(wl, values)
     # bookkeeping, bit-exact
@@ -184,10 +184,65 @@ def test_copy_blocks_skips_only_conflicting_pairs():
     assert pool.get_error() != 0
 
 
+# ------------------------------------------------------- shared prefix ---
+
+SHARED_CASES = [
+    ("prefix", dict(num_seqs=6, prefix_len=300, suffix_min=1, suffix_max=40, **D128)),
+    ("prefix", dict(num_seqs=70, prefix_len=1030, suffix_min=0, suffix_max=30, **D128)),
+    ("prefix", dict(num_seqs=9, prefix_len=700, suffix_min=5, suffix_max=60, num_q_heads=64,
+                    num_kv_heads=8, head_dim=128)),                              # G = 8
+    ("prefix", dict(num_seqs=5, prefix_len=500, suffix_min=1, suffix_max=9, num_q_heads=10,
+                    num_kv_heads=2, head_dim=128)),                              # G = 5
+    ("prefix", dict(num_seqs=5, prefix_len=640, suffix_min=1, suffix_max=70, block_size=32,
+                    num_q_heads=16, num_kv_heads=4, head_dim=64)),
+    ("mixed", dict(num_seqs=40, median=60, min_len=1, max_len=600, prefix_min=100,
+                   prefix_max=900, num_q_heads=64, num_kv_heads=8, head_dim=128)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SHARED_CASES, ids=[f"{n}-{i}" for i, (n, _) in enumerate(SHARED_CASES)])
+def test_shared_prefix_parity(name, kw):
+    wl = wls.make_workload(name, **kw)
+    values = wls.generate_values(wl, "cpu")
+    err, pool, step = _check(wl, values, shared=True)
+    offs, seqs, nsh = step.groups
+    assert len(nsh) >= 1 and nsh.min() >= 1, "the workload must have a shared span"
+    plain = pool.decode(step.q, step.block_tables, step.context_lens, step.scale)
+    torch.cuda.synchronize()
+    diff = (plain - step.out).abs().max().item()
+    assert diff <= 1e-4, f"shared vs plain decode differ by {diff:.3g}"
+    print(f"{name} {kw}: groups {len(nsh)} shared blocks {nsh.tolist()} max-abs {err:.3g}")
+
+
+def test_shared_description_is_checked_on_the_device():
+    from paged_kv_cache_253_gb300._lib import PA_ERR_INVALID_ARG
+    wl = wls.make_workload("prefix", num_seqs=4, prefix_len=100, suffix_min=1, suffix_max=5,
+                           **D128)
+    values = wls.generate_values(wl, "cpu")
+    pool, bm, _, step = run_library(wl, values)
+    assert pool.get_error() == 0
+    offs, seqs, nsh = step.groups
+    bad_tables = step.block_tables.clone()
+    bad_tables[int(seqs[1]), 0] = bad_tables[int(seqs[1]), 1]      # members disagree
+    pool.decode_shared(step.q, bad_tables.contiguous(), step.context_lens, step.scale,
+                       (offs, seqs, nsh))
+    assert pool.get_error() == PA_ERR_INVALID_ARG
+    from paged_kv_cache_253_gb300._lib import PagedAttnError
+    with pytest.raises(PagedAttnError):                                # beyond the table: host
+        pool.decode_shared(step.q, step.block_tables, step.context_lens, step.scale,
+                           (offs, seqs, nsh + 50))
+    assert nsh[0] + 1 <= step.block_tables.shape[1]
+    pool.decode_shared(step.q, step.block_tables, step.context_lens, step.scale,
+                       (offs, seqs, nsh + 1))                          # beyond the contexts: device
+    assert pool.get_error() == PA_ERR_INVALID_ARG
+    out = pool.decode_shared(step.q, step.block_tables, step.context_lens, step.scale,
+                             (offs, seqs, nsh))
+    torch.cuda.synchronize()
+    assert pool.get_error() == 0
+    assert torch.allclose(out, step.out, atol=1e-6, rtol=0)
+
+
 # ---------------------------------------------------------- full sizes ---
-
-FULL = ["decode", "prefix", "long", "mixed"]
-
 
 def _sample(wl, n=10):
     """Batch entries whose outputs the oracle recomputes: longest, shortest,
@@ -199,12 +254,17 @@ def _sample(wl, n=10):
     return sorted(pick)
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_parity(name):
+FULL_CASES = [("decode", False), ("long", False), ("prefix", False), ("prefix", True),
+              ("mixed", False), ("mixed", True)]
+
+
+@pytest.mark.parametrize("name,shared", FULL_CASES, ids=[f"{n}-{'shared' if s else 'plain'}"
+                                                          for n, s in FULL_CASES])
+def test_full_size_parity(name, shared):
     wl = wls.make_workload(name)
     values = wls.generate_values(wl, "cuda")
     seqs = _sample(wl)
     if name == "long":
         seqs = list(range(wl.num_seqs))
-    err, pool, step = _check(wl, values, seqs=seqs, threads=8)
-    print(f"{name}: max-abs over {len(seqs)} sampled sequences {err:.3g}")
+    err, pool, step = _check(wl, values, seqs=seqs, threads=8, shared=shared)
+    print(f"{name} shared={shared}: max-abs over {len(seqs)} sampled sequences {err:.3g}")
