@@ -150,6 +150,22 @@ int pa_decode(pa_pool *pool, const void *q, int num_seqs, int num_q_heads,
               const int32_t *context_lens, float scale, void *out, pa_dtype out_dtype,
               void *stream);
 
+/* Append then decode in one call: for each sequence s, its new token's keys
+ * and values k[s], v[s] ([S][kv_heads][head_dim], pool dtype, device) are
+ * written to slot_mapping[s] (device int64 [S]; negative = no token), exactly
+ * as pa_append_kv with T = S would, and then decode attention runs exactly as
+ * pa_decode.  Each slot must be the slot of position context_lens[s] - 1 of
+ * sequence s (the token the decode of s reads last); otherwise nothing is
+ * written for it and PA_ERR_INVALID_ARG is recorded on the device.  On the
+ * bf16 tensor-core path the write is done inside the decode kernel by the warp
+ * that reads that block (one launch fewer per step); other shapes run
+ * pa_append_kv and pa_decode back to back.  Copy-on-write copies, if any,
+ * must be issued before (pa_copy_blocks). */
+int pa_append_decode(pa_pool *pool, const void *k, const void *v, const int64_t *slot_mapping,
+                     const void *q, int num_seqs, int num_q_heads, const int32_t *block_tables,
+                     int max_blocks_per_seq, const int32_t *context_lens, float scale,
+                     void *out, pa_dtype out_dtype, void *stream);
+
 /* Size the pool's decode workspace for batches up to these bounds. */
 int pa_decode_reserve(pa_pool *pool, int max_seqs, int max_q_heads);
 

@@ -47,6 +47,8 @@ SIGNATURES = {
     "pa_decode": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_void_p, c_float,
                           c_void_p, c_int, c_void_p]),
     "pa_decode_reserve": (c_int, [c_void_p, c_int, c_int]),
+    "pa_append_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                 c_void_p, c_int, c_void_p, c_float, c_void_p, c_int, c_void_p]),
     "pa_decode_shared": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_void_p,
                                  c_float, c_void_p, c_int, c_i32p, c_i32p, c_i32p, c_int,
                                  c_void_p]),

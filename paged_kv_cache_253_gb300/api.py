@@ -106,6 +106,28 @@ class KVPool:
                             _CODE[out.dtype], _stream()), "pa_decode")
         return out
 
+    def append_decode(self, k, v, slot_mapping, q, block_tables, context_lens, scale, out=None,
+                      out_dtype=torch.float32):
+        """Write each sequence's new token (k[s], v[s] at slot_mapping[s]), then decode."""
+        S, hq, d = q.shape
+        shape = (S, self.kv_heads, self.head_dim)
+        if tuple(k.shape) != shape or tuple(v.shape) != shape or tuple(slot_mapping.shape) != (S,):
+            raise ValueError(f"k/v must be {shape}, slot_mapping [S]")
+        if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+            raise ValueError("block_tables [S, max_blocks] / context_lens [S]")
+        if out is None:
+            out = torch.empty((S, hq, d), dtype=out_dtype, device=self.device)
+        L.check(L.pa_append_decode(self.handle, _dev(k, self.dtype, "k", self.device),
+                                   _dev(v, self.dtype, "v", self.device),
+                                   _dev(slot_mapping, torch.int64, "slot_mapping", self.device),
+                                   _dev(q, self.dtype, "q", self.device), S, hq,
+                                   _dev(block_tables, torch.int32, "block_tables", self.device),
+                                   int(block_tables.shape[1]),
+                                   _dev(context_lens, torch.int32, "context_lens", self.device),
+                                   float(scale), _dev(out, out.dtype, "out", self.device),
+                                   _CODE[out.dtype], _stream()), "pa_append_decode")
+        return out
+
     def decode_shared(self, q, block_tables, context_lens, scale, groups, out=None,
                       out_dtype=torch.float32):
         """Decode with shared leading blocks read once per group.

@@ -239,10 +239,17 @@ struct SharedPlan {
     size_t off_items, off_sgroup, off_smember, off_sstart, off_goff, off_gmem, off_gnc, off_gbase, off_gtok;
 };
 
+// Fused append: the new token of each sequence (k, v [S][Hkv][D], slots [S]).
+struct NewTokens {
+    const void* k;
+    const void* v;
+    const int64_t* slots;
+};
+
 static int decode_impl(pa_pool* pool, const void* q, int num_seqs, int num_q_heads,
                        const int32_t* block_tables, int max_blocks_per_seq,
                        const int32_t* context_lens, float scale, void* out, pa_dtype out_dtype,
-                       void* stream, const SharedPlan* sh) {
+                       void* stream, const SharedPlan* sh, const NewTokens* nt = nullptr) {
     int rc = check_decode_args(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
                                context_lens, out, out_dtype);
     if (rc != PA_OK || num_seqs == 0) return rc;
@@ -251,9 +258,16 @@ static int decode_impl(pa_pool* pool, const void* q, int num_seqs, int num_q_hea
     const int G = num_q_heads / pool->kv_heads;
     pa_detail::DecodePlan plan;
     plan.shared = sh != nullptr;
+    plan.fuse = nt != nullptr && sh == nullptr;
     rc = pa_detail::plan_decode(pool, num_seqs, num_q_heads, max_blocks_per_seq, &plan);
     if (rc != PA_OK) return rc;
     if (sh && !plan.fast) return PA_ERR_UNSUPPORTED;
+    if (nt && !(plan.fast && plan.fuse)) {         // no fused form: append first, then decode
+        rc = pa_detail::launch_append(pool, nt->k, nt->v, nt->slots, num_seqs,
+                                      static_cast<cudaStream_t>(stream));
+        if (rc != PA_OK) return rc;
+        plan.fuse = false;
+    }
     size_t cb = 0;
     size_t need = workspace_bytes(plan, num_seqs, pool->kv_heads, G, pool->head_dim, &cb);
     const size_t sacc_off = need;
@@ -323,7 +337,24 @@ static int decode_impl(pa_pool* pool, const void* q, int num_seqs, int num_q_hea
     p.num_blocks = pool->num_blocks;
     p.max_blocks = max_blocks_per_seq;
     p.out_bf16 = out_dtype == PA_BF16;
+    if (plan.fast && plan.fuse) {
+        p.new_k = nt->k;
+        p.new_v = nt->v;
+        p.new_slots = nt->slots;
+    }
     return pa_detail::launch_decode(plan, p, st);
+}
+
+int pa_append_decode(pa_pool* pool, const void* k, const void* v, const int64_t* slot_mapping,
+                     const void* q, int num_seqs, int num_q_heads, const int32_t* block_tables,
+                     int max_blocks_per_seq, const int32_t* context_lens, float scale, void* out,
+                     pa_dtype out_dtype, void* stream) {
+    if (num_seqs > 0 && (!k || !v || !slot_mapping || !aligned(slot_mapping, 8) ||
+                         !aligned(k, 16) || !aligned(v, 16)))
+        return PA_ERR_INVALID_ARG;
+    const NewTokens nt{k, v, slot_mapping};
+    return decode_impl(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                       context_lens, scale, out, out_dtype, stream, nullptr, &nt);
 }
 
 int pa_decode(pa_pool* pool, const void* q, int num_seqs, int num_q_heads,

@@ -36,6 +36,7 @@
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -353,7 +354,7 @@ __device__ __forceinline__ void cp_async_wait() {
 // ahead of the unit being computed, so each warp keeps several tiles in
 // flight.  K rows are stored with 16-byte chunk c of odd rows at c ^ 4, which
 // makes the fragment reads below bank-conflict free.
-template <int D>
+template <int D, bool FUSE>
 __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, int tok0,
                                           int tok1, int L, unsigned char* ring, float* sm_o,
                                           float* sm_m, float* sm_l) {
@@ -459,39 +460,82 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
     }
     cp_async_wait<0>();
 #else
-    int my_phys = -1;
-    for (int i = 0; i < nblk; ++i) {
-        const int lb = lb0 + warp + kWarps * i;
-        if ((i & 31) == 0) {
-            const int mine = lb + lane * kWarps;
-            my_phys = mine < lb1 ? __ldg(table + mine) : -1;
-        }
-        const int phys = __shfl_sync(0xffffffffu, my_phys, i & 31);
-        if (phys < 0 || phys >= p.num_blocks) {
-            if (lane == 0) record_error(p.err, PA_ERR_BAD_BLOCK_ID);
-            continue;
-        }
-        const size_t tile = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems;
-        for (int sub = 0; sub < nsub; ++sub) {
-            const int nvalid = min(16, L - (lb * B + sub * 16));
-            if (nvalid <= 0) break;
-            const uint16_t* kt = kpool + tile + static_cast<size_t>(sub) * 16 * D;
-            const uint16_t* vt = vpool + tile + sub * 16 + 4 * c;
-            uint4 k0[NJ], k1[NJ];
-            uint2 v0[NT], v1[NT];
-#pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                k0[j] = pa_dev::ld_stream16(kt + r0 * D + (4 * j + c) * 8);
-                k1[j] = pa_dev::ld_stream16(kt + r1 * D + (4 * j + c) * 8);
-            }
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                v0[t] = pa_dev::ld_stream8(vt + static_cast<size_t>(16 * t + g) * B);
-                v1[t] = pa_dev::ld_stream8(vt + static_cast<size_t>(16 * t + g + 8) * B);
-            }
-            tile_update<D>(a, k0, k1, v0, v1, nvalid, sl, r0, r1, c);
-        }
+    // Fused append: the warp that reads the block holding position L-1 first
+    // writes the sequence's new token there (key row, value column), then
+    // reads that block through L2 so it sees its own writes.
+    constexpr int VPL = D / 32;                   // value elements per lane
+    const int lb_last = L > 0 ? (L - 1) / B : -1;
+    const bool own_new = FUSE && lb_last >= lb0 && lb_last < lb1 &&
+                         (lb_last - lb0) % kWarps == warp;
+    const size_t new_row = (static_cast<size_t>(s) * p.Hkv + h) * D;
+    if (own_new && lane < 2 * D * 2 / 128) {      // start the new token's rows towards L2
+        const char* src = static_cast<const char*>(lane < D * 2 / 128 ? p.new_k : p.new_v) +
+                          new_row * 2 + (lane % (D * 2 / 128)) * 128;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
     }
+    auto walk = [&](auto cg_tag) {
+        constexpr bool CG = decltype(cg_tag)::value;
+        int my_phys = -1;
+        for (int i = 0; i < nblk; ++i) {
+            const int lb = lb0 + warp + kWarps * i;
+            if ((i & 31) == 0) {
+                const int mine = lb + lane * kWarps;
+                my_phys = mine < lb1 ? __ldg(table + mine) : -1;
+            }
+            const int phys = __shfl_sync(0xffffffffu, my_phys, i & 31);
+            if (phys < 0 || phys >= p.num_blocks) {
+                if (lane == 0) record_error(p.err, PA_ERR_BAD_BLOCK_ID);
+                continue;
+            }
+            const size_t tile = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems;
+            if (own_new && lb == lb_last) {
+                const int64_t new_slot = __ldg(p.new_slots + s);
+                const int off = (L - 1) - lb * B;
+                if (new_slot >= 0 && new_slot != static_cast<int64_t>(phys) * B + off) {
+                    if (lane == 0) record_error(p.err, PA_ERR_INVALID_ARG);   // not this sequence's slot
+                } else if (new_slot >= 0) {
+                    const uint16_t* ks = static_cast<const uint16_t*>(p.new_k) + new_row;
+                    const uint16_t* vs = static_cast<const uint16_t*>(p.new_v) + new_row;
+                    uint16_t* kw = const_cast<uint16_t*>(kpool) + tile + static_cast<size_t>(off) * D;
+                    uint16_t* vw = const_cast<uint16_t*>(vpool) + tile + off;
+                    if (lane < D / 8)
+                        *reinterpret_cast<uint4*>(kw + lane * 8) = __ldg(reinterpret_cast<const uint4*>(ks + lane * 8));
+    #pragma unroll
+                    for (int e = 0; e < VPL; ++e)
+                        vw[static_cast<size_t>(lane * VPL + e) * B] = __ldg(vs + lane * VPL + e);
+                }
+                __syncwarp();
+            }
+            for (int sub = 0; sub < nsub; ++sub) {
+                const int nvalid = min(16, L - (lb * B + sub * 16));
+                if (nvalid <= 0) break;
+                const uint16_t* kt = kpool + tile + static_cast<size_t>(sub) * 16 * D;
+                const uint16_t* vt = vpool + tile + sub * 16 + 4 * c;
+                uint4 k0[NJ], k1[NJ];
+                uint2 v0[NT], v1[NT];
+                // the warp that wrote the new token loads through L2 (ld.global.cg) so
+                // it sees its own writes; every other warp uses the read-only path
+    #pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    k0[j] = CG ? pa_dev::ld_cg16(kt + r0 * D + (4 * j + c) * 8)
+                                 : pa_dev::ld_stream16(kt + r0 * D + (4 * j + c) * 8);
+                    k1[j] = CG ? pa_dev::ld_cg16(kt + r1 * D + (4 * j + c) * 8)
+                                 : pa_dev::ld_stream16(kt + r1 * D + (4 * j + c) * 8);
+                }
+    #pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    v0[t] = CG ? pa_dev::ld_cg8(vt + static_cast<size_t>(16 * t + g) * B)
+                                 : pa_dev::ld_stream8(vt + static_cast<size_t>(16 * t + g) * B);
+                    v1[t] = CG ? pa_dev::ld_cg8(vt + static_cast<size_t>(16 * t + g + 8) * B)
+                                 : pa_dev::ld_stream8(vt + static_cast<size_t>(16 * t + g + 8) * B);
+                }
+                tile_update<D>(a, k0, k1, v0, v1, nvalid, sl, r0, r1, c);
+            }
+        }
+    };
+    // only the warp that writes the new token needs loads that see it
+    if (own_new) walk(std::true_type{});
+    else walk(std::false_type{});
 #endif
     float l0 = a.l0, l1 = a.l1;
 #pragma unroll
@@ -761,7 +805,7 @@ __device__ __forceinline__ size_t warp_ring_offset(int D) {
     return static_cast<size_t>(threadIdx.x >> 5) * PA_STAGES * 64 * D;
 }
 
-template <int D, bool SHARED>
+template <int D, bool SHARED, bool FUSE>
 __global__ void __launch_bounds__(kThreads, SHARED ? 2 : PA_MIN_CTAS)
 decode_fast_kernel(const DecodeParams p) {
     constexpr int OS = D + 4;
@@ -796,7 +840,7 @@ decode_fast_kernel(const DecodeParams p) {
         const int start = priv_start(p, s);
         const int nP = max(1, (max(0, L - start) + sc.PT - 1) / sc.PT);
         const int tok0 = start + part * sc.PT, tok1 = min(L, tok0 + sc.PT);
-        fast_item<D>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
+        fast_item<D, FUSE>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
         __syncthreads();
         // merge the warps' softmax states (in place into warp 0's buffer)
         for (int idx = threadIdx.x; idx < p.G * D; idx += kThreads) {
@@ -1043,13 +1087,17 @@ int plan_decode(const pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* 
         plan->pt_fixed = 0;
         plan->pt_min = std::max(B, (64 + B - 1) / B * B);
         if (plan->shared) {
-            if (D == 64) occ = occupancy(decode_fast_kernel<64, true>, plan->smem);
-            else if (D == 128) occ = occupancy(decode_fast_kernel<128, true>, plan->smem);
-            else occ = occupancy(decode_fast_kernel<256, true>, plan->smem);
+            if (D == 64) occ = occupancy(decode_fast_kernel<64, true, false>, plan->smem);
+            else if (D == 128) occ = occupancy(decode_fast_kernel<128, true, false>, plan->smem);
+            else occ = occupancy(decode_fast_kernel<256, true, false>, plan->smem);
+        } else if (plan->fuse) {
+            if (D == 64) occ = occupancy(decode_fast_kernel<64, false, true>, plan->smem);
+            else if (D == 128) occ = occupancy(decode_fast_kernel<128, false, true>, plan->smem);
+            else occ = occupancy(decode_fast_kernel<256, false, true>, plan->smem);
         } else {
-            if (D == 64) occ = occupancy(decode_fast_kernel<64, false>, plan->smem);
-            else if (D == 128) occ = occupancy(decode_fast_kernel<128, false>, plan->smem);
-            else occ = occupancy(decode_fast_kernel<256, false>, plan->smem);
+            if (D == 64) occ = occupancy(decode_fast_kernel<64, false, false>, plan->smem);
+            else if (D == 128) occ = occupancy(decode_fast_kernel<128, false, false>, plan->smem);
+            else occ = occupancy(decode_fast_kernel<256, false, false>, plan->smem);
         }
     } else {
         const int PT = B >= 256 ? B : (256 / B) * B;
@@ -1082,13 +1130,17 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
     const dim3 grid(plan.grid), block(plan.threads);
     cudaError_t e;
     if (plan.fast && plan.shared) {
-        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, true>, grid, block, plan.smem, st, p);
-        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, true>, grid, block, plan.smem, st, p);
-        else e = launch_pdl(decode_fast_kernel<256, true>, grid, block, plan.smem, st, p);
+        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, true, false>, grid, block, plan.smem, st, p);
+        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, true, false>, grid, block, plan.smem, st, p);
+        else e = launch_pdl(decode_fast_kernel<256, true, false>, grid, block, plan.smem, st, p);
+    } else if (plan.fast && plan.fuse) {
+        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, true>, grid, block, plan.smem, st, p);
+        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, true>, grid, block, plan.smem, st, p);
+        else e = launch_pdl(decode_fast_kernel<256, false, true>, grid, block, plan.smem, st, p);
     } else if (plan.fast) {
-        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false>, grid, block, plan.smem, st, p);
-        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false>, grid, block, plan.smem, st, p);
-        else e = launch_pdl(decode_fast_kernel<256, false>, grid, block, plan.smem, st, p);
+        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, false>, grid, block, plan.smem, st, p);
+        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, false>, grid, block, plan.smem, st, p);
+        else e = launch_pdl(decode_fast_kernel<256, false, false>, grid, block, plan.smem, st, p);
     } else if (plan.bf16) {
         e = launch_pdl(decode_simple_kernel<uint16_t>, grid, block, plan.smem, st, p);
     } else {

@@ -61,6 +61,11 @@ struct DecodeParams {
     const int* g_shared_tokens; // [Ng] shared tokens of each group
     float* spart_acc;           // [slots][Hkv][G][D] shared-span partial sums
     float* spart_ml;            // [slots][Hkv][G][2]
+    // Fused append (pa_append_decode): each sequence's new token, written by
+    // the warp that reads the sequence's last block; null otherwise.
+    const void* new_k;          // [S][Hkv][D]
+    const void* new_v;          // [S][Hkv][D]
+    const int64_t* new_slots;   // [S] slot of position L-1 of each sequence, or < 0
 };
 
 // Decode workspace header: ticket[2], 2 spare ints, then the published
@@ -99,6 +104,7 @@ int launch_copy(const pa_pool* p, const int64_t* pairs, int P, cudaStream_t st);
 // Decode: how the launch is shaped for a pool and batch.
 struct DecodePlan {
     bool shared = false;        // shared-prefix items present (fast path only)
+    bool fuse = false;          // the decode kernel also appends each sequence's new token
     bool fast;                  // bf16 tensor-core path
     bool bf16;                  // pool element type is bf16
     int grid, threads;

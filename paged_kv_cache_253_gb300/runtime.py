@@ -120,6 +120,7 @@ class DecodeStep:
     scale: float
     out: torch.Tensor
     groups: tuple = None           # (offsets, seqs, shared_blocks): decode with shared reads
+    fused: bool = True             # append inside the decode kernel when there is no sharing
 
     @property
     def num_pairs(self):
@@ -132,19 +133,27 @@ class DecodeStep:
         return self.pool.decode(self.q, self.block_tables, self.context_lens, self.scale,
                                 out=self.out)
 
+    def sharing(self):
+        return self.groups is not None and len(self.groups[2]) > 0
+
     def run(self):
         if self.num_pairs:
             self.pool.copy_blocks(self.pairs)
+        if self.fused and not self.sharing():
+            self.pool.append_decode(self.new_k, self.new_v, self.slots, self.q, self.block_tables,
+                                    self.context_lens, self.scale, out=self.out)
+            return self.out
         self.pool.append_kv(self.new_k, self.new_v, self.slots)
         self.decode()
         return self.out
 
     def launches(self):
-        """Library calls per step (pa_decode itself launches two kernels)."""
-        return 2 + (1 if self.num_pairs else 0)
+        """Kernels per step: [copy] + [append] + decode split + merge."""
+        fused = self.fused and not self.sharing()
+        return (1 if self.num_pairs else 0) + (0 if fused else 1) + 2
 
 
-def prepare_step(wl, values, pool, bm, out_dtype=torch.float32, shared=True):
+def prepare_step(wl, values, pool, bm, out_dtype=torch.float32, shared=True, fused=True):
     """Reserve the step's slots in the block manager and upload its inputs.
 
     With ``shared`` the step decodes through pa_decode_shared whenever the block
@@ -165,4 +174,4 @@ def prepare_step(wl, values, pool, bm, out_dtype=torch.float32, shared=True):
         context_lens=torch.as_tensor(lens, device=dev),
         scale=wl.scale,
         out=torch.empty((S, wl.num_q_heads, wl.head_dim), dtype=out_dtype, device=dev),
-        groups=groups)
+        groups=groups, fused=fused)

@@ -22,9 +22,10 @@ def bits(t):
     return t.numpy()
 
 
-def run_library(wl, values, out_dtype=torch.float32, shared=True):
+def run_library(wl, values, out_dtype=torch.float32, shared=True, fused=True):
     pool, bm, setup_pairs = runtime.replay_setup(wl, values, "cuda")
-    step = runtime.prepare_step(wl, values, pool, bm, out_dtype=out_dtype, shared=shared)
+    step = runtime.prepare_step(wl, values, pool, bm, out_dtype=out_dtype, shared=shared,
+                                fused=fused)
     step.run()
     torch.cuda.synchronize()
     return pool, bm, setup_pairs, step

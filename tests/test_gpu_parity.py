@@ -184,6 +184,37 @@ def test_copy_blocks_skips_only_conflicting_pairs():
     assert pool.get_error() != 0
 
 
+@pytest.mark.parametrize("name,kw", [SMALL[1], SMALL[5], SMALL[8], SMALL[11], SMALL[12],
+                                     SMALL[13]], ids=lambda x: str(x)[:40])
+def test_fused_append_matches_separate_calls(name, kw):
+    """pa_append_decode leaves the same pool bits and output as pa_append_kv
+    followed by pa_decode."""
+    wl = wls.make_workload(name, **kw)
+    values = wls.generate_values(wl, "cpu")
+    outs, pools = [], []
+    for fused in (False, True):
+        pool, bm, _, step = run_library(wl, values, shared=False, fused=fused)
+        assert pool.get_error() == 0
+        outs.append(step.out.clone())
+        pools.append(pool.export())
+    torch.cuda.synchronize()
+    assert torch.equal(pools[0][0], pools[1][0]) and torch.equal(pools[0][1], pools[1][1])
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_fused_append_rejects_a_foreign_slot():
+    from paged_kv_cache_253_gb300._lib import PA_ERR_INVALID_ARG
+    wl = wls.make_workload("decode", num_seqs=3, min_len=20, max_len=60, **D128)
+    values = wls.generate_values(wl, "cpu")
+    pool, bm, _, step = run_library(wl, values)
+    assert pool.get_error() == 0
+    wrong = step.slots.clone()
+    wrong[0], wrong[1] = step.slots[1], step.slots[0]
+    pool.append_decode(step.new_k, step.new_v, wrong, step.q, step.block_tables,
+                       step.context_lens, step.scale)
+    assert pool.get_error() == PA_ERR_INVALID_ARG
+
+
 # ------------------------------------------------------- shared prefix ---
 
 SHARED_CASES = [
