@@ -1003,6 +1003,10 @@ __global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodePara
         return q < nP ? p.part_ml + ((static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv) * p.G + n) * 2
                       : p.spart_ml + ((slot0 + static_cast<size_t>(q - nP) * p.Hkv) * p.G + n) * 2;
     };
+    // phase 1: per head, the running maxima and sums of all partitions give the
+    // merged max M, the merged sum L and one weight 2^(m_q - M) per partition
+    constexpr int kQ = 256;                                 // weights kept in shared memory
+    __shared__ float s_f[kQ][16];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int n = warp; n < p.G; n += kWarps) {
         float M = -INFINITY;
@@ -1010,11 +1014,11 @@ __global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodePara
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float l = 0.f;
-        if (M != -INFINITY) {
-            for (int q = lane; q < nAll; q += 32) {
-                const float* ml = ml_of(q, n);
-                l += ml[1] * pa_dev::ex2(ml[0] - M);
-            }
+        for (int q = lane; q < nAll; q += 32) {
+            const float* ml = ml_of(q, n);
+            const float f = M != -INFINITY ? pa_dev::ex2(ml[0] - M) : 0.f;
+            l += ml[1] * f;
+            if (q < kQ) s_f[q][n] = f;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
@@ -1024,6 +1028,7 @@ __global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodePara
         }
     }
     __syncthreads();
+    // phase 2: weighted sum of the partial accumulators, 4 values per thread
     const int GD = p.G * p.D;
     const size_t out0 = (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G) * p.D;
     for (int e = threadIdx.x * 4; e < GD; e += kThreads * 4) {   // D % 4 == 0: never splits a head
@@ -1031,12 +1036,13 @@ __global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodePara
         const float M = s_M[n], Lsum = s_L[n];
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (M != -INFINITY) {
+#pragma unroll 4
             for (int q = 0; q < nAll; ++q) {
-                const float f = pa_dev::ex2(ml_of(q, n)[0] - M);
+                const float f = q < kQ ? s_f[q][n] : pa_dev::ex2(ml_of(q, n)[0] - M);
                 const float* src = q < nP
                     ? p.part_acc + (static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv) * GD
                     : p.spart_acc + (slot0 + static_cast<size_t>(q - nP) * p.Hkv) * GD;
-                const float4 a = *reinterpret_cast<const float4*>(src + e);
+                const float4 a = __ldcg(reinterpret_cast<const float4*>(src + e));
                 acc.x += f * a.x; acc.y += f * a.y; acc.z += f * a.z; acc.w += f * a.w;
             }
         }
