@@ -153,15 +153,32 @@ class DecodeStep:
         return (1 if self.num_pairs else 0) + (0 if fused else 1) + 2
 
 
-def prepare_step(wl, values, pool, bm, out_dtype=torch.float32, shared=True, fused=True):
+SHARED_MIN_FRACTION = 0.5
+
+
+def shared_fraction(groups, lens, block_size):
+    """Fraction of a step's logical KV reads that fall in shared spans."""
+    offs, seqs, nsh = groups
+    shared = sum((int(offs[g + 1]) - int(offs[g])) * int(nsh[g]) * block_size
+                 for g in range(len(nsh)))
+    return shared / max(1, int(np.asarray(lens).sum()))
+
+
+def prepare_step(wl, values, pool, bm, out_dtype=torch.float32, shared="auto", fused=True):
     """Reserve the step's slots in the block manager and upload its inputs.
 
-    With ``shared`` the step decodes through pa_decode_shared whenever the block
-    manager finds batch entries that share leading blocks."""
+    shared=True decodes through pa_decode_shared whenever the block manager
+    finds batch entries that share leading blocks; "auto" does so only when the
+    shared spans are at least SHARED_MIN_FRACTION of the step's logical KV
+    reads (below that, L2 already absorbs the repeated reads and the plain
+    kernel's higher occupancy wins, as measured on the mixed workload)."""
     dev = pool.device
     slots, pairs = bm.append_slots(wl.batch, wl.step_tokens)
     tables, lens = bm.batch_tables(wl.batch)
     groups = bm.prefix_groups(wl.batch) if shared else None
+    if shared == "auto" and groups is not None and \
+            shared_fraction(groups, lens, wl.block_size) < SHARED_MIN_FRACTION:
+        groups = None
     S = wl.num_seqs
     return DecodeStep(
         pool=pool,
