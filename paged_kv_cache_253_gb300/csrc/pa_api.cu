@@ -3,6 +3,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -231,6 +232,7 @@ int pa_decode_reserve(pa_pool* pool, int max_seqs, int max_q_heads) {
 
 // Host plan of the shared-prefix items (see pa_decode_shared).
 struct SharedPlan {
+    bool tc = false;            // shared items on the tcgen05 kernel (128-row tiles)
     int num_groups = 0;
     int K = 0;                  // items before expanding over KV heads
     int slots = 0;              // shared-partial slots (members x chunks)
@@ -259,6 +261,7 @@ static int decode_impl(pa_pool* pool, const void* q, int num_seqs, int num_q_hea
     pa_detail::DecodePlan plan;
     plan.shared = sh != nullptr;
     plan.fuse = nt != nullptr && sh == nullptr;
+    plan.tc = sh != nullptr && sh->tc;
     rc = pa_detail::plan_decode(pool, num_seqs, num_q_heads, max_blocks_per_seq, &plan);
     if (rc != PA_OK) return rc;
     if (sh && !plan.fast) return PA_ERR_UNSUPPORTED;
@@ -399,7 +402,11 @@ int pa_decode_shared(pa_pool* pool, const void* q, int num_seqs, int num_q_heads
                            context_lens, scale, out, out_dtype, stream, nullptr);
     SharedPlan sh;
     sh.num_groups = static_cast<int>(keep.size());
-    sh.members_per_tile = std::max(1, 64 / G);
+    // tcgen05 items take 128 query rows; the mma.sync variant 64 (PA_SHARED_MMA_SYNC=1
+    // in the environment selects it, for comparison)
+    const char* force_sync = std::getenv("PA_SHARED_MMA_SYNC");
+    sh.tc = pa_detail::shared_tc_eligible(pool, G) && !(force_sync && force_sync[0] == '1');
+    sh.members_per_tile = std::max(1, (sh.tc ? pa_detail::shared_tc_rows() : 64) / G);
     sh.chunk_tokens = std::max(B, 512 / B * B);
     const int Ng = sh.num_groups;
     std::vector<int> items, sgroup(num_seqs, -1), smember(num_seqs, 0), sstart(num_seqs, 0);

@@ -1085,14 +1085,15 @@ int plan_decode(const pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* 
     const bool fast = pool->dtype == PA_BF16 && (D == 64 || D == 128 || D == 256) &&
                       B % 16 == 0 && G <= 8;
     plan->fast = fast;
+    plan->pool = pool;
     plan->bf16 = pool->dtype == PA_BF16;
     plan->threads = kThreads;
     int occ = 0;
     if (fast) {
-        plan->smem = fast_smem(D, S, plan->shared);
+        plan->smem = fast_smem(D, S, plan->shared && !plan->tc);
         plan->pt_fixed = 0;
         plan->pt_min = std::max(B, (64 + B - 1) / B * B);
-        if (plan->shared) {
+        if (plan->shared && !plan->tc) {
             if (D == 64) occ = occupancy(decode_fast_kernel<64, true, false>, plan->smem);
             else if (D == 128) occ = occupancy(decode_fast_kernel<128, true, false>, plan->smem);
             else occ = occupancy(decode_fast_kernel<256, true, false>, plan->smem);
@@ -1135,7 +1136,16 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
     p.pt_fixed = plan.pt_fixed;
     const dim3 grid(plan.grid), block(plan.threads);
     cudaError_t e;
-    if (plan.fast && plan.shared) {
+    if (plan.fast && plan.shared && plan.tc) {
+        // shared items on tcgen05 first, then the private spans on the plain split kernel
+        const int rc = launch_shared_tc(plan.pool, p, st);
+        if (rc != PA_OK) return rc;
+        DecodeParams q = p;
+        q.n_shared_items = 0;
+        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, false>, grid, block, plan.smem, st, q);
+        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, false>, grid, block, plan.smem, st, q);
+        else e = launch_pdl(decode_fast_kernel<256, false, false>, grid, block, plan.smem, st, q);
+    } else if (plan.fast && plan.shared) {
         if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, true, false>, grid, block, plan.smem, st, p);
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, true, false>, grid, block, plan.smem, st, p);
         else e = launch_pdl(decode_fast_kernel<256, true, false>, grid, block, plan.smem, st, p);

@@ -105,6 +105,8 @@ int launch_copy(const pa_pool* p, const int64_t* pairs, int P, cudaStream_t st);
 struct DecodePlan {
     bool shared = false;        // shared-prefix items present (fast path only)
     bool fuse = false;          // the decode kernel also appends each sequence's new token
+    bool tc = false;            // shared items run in the tcgen05 kernel before the split pass
+    const pa_pool* pool = nullptr;
     bool fast;                  // bf16 tensor-core path
     bool bf16;                  // pool element type is bf16
     int grid, threads;
@@ -114,5 +116,10 @@ struct DecodePlan {
 };
 int plan_decode(const pa_pool* p, int S, int Hq, int max_blocks, DecodePlan* plan);
 int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t st);
+
+// tcgen05 shared-prefix items (pa_shared_tc.cu).
+bool shared_tc_eligible(const pa_pool* pool, int G);
+int shared_tc_rows();
+int launch_shared_tc(const pa_pool* pool, const DecodeParams& p, cudaStream_t st);
 
 }  // namespace pa_detail

@@ -1,0 +1,343 @@
+// Shared-prefix decode items on the 5th-generation tensor cores (tcgen05).
+//
+// For a group of requests whose block tables start with the same physical
+// blocks (zenaique prefix-sharing answer: requests with one prefix point at one
+// copy; kgptalkie "Day 28", "Prefix Sharing Is a Natural Extension"), every
+// query of every member attends to the shared span.  Stacked, those queries
+// form a real dense contraction: 128 query rows (members x their G heads) of
+// one KV head against the span's keys, read once per 128 rows.
+//
+// One CTA (4 warps, 128 threads) takes an item = (group, KV head, tile of
+// 128 / G members, chunk of 512 shared tokens) and walks it in 64-token steps:
+//   S[128 x 64]   = Q[128 x 128] . K^T           tcgen05.mma, fp32 in TMEM cols [0,64)
+//   softmax       thread t owns query row t = TMEM lane t (tcgen05.ld), exp2 in
+//                 fp32 with a reference maximum that is raised only when a row's
+//                 maximum grows by more than 2^8 (then O is rescaled in TMEM)
+//   O[128 x 128] += P[128 x 64] . V[64 x 128]    tcgen05.mma, fp32 in TMEM cols [128,256),
+//                 P entering as a bf16 high part plus a bf16 low part
+// Q, K (64 tokens x 128 d) and V^T (128 d x 64 tokens) are staged with cp.async
+// into 128-byte-swizzled K-major shared-memory tiles (two K/V stages); P goes
+// from registers to TMEM (tcgen05.st) and feeds the value product from there, so
+// a CTA needs ~99 KB of shared memory and two fit on an SM; one thread
+// issues the MMAs and commits them to an mbarrier that the others wait on
+// (every wait bounded: on timeout the item records PA_ERR_CUDA and the CTA stops).
+// Each row's (acc, max, sum) goes to the same shared-partial slot the merge
+// kernel reads for the mma.sync variant.
+#include <cstdint>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_tc.cuh"
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kD = 128;                  // head_dim of this path
+constexpr int kRows = 128;               // M: query rows per item
+constexpr int kStep = 64;                // tokens per step (N of S, K of P.V)
+constexpr int kTmemCols = 256;           // S [0,64), O [64,192), P hi [192,224), P lo [224,256)
+constexpr uint32_t kWaitLimit = 1u << 26;
+
+// shared-memory map (offsets from a 1024-aligned base); ~99 KB, two CTAs per SM
+constexpr uint32_t kQOff = 0;                            // 2 regions x [128 rows][128 B]
+constexpr uint32_t kStageOff = 32768;                    // stage s: K (2 x [64][128 B]) then V^T ([128][128 B])
+constexpr uint32_t kStageBytes = 32768;
+constexpr uint32_t kMiscOff = kStageOff + 2 * kStageBytes;   // mbarriers, TMEM slot, table slice
+constexpr uint32_t kSmemBytes = kMiscOff + 256 + 1024;   // + alignment slack
+
+constexpr uint32_t kIdescQK = pa_tc::idesc_bf16_f32(kRows, kStep);
+constexpr uint32_t kIdescPV = pa_tc::idesc_bf16_f32(kRows, kD);
+
+__device__ __forceinline__ float exp2_approx(float x) { return pa_dev::ex2(x); }
+
+__device__ __forceinline__ int seq_len(const DecodeParams& p, int s) {
+    const int L = __ldg(p.lens + s);
+    return L < 0 ? 0 : min(L, p.max_blocks * p.B);
+}
+
+__global__ void __launch_bounds__(kThreads, 2) shared_tc_kernel(const DecodeParams p) {
+    extern __shared__ unsigned char tc_raw[];
+    const uint32_t raw_s = pa_tc::smem_u32(tc_raw);
+    unsigned char* base = tc_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sbase = pa_tc::smem_u32(base);
+    uint64_t* bar_s = reinterpret_cast<uint64_t*>(base + kMiscOff);
+    uint64_t* bar_pv = bar_s + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kMiscOff + 16);
+    int* s_tbl = reinterpret_cast<int*>(base + kMiscOff + 32);   // 32 block ids of a chunk
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    pa_dev::wait_prior_grid();
+    if (tid == 0) {
+        pa_tc::mbar_init(bar_s, 1);
+        pa_tc::mbar_init(bar_pv, 1);
+        pa_tc::mbar_init_fence();
+    }
+    if (warp == 0) pa_tc::tmem_alloc<kTmemCols>(tslot);
+    pa_tc::fence_before_sync();
+    __syncthreads();
+    pa_tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tS = tmem, tO = tmem + 64, tPh = tmem + 192, tPl = tmem + 224;
+    const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;   // this warp's TMEM lanes
+    uint32_t ph_s = 0, ph_pv = 0;
+    bool ok = true;
+
+    const int G = p.G, B = p.B, Hkv = p.Hkv;
+    const uint16_t* kpool = static_cast<const uint16_t*>(p.k);
+    const uint16_t* vpool = static_cast<const uint16_t*>(p.v);
+    const uint16_t* qg = static_cast<const uint16_t*>(p.q);
+    const size_t tile_elems = static_cast<size_t>(B) * kD;
+    const float sl = p.scale_log2;
+
+    for (int item = blockIdx.x; ok && item < p.n_shared_items; item += gridDim.x) {
+        const int k = item / Hkv, h = item - k * Hkv;
+        const int grp = p.sh_items[4 * k], tile = p.sh_items[4 * k + 1], chunk = p.sh_items[4 * k + 2];
+        const int moff = p.g_members_off[grp];
+        const int M = p.g_members_off[grp + 1] - moff;
+        const int mpt = p.members_per_tile;
+        const int m0 = tile * mpt, m1 = min(M, m0 + mpt);
+        const int shared_tok = p.g_shared_tokens[grp];
+        const int t0 = chunk * p.chunk_tokens, t1 = min(shared_tok, t0 + p.chunk_tokens);
+        const int nsteps = (t1 - t0 + kStep - 1) / kStep;
+        const int nC = p.g_nchunks[grp];
+        const int32_t* table = p.tables + static_cast<size_t>(p.g_members[moff]) * p.max_blocks;
+        const int lbc = t0 / B, nbc = (t1 - t0) / B;
+
+        // validation (recorded, never trapped): members cover the span and agree
+        if (chunk == 0 && tid < m1 - m0 && seq_len(p, p.g_members[moff + m0 + tid]) < shared_tok)
+            pa_dev::record_error(p.err, PA_ERR_INVALID_ARG);
+        for (int e = tid; e < (m1 - m0) * nbc; e += kThreads) {
+            const int mi = e / nbc, bi = e - mi * nbc;
+            const int32_t* mt = p.tables + static_cast<size_t>(p.g_members[moff + m0 + mi]) * p.max_blocks;
+            if (__ldg(mt + lbc + bi) != __ldg(table + lbc + bi))
+                pa_dev::record_error(p.err, PA_ERR_INVALID_ARG);
+        }
+        if (tid < nbc) {
+            int b = __ldg(table + lbc + tid);
+            if (b < 0 || b >= p.num_blocks) {
+                pa_dev::record_error(p.err, PA_ERR_BAD_BLOCK_ID);
+                b = -1;
+            }
+            s_tbl[tid] = b;
+        }
+
+        // this thread's query row
+        const int row_m = m0 + tid / G, row_n = tid - (tid / G) * G;
+        const bool row_ok = tid < mpt * G && row_m < m1;
+        const int row_s = row_ok ? p.g_members[moff + row_m] : 0;
+
+        // Q tile: 128 rows x 16 chunks of 16 B, zero rows where no query
+        for (int idx = tid; idx < kRows * 16; idx += kThreads) {
+            const int r = idx >> 4, c16 = idx & 15;
+            const int rm = m0 + r / G, rn = r - (r / G) * G;
+            const bool v = r < mpt * G && rm < m1;
+            const uint16_t* src = qg + (v ? ((static_cast<size_t>(p.g_members[moff + rm]) * p.Hq +
+                                              static_cast<size_t>(h) * G + rn) * kD + c16 * 8)
+                                          : 0);
+            pa_tc::cp16(sbase + kQOff + (c16 >> 3) * 16384 + pa_tc::sw128_off(r, c16 & 7), src,
+                        v ? 16u : 0u);
+        }
+        pa_tc::cp_commit();
+        __syncthreads();                                   // s_tbl visible
+
+        // Each thread copies a fixed 16-byte column of every tile: K chunk c16 of
+        // tokens tr + 8i, V^T chunk cv (8 tokens) of rows dr + 16i.  Block sizes are
+        // powers of two, so block and offset come from shifts and masks.
+        const int lgB = __ffs(B) - 1;
+        const int c16 = tid & 15, tr = tid >> 4;
+        const int cv = tid & 7, dr = tid >> 3;
+        auto load_step = [&](int j) {
+            const uint32_t st = sbase + kStageOff + (j & 1) * kStageBytes;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {                                  // K: 64 tokens x 16 chunks
+                const int rel = j * kStep + tr + 8 * i;                    // token offset inside the chunk
+                const bool v = t0 + rel < t1;
+                const int phys = v ? s_tbl[rel >> lgB] : -1;
+                const uint16_t* src = kpool + (phys >= 0 ? (static_cast<size_t>(phys) * Hkv + h) * tile_elems +
+                                                               (static_cast<size_t>(rel & (B - 1)) << 7) + c16 * 8
+                                                         : 0);
+                pa_tc::cp16(st + (c16 >> 3) * 8192 + pa_tc::sw128_off(tr + 8 * i, c16 & 7), src,
+                            phys >= 0 ? 16u : 0u);
+            }
+            {                                                              // V^T: 128 d x 8 chunks
+                const int rel = j * kStep + 8 * cv;
+                const bool v = t0 + rel < t1;
+                const int phys = v ? s_tbl[rel >> lgB] : -1;
+                const uint16_t* vb = vpool + (phys >= 0 ? (static_cast<size_t>(phys) * Hkv + h) * tile_elems +
+                                                              (rel & (B - 1))
+                                                        : 0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int d = dr + 16 * i;
+                    pa_tc::cp16(st + 16384 + pa_tc::sw128_off(d, cv), vb + (phys >= 0 ? d * B : 0),
+                                phys >= 0 ? 16u : 0u);
+                }
+            }
+            pa_tc::cp_commit();
+        };
+
+        load_step(0);
+        float m_ref = -INFINITY, l = 0.f;
+        for (int j = 0; j < nsteps && ok; ++j) {
+            const int st = j & 1;
+            if (j > 0) {                                   // P.V of step j-1 done: its stage and P are free
+                const bool w = pa_tc::mbar_wait(bar_pv, ph_pv, kWaitLimit);
+                if (!__syncthreads_and(w)) { ok = false; break; }
+                ph_pv ^= 1u;
+            }
+            if (j + 1 < nsteps) load_step(j + 1);
+            else pa_tc::cp_commit();
+            pa_tc::cp_wait<1>();
+            pa_tc::fence_smem_to_async();
+            pa_tc::fence_before_sync();
+            __syncthreads();
+            pa_tc::fence_after_sync();
+            const uint32_t kst = sbase + kStageOff + st * kStageBytes;
+            if (tid == 0) {
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint64_t a = pa_tc::sw128_desc(sbase + kQOff + (kk >> 2) * 16384 + (kk & 3) * 32);
+                    const uint64_t b = pa_tc::sw128_desc(kst + (kk >> 2) * 8192 + (kk & 3) * 32);
+                    pa_tc::mma_bf16(tS, a, b, kIdescQK, kk > 0);
+                }
+                pa_tc::commit(bar_s);
+            }
+            {
+                const bool w = pa_tc::mbar_wait(bar_s, ph_s, kWaitLimit);
+                if (!__syncthreads_and(w)) { ok = false; break; }
+            }
+            ph_s ^= 1u;
+            pa_tc::fence_after_sync();
+            float s[64];
+            {
+                float a32[32], b32[32];
+                pa_tc::tmem_ld32(tS + lane_sel, a32);
+                pa_tc::tmem_ld32(tS + lane_sel + 32, b32);
+                pa_tc::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    s[i] = a32[i];
+                    s[32 + i] = b32[i];
+                }
+            }
+            const int nvalid = min(kStep, t1 - (t0 + j * kStep));
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                s[i] = i < nvalid ? s[i] * sl : -INFINITY;
+                mx = fmaxf(mx, s[i]);
+            }
+            // raise the reference maximum only when it is far behind (or unset)
+            const bool first = m_ref == -INFINITY;
+            const bool raise = !first && mx > m_ref + 8.f;
+            if (first) m_ref = mx;
+            if (__any_sync(0xffffffffu, raise)) {          // rescale this warp's rows of O
+                const float corr = raise ? exp2_approx(m_ref - mx) : 1.f;
+                if (raise) {
+                    l *= corr;
+                    m_ref = mx;
+                }
+#pragma unroll
+                for (int cc = 0; cc < kD / 32; ++cc) {
+                    float o[32];
+                    pa_tc::tmem_ld32(tO + lane_sel + cc * 32, o);
+                    pa_tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= corr;
+                    pa_tc::tmem_st32(tO + lane_sel + cc * 32, o);
+                }
+                pa_tc::tmem_wait_st();
+            }
+            const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+            float sum = 0.f;
+            {
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = exp2_approx(s[2 * e] - ref);
+                    const float p1 = exp2_approx(s[2 * e + 1] - ref);
+                    sum += p0 + p1;
+                    hi[e] = pa_dev::pack_bf16(p0, p1);
+                    lo[e] = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(hi[e]), p1 - pa_dev::bf16_hi(hi[e]));
+                }
+                pa_tc::tmem_st32u(tPh + lane_sel, hi);         // this row of P, bf16 pairs
+                pa_tc::tmem_st32u(tPl + lane_sel, lo);
+                pa_tc::tmem_wait_st();
+            }
+            l += sum;
+            pa_tc::fence_before_sync();
+            __syncthreads();
+            pa_tc::fence_after_sync();
+            if (tid == 0) {
+#pragma unroll
+                for (int kk = 0; kk < kStep / 16; ++kk) {
+                    const uint64_t b = pa_tc::sw128_desc(kst + 16384 + kk * 32);
+                    pa_tc::mma_bf16_ta(tO, tPh + kk * 8, b, kIdescPV, j > 0 || kk > 0);
+                    pa_tc::mma_bf16_ta(tO, tPl + kk * 8, b, kIdescPV, true);
+                }
+                pa_tc::commit(bar_pv);
+            }
+        }
+        if (!ok) break;
+        {
+            const bool w = pa_tc::mbar_wait(bar_pv, ph_pv, kWaitLimit);
+            if (!__syncthreads_and(w)) { ok = false; break; }
+        }
+        ph_pv ^= 1u;
+        pa_tc::fence_after_sync();
+        // this row's partial: O (relative to m_ref), m_ref, l
+        const size_t slot = row_ok ? (static_cast<size_t>(p.g_spart_base[grp]) +
+                                      static_cast<size_t>(row_m) * nC + chunk) * Hkv + h : 0;
+        float* acc = p.spart_acc + (slot * G + row_n) * kD;
+#pragma unroll
+        for (int cc = 0; cc < kD / 32; ++cc) {
+            float o[32];
+            pa_tc::tmem_ld32(tO + lane_sel + cc * 32, o);
+            pa_tc::tmem_wait_ld();
+            if (row_ok) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4*>(acc + cc * 32 + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+            }
+        }
+        if (row_ok) {
+            p.spart_ml[(slot * G + row_n) * 2] = m_ref;
+            p.spart_ml[(slot * G + row_n) * 2 + 1] = l;
+        }
+        (void)row_s;
+        pa_tc::fence_before_sync();
+        __syncthreads();                                   // TMEM and stages are reused by the next item
+        pa_tc::fence_after_sync();
+    }
+    if (!ok && tid == 0) pa_dev::record_error(p.err, PA_ERR_CUDA);
+    pa_tc::cp_wait<0>();
+    pa_dev::allow_next_grid();
+    pa_tc::fence_before_sync();
+    __syncthreads();
+    pa_tc::fence_after_sync();
+    if (warp == 0) pa_tc::tmem_free<kTmemCols>(tmem);
+}
+
+}  // namespace
+
+namespace pa_detail {
+
+bool shared_tc_eligible(const pa_pool* pool, int G) {
+    return pool->dtype == PA_BF16 && pool->head_dim == kD && G >= 1 && G <= 8 &&
+           (pool->block_size == 16 || pool->block_size == 32 || pool->block_size == 64);
+}
+
+int shared_tc_rows() { return kRows; }
+
+int launch_shared_tc(const pa_pool* pool, const DecodeParams& p, cudaStream_t st) {
+    if (p.n_shared_items <= 0) return PA_OK;
+    if (cudaFuncSetAttribute(shared_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    const int grid = p.n_shared_items < 2 * pool->num_sms ? p.n_shared_items : 2 * pool->num_sms;
+    const cudaError_t e = launch_pdl(shared_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, p);
+    count_launch();
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa_detail
