@@ -243,7 +243,9 @@ def run_ours(args):
     pool, bm, _ = runtime.replay_setup(wl, values, f"cuda:{local}")
     step = runtime.prepare_step(wl, values, pool, bm)
     lens = step.context_lens.cpu().numpy()
-    kv_bytes = _kv_bytes(wl, lens, step.groups)
+    # unique bytes: a shared span counts once per group whichever decode path runs
+    all_groups = bm.prefix_groups(wl.batch)
+    kv_bytes = _kv_bytes(wl, lens, all_groups)
     logical_kv_bytes = _kv_bytes(wl, lens)
     algo_bytes = _algo_bytes(wl, lens) - logical_kv_bytes + kv_bytes
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=f"cuda:{local}")
@@ -327,7 +329,8 @@ def run_ours(args):
         "config": {"workload": _workload_desc(wl),
                    "l2": "flushed between steps (256 MiB write, outside the timed events)",
                    "kv_bytes_per_step": kv_bytes, "logical_kv_bytes_per_step": logical_kv_bytes,
-                   "shared_groups": int(len(step.groups[2])) if step.groups is not None else 0,
+                   "shared_groups": int(len(all_groups[2])),
+                   "shared_path": bool(step.sharing()),
                    "copy_pairs_per_step": step.num_pairs,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_frac_of_" + peak_kind: round(value / world / peak, 4),
