@@ -1079,7 +1079,7 @@ int occupancy(K kernel, size_t smem) {
 
 namespace pa_detail {
 
-int plan_decode(const pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) {
+int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) {
     const int Hkv = pool->kv_heads, D = pool->head_dim, B = pool->block_size;
     const int G = Hq / Hkv;
     const bool fast = pool->dtype == PA_BF16 && (D == 64 || D == 128 || D == 256) &&

@@ -7,6 +7,7 @@
 #include <utility>
 #include <vector>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "pa.h"
@@ -21,6 +22,11 @@ struct pa_pool {
     void* ws = nullptr;         // decode workspace: header, then partials
     size_t ws_bytes = 0;
     int num_sms = 0;
+    // TMA descriptors of K (boxes 64 d x 16 tokens, 128-byte swizzle) and of V^T
+    // (boxes 16 tokens x 128 d, 32-byte swizzle), made on first use
+    alignas(64) CUtensorMap kmap;
+    alignas(64) CUtensorMap vmap;
+    bool tmaps_ready = false;
     // shared-prefix descriptor last uploaded by pa_decode_shared (host copy + device copy)
     std::vector<int> desc_host;
     int* desc_dev = nullptr;
@@ -106,7 +112,7 @@ struct DecodePlan {
     bool shared = false;        // shared-prefix items present (fast path only)
     bool fuse = false;          // the decode kernel also appends each sequence's new token
     bool tc = false;            // shared items run in the tcgen05 kernel before the split pass
-    const pa_pool* pool = nullptr;
+    pa_pool* pool = nullptr;
     bool fast;                  // bf16 tensor-core path
     bool bf16;                  // pool element type is bf16
     int grid, threads;
@@ -114,12 +120,12 @@ struct DecodePlan {
     int items_target, pt_min, pt_fixed;
     size_t max_items;
 };
-int plan_decode(const pa_pool* p, int S, int Hq, int max_blocks, DecodePlan* plan);
+int plan_decode(pa_pool* p, int S, int Hq, int max_blocks, DecodePlan* plan);
 int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t st);
 
 // tcgen05 shared-prefix items (pa_shared_tc.cu).
 bool shared_tc_eligible(const pa_pool* pool, int G);
 int shared_tc_rows();
-int launch_shared_tc(const pa_pool* pool, const DecodeParams& p, cudaStream_t st);
+int launch_shared_tc(pa_pool* pool, const DecodeParams& p, cudaStream_t st);
 
 }  // namespace pa_detail

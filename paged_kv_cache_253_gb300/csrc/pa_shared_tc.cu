@@ -25,6 +25,9 @@
 // kernel reads for the mma.sync variant.
 #include <cstdint>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_tc.cuh"
@@ -55,23 +58,33 @@ __device__ __forceinline__ int seq_len(const DecodeParams& p, int s) {
     return L < 0 ? 0 : min(L, p.max_blocks * p.B);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) shared_tc_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 2)
+shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
+                 const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ unsigned char tc_raw[];
     const uint32_t raw_s = pa_tc::smem_u32(tc_raw);
     unsigned char* base = tc_raw + ((1024u - (raw_s & 1023u)) & 1023u);
     const uint32_t sbase = pa_tc::smem_u32(base);
     uint64_t* bar_s = reinterpret_cast<uint64_t*>(base + kMiscOff);
     uint64_t* bar_pv = bar_s + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kMiscOff + 16);
-    int* s_tbl = reinterpret_cast<int*>(base + kMiscOff + 32);   // 32 block ids of a chunk
+    uint64_t* bar_full = bar_s + 2;                                // [2]: a stage's TMA copies landed
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kMiscOff + 32);
+    int* s_tbl = reinterpret_cast<int*>(base + kMiscOff + 64);   // 32 block ids of a chunk
 
     const int tid = threadIdx.x, warp = tid >> 5;
     pa_dev::wait_prior_grid();
     if (tid == 0) {
         pa_tc::mbar_init(bar_s, 1);
         pa_tc::mbar_init(bar_pv, 1);
+        pa_tc::mbar_init(bar_full, 1);
+        pa_tc::mbar_init(bar_full + 1, 1);
         pa_tc::mbar_init_fence();
     }
+    // Stages start zeroed: a step past the span's end leaves some block slots
+    // unloaded, and their (zero-probability) values must be finite.
+    for (uint32_t o = tid * 16; o < 2 * kStageBytes; o += kThreads * 16)
+        *reinterpret_cast<uint4*>(base + kStageOff + o) = make_uint4(0u, 0u, 0u, 0u);
+    pa_tc::fence_smem_to_async();
     if (warp == 0) pa_tc::tmem_alloc<kTmemCols>(tslot);
     pa_tc::fence_before_sync();
     __syncthreads();
@@ -79,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 2) shared_tc_kernel(const DecodePara
     const uint32_t tmem = *tslot;
     const uint32_t tS = tmem, tO = tmem + 64, tPh = tmem + 192, tPl = tmem + 224;
     const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;   // this warp's TMEM lanes
-    uint32_t ph_s = 0, ph_pv = 0;
+    uint32_t ph_s = 0, ph_pv = 0, ph_full0 = 0, ph_full1 = 0;
     bool ok = true;
 
     const int G = p.G, B = p.B, Hkv = p.Hkv;
@@ -140,40 +153,32 @@ __global__ void __launch_bounds__(kThreads, 2) shared_tc_kernel(const DecodePara
         pa_tc::cp_commit();
         __syncthreads();                                   // s_tbl visible
 
-        // Each thread copies a fixed 16-byte column of every tile: K chunk c16 of
-        // tokens tr + 8i, V^T chunk cv (8 tokens) of rows dr + 16i.  Block sizes are
-        // powers of two, so block and offset come from shifts and masks.
-        const int lgB = __ffs(B) - 1;
-        const int c16 = tid & 15, tr = tid >> 4;
-        const int cv = tid & 7, dr = tid >> 3;
+        // One thread stages a step: per 16-token block, its K rows as two
+        // 64-d boxes (128-byte swizzle, placed at row 16b of the two K regions)
+        // and its V^T tile as one 16-token x 128-d box (32-byte swizzle, own
+        // 4 KB region); the stage's mbarrier completes when all bytes landed.
         auto load_step = [&](int j) {
-            const uint32_t st = sbase + kStageOff + (j & 1) * kStageBytes;
+            if (tid != 0) return;
+            const int st = j & 1;
+            const uint32_t kst = sbase + kStageOff + st * kStageBytes;
+            uint32_t bytes = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {                                  // K: 64 tokens x 16 chunks
-                const int rel = j * kStep + tr + 8 * i;                    // token offset inside the chunk
-                const bool v = t0 + rel < t1;
-                const int phys = v ? s_tbl[rel >> lgB] : -1;
-                const uint16_t* src = kpool + (phys >= 0 ? (static_cast<size_t>(phys) * Hkv + h) * tile_elems +
-                                                               (static_cast<size_t>(rel & (B - 1)) << 7) + c16 * 8
-                                                         : 0);
-                pa_tc::cp16(st + (c16 >> 3) * 8192 + pa_tc::sw128_off(tr + 8 * i, c16 & 7), src,
-                            phys >= 0 ? 16u : 0u);
+            for (int b = 0; b < kStep / 16; ++b) {
+                const int rel = j * kStep + 16 * b;
+                if (t0 + rel < t1 && s_tbl[rel >> 4] >= 0) bytes += 2 * 2048 + 4096;
             }
-            {                                                              // V^T: 128 d x 8 chunks
-                const int rel = j * kStep + 8 * cv;
-                const bool v = t0 + rel < t1;
-                const int phys = v ? s_tbl[rel >> lgB] : -1;
-                const uint16_t* vb = vpool + (phys >= 0 ? (static_cast<size_t>(phys) * Hkv + h) * tile_elems +
-                                                              (rel & (B - 1))
-                                                        : 0);
+            pa_tc::mbar_expect_tx(bar_full + st, bytes);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int d = dr + 16 * i;
-                    pa_tc::cp16(st + 16384 + pa_tc::sw128_off(d, cv), vb + (phys >= 0 ? d * B : 0),
-                                phys >= 0 ? 16u : 0u);
-                }
+            for (int b = 0; b < kStep / 16; ++b) {
+                const int rel = j * kStep + 16 * b;
+                if (t0 + rel >= t1) continue;
+                const int phys = s_tbl[rel >> 4];
+                if (phys < 0) continue;
+                const int yk = (phys * Hkv + h) * 16, yv = (phys * Hkv + h) * kD;
+                pa_tc::tma_load_2d(kst + b * 2048, &kmap, 0, yk, bar_full + st);
+                pa_tc::tma_load_2d(kst + 8192 + b * 2048, &kmap, 64, yk, bar_full + st);
+                pa_tc::tma_load_2d(kst + 16384 + b * 4096, &vmap, 0, yv, bar_full + st);
             }
-            pa_tc::cp_commit();
         };
 
         load_step(0);
@@ -186,8 +191,12 @@ __global__ void __launch_bounds__(kThreads, 2) shared_tc_kernel(const DecodePara
                 ph_pv ^= 1u;
             }
             if (j + 1 < nsteps) load_step(j + 1);
-            else pa_tc::cp_commit();
-            pa_tc::cp_wait<1>();
+            if (j == 0) pa_tc::cp_wait<0>();               // this item's Q rows (cp.async)
+            {
+                const bool w = pa_tc::mbar_wait(bar_full + st, st ? ph_full1 : ph_full0, kWaitLimit);
+                if (st) ph_full1 ^= 1u; else ph_full0 ^= 1u;
+                if (!__syncthreads_and(w)) { ok = false; break; }
+            }
             pa_tc::fence_smem_to_async();
             pa_tc::fence_before_sync();
             __syncthreads();
@@ -271,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 2) shared_tc_kernel(const DecodePara
             if (tid == 0) {
 #pragma unroll
                 for (int kk = 0; kk < kStep / 16; ++kk) {
-                    const uint64_t b = pa_tc::sw128_desc(kst + 16384 + kk * 32);
+                    const uint64_t b = pa_tc::sw32_desc(kst + 16384 + kk * 4096);   // block kk's V^T
                     pa_tc::mma_bf16_ta(tO, tPh + kk * 8, b, kIdescPV, j > 0 || kk > 0);
                     pa_tc::mma_bf16_ta(tO, tPl + kk * 8, b, kIdescPV, true);
                 }
@@ -324,18 +333,52 @@ namespace pa_detail {
 
 bool shared_tc_eligible(const pa_pool* pool, int G) {
     return pool->dtype == PA_BF16 && pool->head_dim == kD && G >= 1 && G <= 8 &&
-           (pool->block_size == 16 || pool->block_size == 32 || pool->block_size == 64);
+           pool->block_size == 16;
+}
+
+// TMA descriptors over the pool: K as [num_blocks*Hkv*16 rows][128 d] with
+// 64 x 16 boxes, V^T as [num_blocks*Hkv*128 rows][16 tokens] with 16 x 128 boxes.
+static int make_tensor_maps(pa_pool* pool) {
+    if (pool->tmaps_ready) return PA_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return PA_ERR_CUDA;
+    auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    const cuuint64_t rows_k = static_cast<cuuint64_t>(pool->num_blocks) * pool->kv_heads * 16;
+    const cuuint64_t rows_v = static_cast<cuuint64_t>(pool->num_blocks) * pool->kv_heads * kD;
+    const cuuint64_t kdim[2] = {static_cast<cuuint64_t>(kD), rows_k};
+    const cuuint64_t kstr[1] = {kD * 2};
+    const cuuint32_t kbox[2] = {64, 16};
+    const cuuint64_t vdim[2] = {16, rows_v};
+    const cuuint64_t vstr[1] = {16 * 2};
+    const cuuint32_t vbox[2] = {16, 128};
+    const cuuint32_t one[2] = {1, 1};
+    if (encode(&pool->kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool->k, kdim, kstr, kbox, one,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PA_ERR_CUDA;
+    if (encode(&pool->vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool->v, vdim, vstr, vbox, one,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PA_ERR_CUDA;
+    pool->tmaps_ready = true;
+    return PA_OK;
 }
 
 int shared_tc_rows() { return kRows; }
 
-int launch_shared_tc(const pa_pool* pool, const DecodeParams& p, cudaStream_t st) {
+int launch_shared_tc(pa_pool* pool, const DecodeParams& p, cudaStream_t st) {
     if (p.n_shared_items <= 0) return PA_OK;
+    const int rc = make_tensor_maps(pool);
+    if (rc != PA_OK) return rc;
     if (cudaFuncSetAttribute(shared_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess)
         return PA_ERR_CUDA;
     const int grid = p.n_shared_items < 2 * pool->num_sms ? p.n_shared_items : 2 * pool->num_sms;
-    const cudaError_t e = launch_pdl(shared_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, p);
+    const cudaError_t e = launch_pdl(shared_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, p,
+                                     pool->kmap, pool->vmap);
     count_launch();
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
