@@ -821,7 +821,7 @@ decode_fast_kernel(const DecodeParams p) {
     int* s_flag = reinterpret_cast<int*>(s_red + kWarps);
     int* s_start = s_flag + 4;                                // [S + 1]
 
-    pa_dev::wait_prior_grid();
+    if (!p.defer_wait) pa_dev::wait_prior_grid();
     const Sched sc = build_schedule(p, s_start, s_red);
     publish_schedule(p, sc, s_start);
     const int n_sh = SHARED ? p.n_shared_items : 0;
@@ -867,6 +867,7 @@ decode_fast_kernel(const DecodeParams p) {
         finish_item(p, pitem, s, h, nP, res_m, res_l, sm_o, OS);
         __syncthreads();
     }
+    if (p.defer_wait) pa_dev::wait_prior_grid();        // the shared-prefix kernel is done too
     pa_dev::allow_next_grid();
     retire_cta(p);
 }
@@ -1142,6 +1143,7 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
         if (rc != PA_OK) return rc;
         DecodeParams q = p;
         q.n_shared_items = 0;
+        q.defer_wait = 1;
         if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, false>, grid, block, plan.smem, st, q);
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, false>, grid, block, plan.smem, st, q);
         else e = launch_pdl(decode_fast_kernel<256, false, false>, grid, block, plan.smem, st, q);

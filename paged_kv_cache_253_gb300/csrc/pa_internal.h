@@ -72,6 +72,10 @@ struct DecodeParams {
     const void* new_k;          // [S][Hkv][D]
     const void* new_v;          // [S][Hkv][D]
     const int64_t* new_slots;   // [S] slot of position L-1 of each sequence, or < 0
+    // 1: the preceding kernel is the tcgen05 shared-prefix kernel, which already
+    // waited for the work before it; the split kernel then runs alongside it and
+    // waits for it only before exiting (so the merge after it sees both).
+    int defer_wait;
 };
 
 // Decode workspace header: ticket[2], 2 spare ints, then the published

@@ -73,6 +73,7 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
 
     const int tid = threadIdx.x, warp = tid >> 5;
     pa_dev::wait_prior_grid();
+    pa_dev::allow_next_grid();       // the private-span split kernel may run alongside
     if (tid == 0) {
         pa_tc::mbar_init(bar_s, 1);
         pa_tc::mbar_init(bar_pv, 1);
@@ -320,7 +321,6 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     }
     if (!ok && tid == 0) pa_dev::record_error(p.err, PA_ERR_CUDA);
     pa_tc::cp_wait<0>();
-    pa_dev::allow_next_grid();
     pa_tc::fence_before_sync();
     __syncthreads();
     pa_tc::fence_after_sync();
