@@ -43,8 +43,7 @@ size_t elem_size(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
 // Workspace: [header: ticket + schedule, 256-aligned][part_acc][part_ml]
 size_t workspace_bytes(const pa_detail::DecodePlan& plan, int S, int Hkv, int G, int D,
                        size_t* counters_bytes) {
-    (void)Hkv;
-    const size_t cb = decode_header_bytes(S);
+    const size_t cb = decode_header_bytes(S, Hkv);
     const size_t acc = round256(plan.max_items * G * D * sizeof(float));
     const size_t ml = round256(plan.max_items * G * 2 * sizeof(float));
     if (counters_bytes) *counters_bytes = cb;
@@ -92,7 +91,9 @@ int pa_pool_create(int num_blocks, int block_size, int kv_heads, int head_dim, p
     if (!p) return PA_ERR_OUT_OF_MEMORY;
     if (cudaGetDevice(&p->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) !=
-            cudaSuccess) {
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&p->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                               p->device) != cudaSuccess) {
         delete p;
         return PA_ERR_CUDA;
     }
@@ -326,6 +327,7 @@ static int decode_impl(pa_pool* pool, const void* q, int num_seqs, int num_q_hea
     p.out = out;
     p.ticket = static_cast<int*>(pool->ws);
     p.sched = p.ticket + 4;
+    p.unit_cnt = decode_unit_counters(p.ticket, num_seqs);
     p.part_acc = reinterpret_cast<float*>(static_cast<char*>(pool->ws) + cb);
     p.part_ml = reinterpret_cast<float*>(
         static_cast<char*>(pool->ws) + cb + round256(plan.max_items * G * pool->head_dim * sizeof(float)));

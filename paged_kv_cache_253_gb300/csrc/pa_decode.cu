@@ -1085,6 +1085,8 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
     const int G = Hq / Hkv;
     const bool fast = pool->dtype == PA_BF16 && (D == 64 || D == 128 || D == 256) &&
                       B % 16 == 0 && G <= 8;
+    if (!plan->shared && fast && plan_stream(pool, S, Hq, max_blocks, plan)) return PA_OK;
+    plan->stream = false;
     plan->fast = fast;
     plan->pool = pool;
     plan->bf16 = pool->dtype == PA_BF16;
@@ -1135,6 +1137,7 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
     p.items_target = plan.items_target;
     p.pt_min = plan.pt_min;
     p.pt_fixed = plan.pt_fixed;
+    if (plan.stream) return launch_stream(plan, p, st);
     const dim3 grid(plan.grid), block(plan.threads);
     cudaError_t e;
     if (plan.fast && plan.shared && plan.tc) {

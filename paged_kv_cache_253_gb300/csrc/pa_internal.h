@@ -22,10 +22,13 @@ struct pa_pool {
     void* ws = nullptr;         // decode workspace: header, then partials
     size_t ws_bytes = 0;
     int num_sms = 0;
+    int smem_optin = 0;         // largest dynamic shared memory a CTA may opt in to
     // TMA descriptors of K (boxes 64 d x 16 tokens, 128-byte swizzle) and of V^T
     // (boxes 16 tokens x 128 d, 32-byte swizzle), made on first use
-    alignas(64) CUtensorMap kmap;
-    alignas(64) CUtensorMap vmap;
+    CUtensorMap kmap;
+    CUtensorMap vmap;
+    // V^T again as 128-byte lines (4 d rows of 16 tokens; boxes of D/4 lines, 128-byte swizzle)
+    CUtensorMap vmap_lines;
     bool tmaps_ready = false;
     // shared-prefix descriptor last uploaded by pa_decode_shared (host copy + device copy)
     std::vector<int> desc_host;
@@ -45,6 +48,7 @@ struct DecodeParams {
     float* part_ml;             // [max_items][G][2]  (running max, sum) in log2 units
     int* ticket;                // [2] work ticket and retired-CTA count, zero between launches
     int* sched;                 // [S + 3] PT, item count, first item of each sequence
+    int* unit_cnt;              // [S * Hkv] pieces of each unit finished (stream-K), zero between launches
     int* err;
     float scale_log2;           // scale * log2(e)
     int S, Hq, Hkv, G, D, B, num_blocks, max_blocks;
@@ -76,13 +80,18 @@ struct DecodeParams {
     // waited for the work before it; the split kernel then runs alongside it and
     // waits for it only before exiting (so the merge after it sees both).
     int defer_wait;
+    // Stream-K split pass (pa_decode_stream.cu): ring stages per warp, bytes per stage.
+    int sk_stages;
+    int sk_stage_bytes;
 };
 
-// Decode workspace header: ticket[2], 2 spare ints, then the published
-// schedule (PT, item count, S + 1 item offsets); zeroed before first use.
-inline size_t decode_header_bytes(int S) {
-    return ((static_cast<size_t>(S) + 8) * sizeof(int) + 255) / 256 * 256;
+// Decode workspace header: ticket[2], 2 spare ints, the published schedule
+// (S + 3 ints used of S + 4), then one arrival counter per (sequence, KV head)
+// unit; zeroed before first use (the kernels reset what they count).
+inline size_t decode_header_bytes(int S, int Hkv) {
+    return ((static_cast<size_t>(S) + 8 + static_cast<size_t>(S) * Hkv) * sizeof(int) + 255) / 256 * 256;
 }
+inline int* decode_unit_counters(int* header, int S) { return header + S + 8; }
 
 namespace pa_detail {
 
@@ -116,6 +125,8 @@ struct DecodePlan {
     bool shared = false;        // shared-prefix items present (fast path only)
     bool fuse = false;          // the decode kernel also appends each sequence's new token
     bool tc = false;            // shared items run in the tcgen05 kernel before the split pass
+    bool stream = false;        // stream-K split pass with TMA-fed per-warp rings
+    int sk_stages = 0, sk_stage_bytes = 0;
     pa_pool* pool = nullptr;
     bool fast;                  // bf16 tensor-core path
     bool bf16;                  // pool element type is bf16
@@ -126,6 +137,14 @@ struct DecodePlan {
 };
 int plan_decode(pa_pool* p, int S, int Hq, int max_blocks, DecodePlan* plan);
 int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t st);
+
+// TMA descriptors of the pool's K and V^T (16-token blocks), made once per pool.
+int ensure_tensor_maps(pa_pool* pool);
+
+// Stream-K split pass (pa_decode_stream.cu): fills `plan` and returns true when
+// the pool and batch suit it (bf16, 16-token blocks, head_dim 64/128/256, G <= 8).
+bool plan_stream(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan);
+int launch_stream(const DecodePlan& plan, const DecodeParams& p, cudaStream_t st);
 
 // tcgen05 shared-prefix items (pa_shared_tc.cu).
 bool shared_tc_eligible(const pa_pool* pool, int G);

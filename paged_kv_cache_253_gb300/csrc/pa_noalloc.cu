@@ -85,7 +85,7 @@ extern "C" int pa_decode_noalloc(pa_pool* pool, const void* q, int num_seqs, int
     pa_detail::DecodePlan plan;
     int rc = pa_detail::plan_decode(pool, num_seqs, num_q_heads, max_blocks_per_seq, &plan);
     if (rc != PA_OK) return rc;
-    const size_t counters = decode_header_bytes(num_seqs);
+    const size_t counters = decode_header_bytes(num_seqs, Hkv);
     const size_t acc = round_up256(plan.max_items * G * D * sizeof(float));
     const size_t ml = round_up256(plan.max_items * G * 2 * sizeof(float));
     if (counters + acc + ml > kScratchBytes) return PA_ERR_UNSUPPORTED;   // batch too large
@@ -94,7 +94,8 @@ extern "C" int pa_decode_noalloc(pa_pool* pool, const void* q, int num_seqs, int
     rc = scratch_address(pool->device, &base);
     if (rc != PA_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // the work ticket must start at zero; the array keeps the previous call's bytes
+    // the work ticket and unit counters must start at zero; the array keeps the
+    // previous call's bytes
     if (cudaMemsetAsync(base, 0, counters, st) != cudaSuccess) return PA_ERR_CUDA;
 
     DecodeParams p{};
@@ -106,6 +107,7 @@ extern "C" int pa_decode_noalloc(pa_pool* pool, const void* q, int num_seqs, int
     p.out = out;
     p.ticket = static_cast<int*>(base);
     p.sched = p.ticket + 4;
+    p.unit_cnt = decode_unit_counters(p.ticket, num_seqs);
     p.part_acc = reinterpret_cast<float*>(static_cast<char*>(base) + counters);
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(base) + counters + acc);
     p.err = pool->err;

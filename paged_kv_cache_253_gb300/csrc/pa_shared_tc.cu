@@ -332,14 +332,22 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
 namespace pa_detail {
 
 bool shared_tc_eligible(const pa_pool* pool, int G) {
+    // TMA coordinates are 32-bit: value rows num_blocks * Hkv * D must stay below 2^31
     return pool->dtype == PA_BF16 && pool->head_dim == kD && G >= 1 && G <= 8 &&
-           pool->block_size == 16;
+           pool->block_size == 16 &&
+           static_cast<long long>(pool->num_blocks) * pool->kv_heads * kD < (1LL << 31);
 }
 
-// TMA descriptors over the pool: K as [num_blocks*Hkv*16 rows][128 d] with
-// 64 x 16 boxes, V^T as [num_blocks*Hkv*128 rows][16 tokens] with 16 x 128 boxes.
-static int make_tensor_maps(pa_pool* pool) {
+// TMA descriptors over the pool (16-token blocks): K as
+// [num_blocks*Hkv*16 rows][D] with 64 x 16 boxes (128-byte swizzle); V^T as
+// [num_blocks*Hkv*D rows][16 tokens] with 16 x D boxes (32-byte swizzle), and
+// the same V^T as [num_blocks*Hkv*D/4 lines][64] with 64 x D/4 boxes
+// (128-byte swizzle: a tile moves as D/4 lines of 128 bytes).
+int ensure_tensor_maps(pa_pool* pool) {
     if (pool->tmaps_ready) return PA_OK;
+    const int D = pool->head_dim;
+    if (pool->dtype != PA_BF16 || pool->block_size != 16 || D % 64 != 0 || D > 256)
+        return PA_ERR_UNSUPPORTED;
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
@@ -347,13 +355,13 @@ static int make_tensor_maps(pa_pool* pool) {
         return PA_ERR_CUDA;
     auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     const cuuint64_t rows_k = static_cast<cuuint64_t>(pool->num_blocks) * pool->kv_heads * 16;
-    const cuuint64_t rows_v = static_cast<cuuint64_t>(pool->num_blocks) * pool->kv_heads * kD;
-    const cuuint64_t kdim[2] = {static_cast<cuuint64_t>(kD), rows_k};
-    const cuuint64_t kstr[1] = {kD * 2};
+    const cuuint64_t rows_v = static_cast<cuuint64_t>(pool->num_blocks) * pool->kv_heads * D;
+    const cuuint64_t kdim[2] = {static_cast<cuuint64_t>(D), rows_k};
+    const cuuint64_t kstr[1] = {static_cast<cuuint64_t>(D) * 2};
     const cuuint32_t kbox[2] = {64, 16};
     const cuuint64_t vdim[2] = {16, rows_v};
     const cuuint64_t vstr[1] = {16 * 2};
-    const cuuint32_t vbox[2] = {16, 128};
+    const cuuint32_t vbox[2] = {16, static_cast<cuuint32_t>(D)};
     const cuuint32_t one[2] = {1, 1};
     if (encode(&pool->kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool->k, kdim, kstr, kbox, one,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -361,6 +369,13 @@ static int make_tensor_maps(pa_pool* pool) {
         return PA_ERR_CUDA;
     if (encode(&pool->vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool->v, vdim, vstr, vbox, one,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PA_ERR_CUDA;
+    const cuuint64_t ldim[2] = {64, static_cast<cuuint64_t>(pool->num_blocks) * pool->kv_heads * D / 4};
+    const cuuint64_t lstr[1] = {128};
+    const cuuint32_t lbox[2] = {64, static_cast<cuuint32_t>(D / 4)};
+    if (encode(&pool->vmap_lines, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool->v, ldim, lstr, lbox, one,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return PA_ERR_CUDA;
     pool->tmaps_ready = true;
@@ -371,7 +386,7 @@ int shared_tc_rows() { return kRows; }
 
 int launch_shared_tc(pa_pool* pool, const DecodeParams& p, cudaStream_t st) {
     if (p.n_shared_items <= 0) return PA_OK;
-    const int rc = make_tensor_maps(pool);
+    const int rc = ensure_tensor_maps(pool);
     if (rc != PA_OK) return rc;
     if (cudaFuncSetAttribute(shared_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess)
