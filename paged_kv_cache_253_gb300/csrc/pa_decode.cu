@@ -35,6 +35,7 @@
 #include <algorithm>
 #include <cfloat>
 #include <cmath>
+#include <cstdlib>
 #include <cstdint>
 #include <type_traits>
 
@@ -57,6 +58,9 @@
 #ifndef PA_MIN_CTAS
 #define PA_MIN_CTAS 3           // resident CTAs per SM the register budget aims at
 #endif
+#ifndef PA_PT_MAX_TOKENS
+#define PA_PT_MAX_TOKENS 2048    // partition cap in tokens for batches of many sequences
+#endif
 #ifndef PA_STAGES
 #define PA_STAGES 0             // cp.async ring depth per warp (0/1: direct register loads)
 #endif
@@ -71,6 +75,7 @@
 namespace {
 
 constexpr int kWarps = PA_WARPS;
+constexpr int kPtMax = PA_PT_MAX_TOKENS;
 constexpr int kSharedStages = PA_SHARED_STAGES;
 constexpr int kSharedUnitsPerSync = PA_SHARED_UNITS_PER_SYNC;
 static_assert(kSharedStages > kSharedUnitsPerSync, "shared pipeline needs copies in flight");
@@ -133,6 +138,16 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
     } else {
         long long need = (total * p.Hkv + p.items_target - 1) / p.items_target;
         need = (need + p.B - 1) / p.B * p.B;
+        // cap the partition so the launch's last items are short (long
+        // sequences split into more items; the merge combines them), but never
+        // below the length that keeps the item count within the workspace:
+        // items <= Hkv * (total / PT + S) <= max_items
+        if (p.pt_max > 0) {
+            const long long room = static_cast<long long>(p.max_items) - static_cast<long long>(p.Hkv) * p.S;
+            long long lo = room > 0 ? (total * p.Hkv + room - 1) / room : need;
+            lo = (lo + p.B - 1) / p.B * p.B;
+            need = min(need, max(static_cast<long long>(p.pt_max), lo));
+        }
         PT = static_cast<int>(max(need, static_cast<long long>(p.pt_min)));
     }
     int cnt = 0;
@@ -1096,6 +1111,14 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
         plan->smem = fast_smem(D, S, plan->shared && !plan->tc);
         plan->pt_fixed = 0;
         plan->pt_min = std::max(B, (64 + B - 1) / B * B);
+        // Batches of more sequences than SMs are mostly one item per sequence,
+        // of uneven sizes; partitions of at most kPtMax tokens then shorten the
+        // launch's tail (measured on GB300: mixed lengths 473 -> 455 us; a few
+        // long sequences, already many equal items, are better uncapped).
+        // PA_PT_MAX overrides the choice (0: no cap).
+        int pt_max = S > pool->num_sms ? kPtMax : 0;
+        if (const char* e = std::getenv("PA_PT_MAX")) pt_max = std::atoi(e);
+        plan->pt_max = pt_max > 0 ? std::max(plan->pt_min, pt_max / B * B) : 0;
         if (plan->shared && !plan->tc) {
             if (D == 64) occ = occupancy(decode_fast_kernel<64, true, false>, plan->smem);
             else if (D == 128) occ = occupancy(decode_fast_kernel<128, true, false>, plan->smem);
@@ -1121,11 +1144,16 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
     plan->grid = pool->num_sms * occ;
     if (fast) {
         plan->items_target = plan->grid * PA_ITEMS_PER_CTA;
-        plan->max_items = static_cast<size_t>(plan->items_target) + static_cast<size_t>(Hkv) * S;
+        // items <= Hkv * (total / PT + S); PT >= total * Hkv / items_target keeps
+        // that below min_items.  The extra items_target of room lets the
+        // partition cap take effect; the kernel never exceeds max_items.
+        plan->min_items = static_cast<size_t>(plan->items_target) + static_cast<size_t>(Hkv) * S;
+        plan->max_items = plan->min_items + (plan->pt_max > 0 ? static_cast<size_t>(plan->items_target) : 0);
     } else {
         plan->items_target = 0;
         const size_t per_seq = (static_cast<size_t>(max_blocks) * B + plan->pt_fixed - 1) / plan->pt_fixed;
         plan->max_items = static_cast<size_t>(Hkv) * S * std::max<size_t>(1, per_seq);
+        plan->min_items = plan->max_items;
     }
     if (static_cast<size_t>(plan->grid) > plan->max_items)
         plan->grid = static_cast<int>(plan->max_items);
@@ -1136,6 +1164,8 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
     DecodeParams p = prm;
     p.items_target = plan.items_target;
     p.pt_min = plan.pt_min;
+    p.pt_max = plan.pt_max;
+    p.max_items = static_cast<int>(std::min<size_t>(plan.max_items, 1u << 30));
     p.pt_fixed = plan.pt_fixed;
     if (plan.stream) return launch_stream(plan, p, st);
     const dim3 grid(plan.grid), block(plan.threads);

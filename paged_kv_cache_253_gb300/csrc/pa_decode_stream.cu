@@ -75,6 +75,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// Counter access with explicit ordering: a piece's partial is published by a
+// release increment; a warp that sees the count through an acquire load (or
+// that fences after its own increment) then reads the other partials.
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ int atom_add_release(int* p, int x) {
+    int v;
+    asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;" : "=r"(v) : "l"(p), "r"(x) : "memory");
+    return v;
+}
+
 // Largest s with s_tiles[s] <= t (s_tiles non-decreasing, s_tiles[0] = 0 <= t < s_tiles[S]).
 __device__ __forceinline__ int seq_of_tile(const int* s_tiles, int S, int t) {
     int lo = 0, hi = S - 1;
@@ -505,6 +519,16 @@ decode_stream_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap k
     const int g = lane >> 2, c = lane & 3;
     bool ok = true;
     int fail_at = 0;
+    // The warp's first piece, when another warp shares its unit: published
+    // mid-range by a release increment whose result is looked at only at the
+    // end of the range (so no wait on it sits in the stream).
+    int pend_u = -1, pend_prev = 0;
+    // The warp's last piece, when shared: a few tiles before its end the
+    // unit's counter is read (acquire); if every other piece is published by
+    // then, this warp merges at once, without an increment.
+    constexpr int kSoleLead = 4;
+    int sole_cnt = -1;
+    bool sole_read = false;
     for (int i = 0; i < n;) {
         // two consecutive tiles of one unit are computed together
         const bool pair = i + 1 < n && cc.j + 1 < cc.nb;
@@ -569,6 +593,16 @@ decode_stream_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap k
         }
         if (pair) advance(cc, s_tiles, S, Hkv);         // cc: the last tile of this step
         const int il = pair ? i + 1 : i;
+        if (!sole_read && n - 1 - il <= kSoleLead) {
+            // this step lies in the range's last kSoleLead tiles: if its unit
+            // reaches the range end (the range's final piece) and is shared with
+            // another warp, start reading the unit's counter
+            const int U0 = s_tiles[s] + h * cc.nb, U1 = U0 + cc.nb;
+            if (U1 >= t1 && (U0 < t0 || U1 > t1)) {
+                sole_read = true;
+                if (lane == 0) sole_cnt = ld_acquire(p.unit_cnt + s * Hkv + h);
+            }
+        }
         const bool last = cc.j == cc.nb - 1 || il == n - 1;
         if (last) {
             float l0 = a.l0, l1 = a.l1;
@@ -634,7 +668,6 @@ decode_stream_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap k
                     }
                 }
                 // The last warp to finish a piece of this unit merges the pieces.
-                __threadfence();
                 __syncwarp();
                 const long long T0 = s_tiles[s] + static_cast<long long>(h) * cc.nb, T1 = T0 + cc.nb;
                 const int w0 = static_cast<int>(((T0 + 1) * Wt - 1) / T);
@@ -643,13 +676,25 @@ decode_stream_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap k
                 for (int w = w0 + lane; w <= w1; w += 32) parts += warp_has_tiles(T, Wt, w);
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) parts += __shfl_xor_sync(0xffffffffu, parts, off);
-                int prev = 0;
-                if (lane == 0) prev = atomicAdd(p.unit_cnt + u, 1);
-                prev = __shfl_sync(0xffffffffu, prev, 0);
-                if (prev == parts - 1) {
-                    __threadfence();
+                const bool final_piece = il == n - 1;
+                const int seen = __shfl_sync(0xffffffffu, sole_cnt, 0);
+                if (final_piece && sole_read && seen == parts - 1) {
+                    // every other piece was published before the read: merge now
                     merge_unit<D>(p, u, s, h, w0, w1, T, Wt, lane);
                     if (lane == 0) p.unit_cnt[u] = 0;     // ready for the next launch
+                } else if (final_piece) {
+                    int prev = 0;
+                    if (lane == 0) prev = atom_add_release(p.unit_cnt + u, 1);
+                    prev = __shfl_sync(0xffffffffu, prev, 0);
+                    if (prev == parts - 1) {
+                        __threadfence();
+                        merge_unit<D>(p, u, s, h, w0, w1, T, Wt, lane);
+                        if (lane == 0) p.unit_cnt[u] = 0;
+                    }
+                } else {
+                    // the range's first piece: publish now, look at the count at the end
+                    if (lane == 0) pend_prev = atom_add_release(p.unit_cnt + u, 1);
+                    pend_u = u;
                 }
             }
         }
@@ -660,6 +705,24 @@ decode_stream_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap k
         if (i + NS < n) issue(i + NS);
         if (pair && i + 1 + NS < n) issue(i + 1 + NS);
         i = il + 1;
+    }
+    if (ok && pend_u >= 0) {
+        // the first piece's increment: if it completed its unit's count, merge it
+        const int su = pend_u / Hkv, hu = pend_u - su * Hkv;
+        const int nbu = (s_tiles[su + 1] - s_tiles[su]) / Hkv;
+        const long long T0 = s_tiles[su] + static_cast<long long>(hu) * nbu, T1 = T0 + nbu;
+        const int w0 = static_cast<int>(((T0 + 1) * Wt - 1) / T);
+        const int w1 = static_cast<int>((T1 * Wt - 1) / T);
+        int parts = 0;
+        for (int w = w0 + lane; w <= w1; w += 32) parts += warp_has_tiles(T, Wt, w);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) parts += __shfl_xor_sync(0xffffffffu, parts, off);
+        const int prev = __shfl_sync(0xffffffffu, pend_prev, 0);
+        if (prev == parts - 1) {
+            __threadfence();
+            merge_unit<D>(p, pend_u, su, hu, w0, w1, T, Wt, lane);
+            if (lane == 0) p.unit_cnt[pend_u] = 0;
+        }
     }
     if (!ok) {
         // a copy did not arrive in time: record it and wait (bounded) for the
@@ -714,8 +777,10 @@ cudaError_t launch_split(const DecodeParams& p, const pa_pool* pool, int grid, s
 }  // namespace
 
 bool plan_stream(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) {
+    // Opt-in (PA_DECODE_STREAM=1): on GB300 the ticketed split kernel measures as
+    // fast or faster on every workload but the smallest batches.
     const char* env = std::getenv("PA_DECODE_STREAM");
-    if (env && env[0] == '0') return false;
+    if (!env || env[0] != '1') return false;
     const int Hkv = pool->kv_heads, D = pool->head_dim, G = Hq / Hkv;
     if (pool->dtype != PA_BF16 || pool->block_size != 16 || G < 1 || G > 8 || S < 1 || S > 4096)
         return false;
@@ -741,6 +806,7 @@ bool plan_stream(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan)
     plan->pt_min = 0;
     plan->pt_fixed = 0;
     plan->max_items = static_cast<size_t>(S) * Hkv + static_cast<size_t>(plan->grid) * kW;
+    plan->min_items = plan->max_items;
     return true;
 }
 

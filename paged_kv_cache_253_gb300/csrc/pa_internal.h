@@ -55,6 +55,8 @@ struct DecodeParams {
     int out_bf16;
     int items_target;           // wanted number of work items (fast path)
     int pt_min;                 // smallest partition, tokens (multiple of B)
+    int pt_max;                 // largest partition, tokens (multiple of B; 0: no cap)
+    int max_items;              // partial slots the workspace holds (fast path)
     int pt_fixed;               // > 0: use exactly this partition size
     // Shared-prefix description (pa_decode_shared); all zero / null otherwise.
     int n_shared_items;         // shared work items, heads included (K * Hkv)
@@ -132,8 +134,9 @@ struct DecodePlan {
     bool bf16;                  // pool element type is bf16
     int grid, threads;
     size_t smem;
-    int items_target, pt_min, pt_fixed;
+    int items_target, pt_min, pt_max = 0, pt_fixed;
     size_t max_items;
+    size_t min_items;           // fewest partial slots the kernel can work with (fast path)
 };
 int plan_decode(pa_pool* p, int S, int Hq, int max_blocks, DecodePlan* plan);
 int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t st);

@@ -86,9 +86,15 @@ extern "C" int pa_decode_noalloc(pa_pool* pool, const void* q, int num_seqs, int
     int rc = pa_detail::plan_decode(pool, num_seqs, num_q_heads, max_blocks_per_seq, &plan);
     if (rc != PA_OK) return rc;
     const size_t counters = decode_header_bytes(num_seqs, Hkv);
+    // partial slots: as many as the plan asks for, or as fit in the array (the
+    // kernel lengthens its partitions to stay within what it is given)
+    const size_t per_item = static_cast<size_t>(G) * (D + 2) * sizeof(float);
+    const size_t fit = kScratchBytes > counters + 512 ? (kScratchBytes - counters - 512) / per_item : 0;
+    if (fit < plan.min_items) return PA_ERR_UNSUPPORTED;                // batch too large
+    if (plan.max_items > fit) plan.max_items = fit;
     const size_t acc = round_up256(plan.max_items * G * D * sizeof(float));
     const size_t ml = round_up256(plan.max_items * G * 2 * sizeof(float));
-    if (counters + acc + ml > kScratchBytes) return PA_ERR_UNSUPPORTED;   // batch too large
+    if (counters + acc + ml > kScratchBytes) return PA_ERR_UNSUPPORTED;
 
     void* base = nullptr;
     rc = scratch_address(pool->device, &base);
