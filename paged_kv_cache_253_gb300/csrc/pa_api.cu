@@ -409,7 +409,9 @@ int pa_decode_shared(pa_pool* pool, const void* q, int num_seqs, int num_q_heads
     const char* force_sync = std::getenv("PA_SHARED_MMA_SYNC");
     sh.tc = pa_detail::shared_tc_eligible(pool, G) && !(force_sync && force_sync[0] == '1');
     sh.members_per_tile = std::max(1, (sh.tc ? pa_detail::shared_tc_rows() : 64) / G);
-    sh.chunk_tokens = std::max(B, 512 / B * B);
+    // shared tokens per item: the tcgen05 kernel stages a 1024-token table slice,
+    // the mma.sync variant one block id per lane (32 blocks)
+    sh.chunk_tokens = sh.tc ? pa_detail::shared_tc_chunk_tokens() : std::max(B, 512 / B * B);
     const int Ng = sh.num_groups;
     std::vector<int> items, sgroup(num_seqs, -1), smember(num_seqs, 0), sstart(num_seqs, 0);
     std::vector<int> goff(Ng + 1, 0), gmem, gnc(Ng), gbase(Ng), gtok(Ng);

@@ -152,6 +152,7 @@ int launch_stream(const DecodePlan& plan, const DecodeParams& p, cudaStream_t st
 // tcgen05 shared-prefix items (pa_shared_tc.cu).
 bool shared_tc_eligible(const pa_pool* pool, int G);
 int shared_tc_rows();
+int shared_tc_chunk_tokens();     // shared tokens per item (a multiple of 16)
 int launch_shared_tc(pa_pool* pool, const DecodeParams& p, cudaStream_t st);
 
 }  // namespace pa_detail

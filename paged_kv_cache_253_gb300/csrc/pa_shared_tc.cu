@@ -8,7 +8,7 @@
 // one KV head against the span's keys, read once per 128 rows.
 //
 // One CTA (4 warps, 128 threads) takes an item = (group, KV head, tile of
-// 128 / G members, chunk of 512 shared tokens) and walks it in 64-token steps:
+// 128 / G members, chunk of 1024 shared tokens) and walks it in 64-token steps:
 //   S[128 x 64]   = Q[128 x 128] . K^T           tcgen05.mma, fp32 in TMEM cols [0,64)
 //   softmax       thread t owns query row t = TMEM lane t (tcgen05.ld), exp2 in
 //                 fp32 with a reference maximum that is raised only when a row's
@@ -46,7 +46,8 @@ constexpr uint32_t kQOff = 0;                            // 2 regions x [128 row
 constexpr uint32_t kStageOff = 32768;                    // stage s: K (2 x [64][128 B]) then V^T ([128][128 B])
 constexpr uint32_t kStageBytes = 32768;
 constexpr uint32_t kMiscOff = kStageOff + 2 * kStageBytes;   // mbarriers, TMEM slot, table slice
-constexpr uint32_t kSmemBytes = kMiscOff + 256 + 1024;   // + alignment slack
+constexpr int kChunkBlocks = 64;                         // shared blocks per item (1024 tokens)
+constexpr uint32_t kSmemBytes = kMiscOff + 64 + 4 * kChunkBlocks + 1024;   // + alignment slack
 
 constexpr uint32_t kIdescQK = pa_tc::idesc_bf16_f32(kRows, kStep);
 constexpr uint32_t kIdescPV = pa_tc::idesc_bf16_f32(kRows, kD);
@@ -69,7 +70,7 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     uint64_t* bar_pv = bar_s + 1;
     uint64_t* bar_full = bar_s + 2;                                // [2]: a stage's TMA copies landed
     uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kMiscOff + 32);
-    int* s_tbl = reinterpret_cast<int*>(base + kMiscOff + 64);   // 32 block ids of a chunk
+    int* s_tbl = reinterpret_cast<int*>(base + kMiscOff + 64);   // kChunkBlocks block ids of a chunk
 
     const int tid = threadIdx.x, warp = tid >> 5;
     pa_dev::wait_prior_grid();
@@ -117,15 +118,19 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         const int32_t* table = p.tables + static_cast<size_t>(p.g_members[moff]) * p.max_blocks;
         const int lbc = t0 / B, nbc = (t1 - t0) / B;
 
-        // validation (recorded, never trapped): members cover the span and agree
-        if (chunk == 0 && tid < m1 - m0 && seq_len(p, p.g_members[moff + m0 + tid]) < shared_tok)
-            pa_dev::record_error(p.err, PA_ERR_INVALID_ARG);
-        for (int e = tid; e < (m1 - m0) * nbc; e += kThreads) {
+        // validation (recorded, never trapped): members cover the span and agree;
+        // the tables do not depend on the head, so the head-0 item checks them
+        if (h == 0 && chunk == 0)
+            for (int mi = tid; mi < m1 - m0; mi += kThreads)
+                if (seq_len(p, p.g_members[moff + m0 + mi]) < shared_tok)
+                    pa_dev::record_error(p.err, PA_ERR_INVALID_ARG);
+        for (int e = tid; h == 0 && e < (m1 - m0) * nbc; e += kThreads) {
             const int mi = e / nbc, bi = e - mi * nbc;
             const int32_t* mt = p.tables + static_cast<size_t>(p.g_members[moff + m0 + mi]) * p.max_blocks;
             if (__ldg(mt + lbc + bi) != __ldg(table + lbc + bi))
                 pa_dev::record_error(p.err, PA_ERR_INVALID_ARG);
         }
+        static_assert(kChunkBlocks <= kThreads, "one thread per block of a chunk");
         if (tid < nbc) {
             int b = __ldg(table + lbc + tid);
             if (b < 0 || b >= p.num_blocks) {
@@ -383,6 +388,7 @@ int ensure_tensor_maps(pa_pool* pool) {
 }
 
 int shared_tc_rows() { return kRows; }
+int shared_tc_chunk_tokens() { return kChunkBlocks * 16; }
 
 int launch_shared_tc(pa_pool* pool, const DecodeParams& p, cudaStream_t st) {
     if (p.n_shared_items <= 0) return PA_OK;
