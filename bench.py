@@ -11,7 +11,7 @@ blocks needed, scattered block tables).  Other workloads: --workload
 
 value      = unique KV bytes the decode reads per step / device step time (GB/s),
              inputs resident in HBM, L2 flushed between steps (a 256 MiB write, then a
-             256 MiB read that leaves L2 holding clean lines).
+             read pass long enough that L2 holds only clean lines).
 e2e        = the same bytes / step time through the public API with host
              buffers: pinned host->device copies of the step's inputs, the
              three library calls, device->host copy of the output.
@@ -255,7 +255,10 @@ def run_ours(args):
     def flush_l2(i):
         # write a buffer larger than L2, then read another one: the timed step
         # starts with none of its inputs in L2 and no dirty lines of the flush
-        # left to write back
+        # left to write back.  The read is a uint8 sum, which torch widens
+        # through a 2 GiB int64 temporary that it then reads again: long enough
+        # to drain every write-back (a bare 256 MiB read left some of the
+        # fill's dirty lines to the timed step, and its times scattered).
         flush.fill_(i & 0xFF)
         flush_rd.sum()
 
@@ -337,7 +340,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic",
         "config": {"workload": _workload_desc(wl),
-                   "l2": "flushed between steps (256 MiB write then 256 MiB read, outside the timed events)",
+                   "l2": "flushed between steps (256 MiB write, then a 256 MiB uint8 sum that reads a 2 GiB int64 widening; outside the timed events)",
                    "kv_bytes_per_step": kv_bytes, "logical_kv_bytes_per_step": logical_kv_bytes,
                    "shared_groups": int(len(all_groups[2])),
                    "shared_path": bool(step.sharing()),

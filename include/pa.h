@@ -134,7 +134,15 @@ int pa_copy_blocks(pa_pool *pool, const int64_t *pairs, int num_pairs, void *str
  *   out           device [S][num_q_heads][head_dim] of out_dtype
  * Keys/values are read once per (sequence, KV head) for all G query heads;
  * long contexts are split over block ranges and merged by log-sum-exp in a
- * second kernel (two launches per call).
+ * second kernel (two launches per call).  Batches with more sequences than
+ * the GPU has SMs use partitions of at most 2048 tokens (environment
+ * PA_PT_MAX=<tokens> overrides, 0 = no cap); the split never produces more
+ * partials than the workspace holds.
+ * Environment PA_DECODE_STREAM=1 selects, for bf16 pools with block_size 16,
+ * head_dim 64 or 128, G <= 8 and S <= 4096, a one-launch stream-K split pass
+ * (every warp an equal run of (sequence, head, block) tiles fed by TMA, pieces
+ * of a sequence merged by the warp that finishes last); same results within
+ * the bf16 tolerance.  The variable is read on every call.
  * Arithmetic: bf16 pools use bf16 tensor-core products with fp32
  * accumulation and fp32 softmax (the probabilities enter the value product
  * as a bf16 high part plus a bf16 low part); f32 pools use fp32 CUDA cores.
@@ -180,10 +188,13 @@ int pa_decode_reserve(pa_pool *pool, int max_seqs, int max_q_heads);
  *   group_shared_blocks host int32 [num_groups]: number of leading table
  *                       entries that are the same physical blocks for every
  *                       member and lie wholly inside every member's context
- * For each group and KV head, tiles of up to 64 query rows (members x their G
- * heads) attend to the shared span together on the tensor cores; each
- * member's private suffix goes through the ordinary split path, and the
- * partials are merged by log-sum-exp.  Groups with fewer than two members
+ * For each group and KV head, tiles of up to 128 query rows (members x their
+ * G heads) attend to 1024-token chunks of the shared span together on the
+ * 5th-generation tensor cores (tcgen05: operands staged by TMA, accumulators
+ * in tensor memory; bf16 pools with head_dim 128, block_size 16, G <= 8; other
+ * tensor-core shapes use 64-row tiles on mma.sync, or PA_SHARED_MMA_SYNC=1 in
+ * the environment selects those); each member's private suffix goes through
+ * the ordinary split path, and the partials are merged by log-sum-exp.  Groups with fewer than two members
  * or no shared block are ignored; shapes outside the bf16 tensor-core path
  * (see pa_decode) fall back to pa_decode.  The device checks that members'
  * leading entries agree and that their contexts cover the shared span, and
@@ -209,8 +220,10 @@ int pa_decode_shared(pa_pool *pool, const void *q, int num_seqs, int num_q_heads
  * the library image that every GPU loading the library holds until the
  * process exits; nothing is allocated or freed by the call (it clears the
  * counters with cudaMemsetAsync on `stream`).  A batch whose partials do not
- * fit returns PA_ERR_UNSUPPORTED before launching anything (roughly: up to
- * 16384 sequences x KV heads at head_dim 128, G 4, on a 152-SM GB300).
+ * fit returns PA_ERR_UNSUPPORTED before launching anything (roughly:
+ * sequences x KV heads up to about 14,000 at head_dim 128, G 4, on a 152-SM
+ * GB300; when the array has less room than the partition cap would use, the
+ * kernel takes longer partitions instead).
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture
  * begins.  All calls on a device share the one array, which keeps the last

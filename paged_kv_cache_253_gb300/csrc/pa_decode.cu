@@ -999,7 +999,6 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(const DecodePar
 // Launched as a programmatic dependent of the split kernel: it may start while
 // the split kernel drains and waits (griddepcontrol.wait) for it to finish.
 __global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodeParams p) {
-    __shared__ float s_M[16], s_L[16];
     pa_dev::wait_prior_grid();
     pa_dev::allow_next_grid();
     const int s = blockIdx.x / p.Hkv, h = blockIdx.x - s * p.Hkv;
@@ -1014,55 +1013,51 @@ __global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodePara
                                      static_cast<size_t>(p.seq_member[s]) * nC) * p.Hkv + h
                                   : 0;
     const int nAll = nP + nC;
-    // partial q < nP: private item; q >= nP: shared chunk q - nP
-    auto ml_of = [&](int q, int n) -> const float* {
-        return q < nP ? p.part_ml + ((static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv) * p.G + n) * 2
-                      : p.spart_ml + ((slot0 + static_cast<size_t>(q - nP) * p.Hkv) * p.G + n) * 2;
-    };
-    // phase 1: per head, the running maxima and sums of all partitions give the
-    // merged max M, the merged sum L and one weight 2^(m_q - M) per partition
-    constexpr int kQ = 256;                                 // weights kept in shared memory
-    __shared__ float s_f[kQ][16];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int n = warp; n < p.G; n += kWarps) {
-        float M = -INFINITY;
-        for (int q = lane; q < nAll; q += 32) M = fmaxf(M, ml_of(q, n)[0]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float l = 0.f;
-        for (int q = lane; q < nAll; q += 32) {
-            const float* ml = ml_of(q, n);
-            const float f = M != -INFINITY ? pa_dev::ex2(ml[0] - M) : 0.f;
-            l += ml[1] * f;
-            if (q < kQ) s_f[q][n] = f;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) {
-            s_M[n] = M;
-            s_L[n] = l;
-        }
-    }
-    __syncthreads();
-    // phase 2: weighted sum of the partial accumulators, 4 values per thread
     const int GD = p.G * p.D;
+    // partial q < nP: private item; q >= nP: shared chunk q - nP
+    auto part = [&](int q) -> size_t {
+        return q < nP ? static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv
+                      : slot0 + static_cast<size_t>(q - nP) * p.Hkv;
+    };
+    // Each thread owns 4 consecutive elements of one head (D % 4 == 0) and
+    // folds the partials in by an online log-sum-exp, loading a batch of
+    // kBatch partials (their (max, sum) and its 4 values) at once so that a
+    // batch costs one memory latency.
+    constexpr int kBatch = 8;
     const size_t out0 = (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G) * p.D;
-    for (int e = threadIdx.x * 4; e < GD; e += kThreads * 4) {   // D % 4 == 0: never splits a head
+    for (int e = threadIdx.x * 4; e < GD; e += kThreads * 4) {
         const int n = e / p.D;
-        const float M = s_M[n], Lsum = s_L[n];
+        float M = -INFINITY, L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-#pragma unroll 4
-            for (int q = 0; q < nAll; ++q) {
-                const float f = q < kQ ? s_f[q][n] : pa_dev::ex2(ml_of(q, n)[0] - M);
-                const float* src = q < nP
-                    ? p.part_acc + (static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv) * GD
-                    : p.spart_acc + (slot0 + static_cast<size_t>(q - nP) * p.Hkv) * GD;
-                const float4 a = __ldcg(reinterpret_cast<const float4*>(src + e));
-                acc.x += f * a.x; acc.y += f * a.y; acc.z += f * a.z; acc.w += f * a.w;
+        for (int q0 = 0; q0 < nAll; q0 += kBatch) {
+            float2 ml[kBatch];
+            float4 x[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                ml[k] = make_float2(-INFINITY, 0.f);
+                x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (q0 + k < nAll) {
+                    const size_t it = part(q0 + k);
+                    const bool pr = q0 + k < nP;
+                    ml[k] = __ldcg(reinterpret_cast<const float2*>((pr ? p.part_ml : p.spart_ml) + (it * p.G + n) * 2));
+                    x[k] = __ldcg(reinterpret_cast<const float4*>((pr ? p.part_acc : p.spart_acc) + it * GD + e));
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (ml[k].x == -INFINITY) continue;         // absent, or a partial that saw nothing
+                const float nm = fmaxf(M, ml[k].x);
+                const float fo = M == -INFINITY ? 0.f : pa_dev::ex2(M - nm);
+                const float fn = pa_dev::ex2(ml[k].x - nm);
+                L = L * fo + ml[k].y * fn;
+                acc.x = acc.x * fo + x[k].x * fn;
+                acc.y = acc.y * fo + x[k].y * fn;
+                acc.z = acc.z * fo + x[k].z * fn;
+                acc.w = acc.w * fo + x[k].w * fn;
+                M = nm;
             }
         }
-        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
         store_out(p, out0 + e + 0, acc.x * inv);
         store_out(p, out0 + e + 1, acc.y * inv);
         store_out(p, out0 + e + 2, acc.z * inv);
