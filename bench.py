@@ -94,7 +94,7 @@ def _traffic_from_profile():
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         text = open(prof).read()
         m_hash = re.search(r"source sha256\[:16\]:\s*`?([0-9a-f]{16})", text)
-        m_tr = re.search(r"dram bytes per launch:\s*`?([0-9]+)", text)
+        m_tr = re.search(r"dram bytes per launch:\s*\|?\s*`?([0-9]+)", text)
         if m_hash and m_tr and m_hash.group(1) == digest:
             return int(m_tr.group(1))
     except OSError:
