@@ -34,6 +34,7 @@
 //     waiting) merges them and resets the counter.
 #include <algorithm>
 #include <cfloat>
+#include <climits>
 #include <cmath>
 #include <cstdlib>
 #include <cstdint>
@@ -76,6 +77,7 @@ namespace {
 
 constexpr int kWarps = PA_WARPS;
 constexpr int kPtMax = PA_PT_MAX_TOKENS;
+constexpr int kGuideMinPT = 256;        // shortest partition of the guided tail, tokens
 constexpr int kSharedStages = PA_SHARED_STAGES;
 constexpr int kSharedUnitsPerSync = PA_SHARED_UNITS_PER_SYNC;
 static_assert(kSharedStages > kSharedUnitsPerSync, "shared pipeline needs copies in flight");
@@ -113,6 +115,9 @@ __device__ __forceinline__ bool in_group(const DecodeParams& p, int s) {
 struct Sched {
     int PT;
     int total_items;    // private items (the shared ones come first in the item order)
+    int PTs;            // partition of sequences s >= S_split (the launch's last items)
+    int S_split;
+    __device__ __forceinline__ int pt(int s) const { return s >= S_split ? PTs : PT; }
 };
 
 // Every CTA derives the same private item list: per sequence nP =
@@ -123,18 +128,27 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
     const int per = (p.S + kThreads - 1) / kThreads;
     const int lo = min(p.S, tid * per), hi = min(p.S, lo + per);
     const bool report = blockIdx.x == 0;
+    // tokens before this thread's sequences (exclusive scan) and in all
     long long tok = 0;
     for (int s = lo; s < hi; ++s) tok += priv_len(p, s, report);
+    long long tinc = tok;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tok += __shfl_xor_sync(0xffffffffu, tok, o);
-    if (lane == 0) s_red[warp] = tok;
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, tinc, o);
+        if (lane >= o) tinc += y;
+    }
+    if (lane == 31) s_red[warp] = tinc;
     __syncthreads();
-    long long total = 0;
+    long long total = 0, tbase = tinc - tok;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) total += s_red[w];
-    int PT;
+    for (int w = 0; w < kWarps; ++w) {
+        total += s_red[w];
+        if (w < warp) tbase += s_red[w];
+    }
+    int PT, PTs;
+    long long split_at = LLONG_MAX;
     if (p.pt_fixed > 0) {
-        PT = p.pt_fixed;
+        PT = PTs = p.pt_fixed;
     } else {
         long long need = (total * p.Hkv + p.items_target - 1) / p.items_target;
         need = (need + p.B - 1) / p.B * p.B;
@@ -149,11 +163,41 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
             need = min(need, max(static_cast<long long>(p.pt_max), lo));
         }
         PT = static_cast<int>(max(need, static_cast<long long>(p.pt_min)));
+        // Guided tail: sequences that start in the last quarter of the tokens
+        // (they are the last items handed out) use partitions a quarter as long,
+        // so the launch ends on short items.  Their tokens are at most a quarter
+        // of the total, so items <= Hkv * (total/PT + total/(4 PTs) + S); used
+        // only when that fits the workspace, and only when the short partitions
+        // still hold kGuideMinPT tokens (shorter items cost more to start than
+        // they save at the end: measured on GB300).
+        PTs = max(p.pt_min, (PT / 4 + p.B - 1) / p.B * p.B);
+        const long long bound = static_cast<long long>(p.Hkv) *
+            ((total + PT - 1) / PT + (total + 4LL * PTs - 1) / (4LL * PTs) + p.S);
+        if (PTs < PT && PTs >= kGuideMinPT && bound <= p.max_items) split_at = total - total / 4;
+        else PTs = PT;
     }
+    // first sequence starting at or after split_at
+    __syncthreads();                                // s_red reuse
+    int* s_split = reinterpret_cast<int*>(s_red);
+    if (tid == 0) *s_split = p.S;
+    __syncthreads();
+    {
+        long long c = tbase;
+        for (int s = lo; s < hi; ++s) {
+            if (c >= split_at) {
+                atomicMin(s_split, s);
+                break;
+            }
+            c += priv_len(p, s, false);
+        }
+    }
+    __syncthreads();
+    const int S_split = *s_split;
+    __syncthreads();                                // s_red reuse below
     int cnt = 0;
     for (int s = lo; s < hi; ++s) {
-        const int L = priv_len(p, s, false);
-        cnt += max(1, (L + PT - 1) / PT) * p.Hkv;
+        const int L = priv_len(p, s, false), pts = s >= S_split ? PTs : PT;
+        cnt += max(1, (L + pts - 1) / pts) * p.Hkv;
     }
     int inc = cnt;                                  // inclusive scan over the block
 #pragma unroll
@@ -161,7 +205,6 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
         const int y = __shfl_up_sync(0xffffffffu, inc, o);
         if (lane >= o) inc += y;
     }
-    __syncthreads();                                // s_red reuse
     if (lane == 31) s_red[warp] = inc;
     __syncthreads();
     int base = inc - cnt;
@@ -169,12 +212,13 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
     int total_items = 0;
     for (int w = 0; w < kWarps; ++w) total_items += static_cast<int>(s_red[w]);
     for (int s = lo; s < hi; ++s) {
+        const int pts = s >= S_split ? PTs : PT;
         s_start[s] = base;
-        base += max(1, (priv_len(p, s, false) + PT - 1) / PT) * p.Hkv;
+        base += max(1, (priv_len(p, s, false) + pts - 1) / pts) * p.Hkv;
     }
     if (tid == 0) s_start[p.S] = total_items;
     __syncthreads();
-    return Sched{PT, total_items};
+    return Sched{PT, total_items, PTs, S_split};
 }
 
 __device__ __forceinline__ int find_seq(const int* s_start, int S, int item) {
@@ -263,6 +307,8 @@ __device__ void publish_schedule(const DecodeParams& p, const Sched& sc, const i
     if (blockIdx.x != 0) return;
     if (threadIdx.x == 0) {
         p.sched[0] = sc.PT;
+        p.ticket[2] = sc.PTs;                       // the header's two spare ints
+        p.ticket[3] = sc.S_split;
         p.sched[1] = sc.total_items;
     }
     for (int i = threadIdx.x; i <= p.S; i += kThreads) p.sched[2 + i] = s_start[i];
@@ -853,8 +899,9 @@ decode_fast_kernel(const DecodeParams p) {
         const int part = local / p.Hkv, h = local - part * p.Hkv;
         const int L = seq_len(p, s, false);
         const int start = priv_start(p, s);
-        const int nP = max(1, (max(0, L - start) + sc.PT - 1) / sc.PT);
-        const int tok0 = start + part * sc.PT, tok1 = min(L, tok0 + sc.PT);
+        const int PTq = sc.pt(s);
+        const int nP = max(1, (max(0, L - start) + PTq - 1) / PTq);
+        const int tok0 = start + part * PTq, tok1 = min(L, tok0 + PTq);
         fast_item<D, FUSE>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
         __syncthreads();
         // merge the warps' softmax states (in place into warp 0's buffer)
@@ -929,8 +976,9 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(const DecodePar
         const int local = item - s_start[s];
         const int part = local / p.Hkv, h = local - part * p.Hkv;
         const int L = seq_len(p, s, false);
-        const int nP = max(1, (L + sched.PT - 1) / sched.PT);
-        const int tok0 = part * sched.PT, nt = max(0, min(L, tok0 + sched.PT) - tok0);
+        const int PTq = sched.pt(s);
+        const int nP = max(1, (L + PTq - 1) / PTq);
+        const int tok0 = part * PTq, nt = max(0, min(L, tok0 + PTq) - tok0);
         const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
         for (int i = tid; i < p.G * p.D; i += kThreads)
             qs[i] = load_elem<E>(q, (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G) * p.D + i);
@@ -1002,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodePara
     pa_dev::wait_prior_grid();
     pa_dev::allow_next_grid();
     const int s = blockIdx.x / p.Hkv, h = blockIdx.x - s * p.Hkv;
-    const int PT = p.sched[0];
+    const int PT = s >= p.ticket[3] ? p.ticket[2] : p.sched[0];     // this sequence's partition
     const int nP = max(1, (priv_len(p, s, false) + PT - 1) / PT);
     const int grp = p.seq_group ? p.seq_group[s] : -1;
     if (nP == 1 && grp < 0) return;                        // written by the split kernel
@@ -1141,9 +1189,10 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
         plan->items_target = plan->grid * PA_ITEMS_PER_CTA;
         // items <= Hkv * (total / PT + S); PT >= total * Hkv / items_target keeps
         // that below min_items.  The extra items_target of room lets the
-        // partition cap take effect; the kernel never exceeds max_items.
+        // partition cap and the guided tail take effect; the kernel never
+        // exceeds max_items.
         plan->min_items = static_cast<size_t>(plan->items_target) + static_cast<size_t>(Hkv) * S;
-        plan->max_items = plan->min_items + (plan->pt_max > 0 ? static_cast<size_t>(plan->items_target) : 0);
+        plan->max_items = plan->min_items + static_cast<size_t>(plan->items_target);
     } else {
         plan->items_target = 0;
         const size_t per_seq = (static_cast<size_t>(max_blocks) * B + plan->pt_fixed - 1) / plan->pt_fixed;

@@ -39,7 +39,7 @@ constexpr int kD = 128;                  // head_dim of this path
 constexpr int kRows = 128;               // M: query rows per item
 constexpr int kStep = 64;                // tokens per step (N of S, K of P.V)
 constexpr int kTmemCols = 256;           // S [0,64), O [64,192), P hi [192,224), P lo [224,256)
-constexpr uint32_t kWaitLimit = 1u << 26;
+constexpr uint32_t kWaitLimit = 1u << 20;      // polls; milliseconds, far beyond any copy or MMA
 
 // shared-memory map (offsets from a 1024-aligned base); ~99 KB, two CTAs per SM
 constexpr uint32_t kQOff = 0;                            // 2 regions x [128 rows][128 B]
