@@ -30,6 +30,7 @@ import json
 import os
 import re
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -108,7 +109,9 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # sample file: PA_CLOCKS_DIR if set (to keep the raw samples), else the temp dir
+        self.path = os.path.join(os.environ.get("PA_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"pa_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
