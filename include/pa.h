@@ -261,7 +261,8 @@ uint64_t pa_launch_count(void);
  *     each), the first block's parent hash being 0; a table maps hash to
  *     physical block; admission reuses leading cached blocks while the
  *     chain hits (token ids and parent block compared too) and stops at the
- *     first miss.  A block leaves the hash table when freed.
+ *     first miss.  A block leaves the hash table when freed (unless
+ *     retention is on: pa_bm_set_retention).
  * Not thread-safe: one manager per thread. */
 
 /* free_order: host int32 [num_blocks], a permutation of 0..num_blocks-1 giving
@@ -328,6 +329,31 @@ int pa_bm_prefix_groups(pa_bm *bm, int n, const int32_t *reqs, int32_t *group_of
 /* 1 if the block is registered in the prefix hash table, 0 if not, -1 if out
  * of range. */
 int pa_bm_is_cached(pa_bm *bm, int block);
+
+/* Retention of cached blocks after their last user leaves ([Z] follow-up on
+ * how eviction interacts with the reference count, left unanswered there;
+ * [K] "Prefix Reuse Also Needs Compatible Computation": systems decide "which
+ * full blocks they retain for reuse").  Off by default (a freed block leaves
+ * the hash table at once).  With on != 0:
+ *   - a block still registered in the hash table whose count reaches zero
+ *     stays registered and becomes evictable instead of joining the free
+ *     pool; evictable blocks are kept in the order they were released;
+ *   - pa_bm_free_request releases a request's blocks deepest first, so a
+ *     chain's later blocks are evicted before its first ones;
+ *   - a new block (growth or copy-on-write) comes from the free pool while it
+ *     has one, else the least recently released evictable block is evicted:
+ *     it leaves the hash table and is reused;
+ *   - an admission hit on an evictable block takes it back (count 0 -> 1).
+ * on == 0 returns every evictable block to the free pool's tail (in release
+ * order), dropping its hash entry. */
+int pa_bm_set_retention(pa_bm *bm, int on);
+
+/* Number of evictable blocks (0 while retention is off); -1 for NULL. */
+int pa_bm_num_evictable(pa_bm *bm);
+
+/* Copy the evictable blocks, least recently released first, into
+ * out[0..cap); *n = their number. */
+int pa_bm_evictable_list(pa_bm *bm, int32_t *out, int cap, int *n);
 
 /* FNV-1a-64 of a byte string (exposed so the hash can be checked). */
 uint64_t pa_bm_fnv1a64(const uint8_t *data, size_t n);

@@ -30,8 +30,15 @@ Readings where the pages are silent (each listed in the design notes):
   - a hit also checks the stored token ids and parent block (collision guard);
   - a full block is registered when it becomes full; if an identical chain is
     already registered the first registration stays;
-  - a block leaves the hash table when its reference count reaches zero
-    (retention of unused cached blocks — eviction — is not modeled);
+  - a block leaves the hash table when its reference count reaches zero,
+    unless retention is on.  Retention (the zenaique follow-up on how eviction
+    interacts with the reference count is left unanswered; kgptalkie says
+    systems decide "which full blocks they retain for reuse"): a registered
+    block whose count reaches zero stays registered and evictable, in release
+    order; a finished request releases its blocks last one first; a new block
+    comes from the free pool while it has one, else the least recently
+    released evictable block is evicted (it leaves the hash table); an
+    admission hit on an evictable block takes it back;
   - a write into a block with reference count 1 happens in place.
 """
 from collections import deque
@@ -61,7 +68,7 @@ def block_hash(parent_hash: int, salt: int, tokens) -> int:
 
 
 class NaiveBlockManager:
-    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+    def __init__(self, num_blocks: int, block_size: int, free_order=None, retain=False):
         if num_blocks <= 0 or block_size <= 0:
             raise BlockManagerError("bad pool size")
         self.num_blocks = num_blocks
@@ -75,21 +82,29 @@ class NaiveBlockManager:
         self.block_key = {}      # registered block -> hash
         self.requests = {}       # id -> dict(table, tokens, hashes, salt)
         self.next_id = 0
+        self.retain = bool(retain)
+        self.evictable = []      # registered blocks nobody holds, least recently released first
 
     # -- helpers ---------------------------------------------------------
     def _take_free(self) -> int:
-        if not self.free:
-            raise BlockManagerError("no free block")
-        return self.free.popleft()
+        if self.free:
+            return self.free.popleft()
+        if self.evictable:                      # evict the least recently released cached block
+            blk = self.evictable.pop(0)
+            del self.cache[self.block_key.pop(blk)]
+            return blk
+        raise BlockManagerError("no free block")
 
     def _release(self, blk: int):
         if self.refcount[blk] <= 0:
             raise BlockManagerError("refcount underflow")
         self.refcount[blk] -= 1
         if self.refcount[blk] == 0:
-            h = self.block_key.pop(blk, None)
-            if h is not None:
-                del self.cache[h]
+            if blk in self.block_key:
+                if self.retain:
+                    self.evictable.append(blk)
+                    return
+                del self.cache[self.block_key.pop(blk)]
             self.free.append(blk)
 
     def _req(self, rid: int) -> dict:
@@ -114,6 +129,8 @@ class NaiveBlockManager:
             if entry is None or entry[1] != parent_blk or entry[2] != toks:
                 break
             blk = entry[0]
+            if self.refcount[blk] == 0:
+                self.evictable.remove(blk)      # in use again
             self.refcount[blk] += 1
             req["table"].append(blk)
             req["tokens"].extend(toks)
@@ -173,9 +190,17 @@ class NaiveBlockManager:
 
     def free_request(self, rid: int):
         req = self._req(rid)
-        for blk in req["table"]:
+        for blk in (reversed(req["table"]) if self.retain else req["table"]):
             self._release(blk)
         del self.requests[rid]
+
+    def set_retention(self, on: bool):
+        if not on:                               # retained blocks rejoin the free pool
+            for blk in self.evictable:
+                del self.cache[self.block_key.pop(blk)]
+                self.free.append(blk)
+            self.evictable = []
+        self.retain = bool(on)
 
     # -- queries ---------------------------------------------------------
     def block_table(self, rid: int) -> list:

@@ -72,6 +72,9 @@ SIGNATURES = {
     "pa_bm_num_free": (c_int, [c_void_p]),
     "pa_bm_free_list": (c_int, [c_void_p, c_i32p, c_int, c_intp]),
     "pa_bm_is_cached": (c_int, [c_void_p, c_int]),
+    "pa_bm_set_retention": (c_int, [c_void_p, c_int]),
+    "pa_bm_num_evictable": (c_int, [c_void_p]),
+    "pa_bm_evictable_list": (c_int, [c_void_p, c_i32p, c_int, c_intp]),
     "pa_bm_prefix_groups": (c_int, [c_void_p, c_int, c_i32p, c_i32p, c_i32p, c_i32p, c_intp]),
     "pa_bm_fnv1a64": (ctypes.c_uint64, [c_u8p, c_size_t]),
 }

@@ -295,6 +295,19 @@ class BlockManager:
     def is_cached(self, block):
         return L.pa_bm_is_cached(self.handle, int(block)) == 1
 
+    def set_retention(self, on):
+        L.check(L.pa_bm_set_retention(self.handle, 1 if on else 0), "pa_bm_set_retention")
+
+    def num_evictable(self):
+        return L.pa_bm_num_evictable(self.handle)
+
+    def evictable_list(self):
+        n = ctypes.c_int()
+        out = np.empty(self.num_blocks, dtype=np.int32)
+        L.check(L.pa_bm_evictable_list(self.handle, _i32p(out), self.num_blocks, ctypes.byref(n)),
+                "pa_bm_evictable_list")
+        return out[:n.value].tolist()
+
 
 def fnv1a64(data: bytes) -> int:
     buf = (ctypes.c_uint8 * max(len(data), 1)).from_buffer_copy(data or b"\0")

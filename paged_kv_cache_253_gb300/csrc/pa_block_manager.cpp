@@ -12,6 +12,8 @@
 #include <cstdint>
 #include <cstring>
 #include <deque>
+#include <iterator>
+#include <list>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -69,6 +71,12 @@ struct pa_bm {
     std::unordered_map<int32_t, uint64_t> block_key;     // cached block -> hash
     std::unordered_map<int, Request> requests;
     int next_id = 0;
+    // Retention (off unless pa_bm_set_retention turns it on): a cached block
+    // whose last user leaves stays in the hash table, evictable, in the order
+    // the blocks were released (least recent first).
+    bool retain = false;
+    std::list<int32_t> evictable;
+    std::unordered_map<int32_t, std::list<int32_t>::iterator> evict_pos;
 
     Request* find(int id) {
         auto it = requests.find(id);
@@ -79,11 +87,44 @@ struct pa_bm {
         if (--refcount[blk] == 0) {
             auto it = block_key.find(blk);
             if (it != block_key.end()) {
+                if (retain) {                   // keep it findable; reuse it last
+                    evictable.push_back(blk);
+                    evict_pos[blk] = std::prev(evictable.end());
+                    return;
+                }
                 cache.erase(it->second);
                 block_key.erase(it);
             }
             free_fifo.push_back(blk);
         }
+    }
+
+    // A block for new tokens: the free pool first, then the least recently
+    // released cached block (which leaves the hash table).  False: none left,
+    // nothing changed.
+    bool take(int32_t* out) {
+        if (!free_fifo.empty()) {
+            *out = free_fifo.front();
+            free_fifo.pop_front();
+            return true;
+        }
+        if (evictable.empty()) return false;
+        const int32_t b = evictable.front();
+        evictable.pop_front();
+        evict_pos.erase(b);
+        auto it = block_key.find(b);
+        cache.erase(it->second);
+        block_key.erase(it);
+        *out = b;
+        return true;
+    }
+
+    // A cache hit on a block nobody holds: it is in use again.
+    void revive(int32_t blk) {
+        auto it = evict_pos.find(blk);
+        if (it == evict_pos.end()) return;
+        evictable.erase(it->second);
+        evict_pos.erase(it);
     }
 
     int append(int id, int32_t token, int64_t* slot, int64_t* src, int64_t* dst) {
@@ -97,17 +138,14 @@ struct pa_bm {
         *src = -1;
         *dst = -1;
         if (offset == 0) {
-            if (free_fifo.empty()) return PA_ERR_NO_FREE_BLOCK;
-            blk = free_fifo.front();
-            free_fifo.pop_front();
+            if (!take(&blk)) return PA_ERR_NO_FREE_BLOCK;
             refcount[blk] = 1;
             r->table.push_back(blk);
         } else {
             blk = r->table[logical];
             if (refcount[blk] > 1) {           // another request still reads it: copy first
-                if (free_fifo.empty()) return PA_ERR_NO_FREE_BLOCK;
-                int32_t fresh = free_fifo.front();
-                free_fifo.pop_front();
+                int32_t fresh;
+                if (!take(&fresh)) return PA_ERR_NO_FREE_BLOCK;
                 refcount[blk] -= 1;
                 refcount[fresh] = 1;
                 r->table[logical] = fresh;
@@ -186,6 +224,7 @@ int pa_bm_add_request(pa_bm* bm, const int32_t* tokens, int n, uint64_t salt, in
             std::memcmp(it->second.tokens.data(), toks, sizeof(int32_t) * B) != 0)
             break;                                 // first miss ends the reuse
         int32_t blk = it->second.block;
+        if (bm->refcount[blk] == 0) bm->revive(blk);
         bm->refcount[blk] += 1;
         r.table.push_back(blk);
         r.tokens.insert(r.tokens.end(), toks, toks + B);
@@ -245,7 +284,12 @@ int pa_bm_free_request(pa_bm* bm, int req) {
     if (!r) return PA_ERR_UNKNOWN_REQUEST;
     for (int32_t b : r->table)
         if (bm->refcount[b] <= 0) return PA_ERR_REFCOUNT;
-    for (int32_t b : r->table) bm->release(b);
+    if (bm->retain) {
+        // deepest block first, so a chain's leaves are evicted before its root
+        for (auto it = r->table.rbegin(); it != r->table.rend(); ++it) bm->release(*it);
+    } else {
+        for (int32_t b : r->table) bm->release(b);
+    }
     bm->requests.erase(req);
     return PA_OK;
 }
@@ -346,6 +390,35 @@ int pa_bm_prefix_groups(pa_bm* bm, int n, const int32_t* reqs, int32_t* group_of
         group_offsets[++ng] = pos;
     }
     *num_groups = ng;
+    return PA_OK;
+}
+
+int pa_bm_set_retention(pa_bm* bm, int on) {
+    if (!bm) return PA_ERR_INVALID_ARG;
+    if (!on) {                                  // retained blocks leave the table, join the pool
+        for (int32_t b : bm->evictable) {
+            auto it = bm->block_key.find(b);
+            bm->cache.erase(it->second);
+            bm->block_key.erase(it);
+            bm->free_fifo.push_back(b);
+        }
+        bm->evictable.clear();
+        bm->evict_pos.clear();
+    }
+    bm->retain = on != 0;
+    return PA_OK;
+}
+
+int pa_bm_num_evictable(pa_bm* bm) { return bm ? static_cast<int>(bm->evictable.size()) : -1; }
+
+int pa_bm_evictable_list(pa_bm* bm, int32_t* out, int cap, int* n) {
+    if (!bm || !n || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID_ARG;
+    *n = static_cast<int>(bm->evictable.size());
+    int i = 0;
+    for (int32_t b : bm->evictable) {
+        if (i >= cap) break;
+        out[i++] = b;
+    }
     return PA_OK;
 }
 

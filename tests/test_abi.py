@@ -66,6 +66,8 @@ def test_fnv_vectors(lib):
 
 def _compare(cbm, nbm, live):
     assert cbm.free_list() == list(nbm.free)
+    assert cbm.evictable_list() == list(nbm.evictable)
+    assert cbm.num_evictable() == len(nbm.evictable)
     assert [cbm.refcount(b) for b in range(nbm.num_blocks)] == nbm.refcount
     assert [cbm.is_cached(b) for b in range(nbm.num_blocks)] == \
         [nbm.is_cached(b) for b in range(nbm.num_blocks)]
@@ -74,18 +76,26 @@ def _compare(cbm, nbm, live):
         assert cbm.seq_len(r) == nbm.seq_len(r)
 
 
-def test_cpp_block_manager_matches_naive_model(lib):
+@pytest.mark.parametrize("retain", [False, True], ids=["free-on-release", "retain-evict"])
+def test_cpp_block_manager_matches_naive_model(lib, retain):
     from paged_kv_cache_253_gb300.api import BlockManager
     from paged_kv_cache_253_gb300._lib import PagedAttnError
-    rng = np.random.default_rng(253)
+    rng = np.random.default_rng(253 + int(retain))
     for trial in range(40):
         B = int(rng.integers(1, 6))
         nb = int(rng.integers(3, 40))
         order = rng.permutation(nb)
-        cbm, nbm = BlockManager(nb, B, order), NaiveBlockManager(nb, B, order)
+        cbm, nbm = BlockManager(nb, B, order), NaiveBlockManager(nb, B, order, retain=retain)
+        cbm.set_retention(retain)
         live = []
         for step in range(250):
-            op = int(rng.integers(0, 12))
+            op = int(rng.integers(0, 13))
+            if op == 12:
+                if retain and rng.random() < 0.2:      # now and then switch retention off and on
+                    on = not nbm.retain
+                    cbm.set_retention(on)
+                    nbm.set_retention(on)
+                continue
             if op == 0 or not live:
                 toks = rng.integers(0, 3, size=int(rng.integers(0, 3 * B + 1))).tolist()
                 salt = int(rng.integers(0, 2))
@@ -179,3 +189,24 @@ def test_prefix_groups_follow_the_tables(lib):
     # no sharing at all: no groups
     offs, seqs, nsh = bm.prefix_groups([other])
     assert offs.tolist() == [0] and len(nsh) == 0
+
+
+def test_retention_evicts_and_reuses_in_the_cpp_manager(lib):
+    """Once the free pool is empty a retained block is evicted and reused: the
+    new owner's appends overwrite it, and a later admission of the old prompt
+    no longer hits it."""
+    from paged_kv_cache_253_gb300.api import BlockManager
+    B, nb = 16, 4
+    bm = BlockManager(nb, B)
+    bm.set_retention(True)
+    a, _ = bm.add_request([])
+    for t in range(2 * B):
+        bm.append_slot(a, t)
+    bm.free_request(a)
+    assert bm.evictable_list() == [1, 0]
+    c, _ = bm.add_request([])
+    for t in range(2 * B + 1):                        # blocks 2, 3, then evicts block 1
+        bm.append_slot(c, 100 + t)
+    assert bm.block_table(c) == [2, 3, 1] and not bm.is_cached(1)
+    d, cached = bm.add_request(list(range(2 * B)))
+    assert cached == B and bm.block_table(d) == [0]    # block 0 still hits, block 1 does not

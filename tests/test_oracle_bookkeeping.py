@@ -25,14 +25,18 @@ def _invariants(bm):
     assert refs == bm.refcount
     free = list(bm.free)
     assert len(set(free)) == len(free)
+    assert not (set(free) & set(bm.evictable)) and len(set(bm.evictable)) == len(bm.evictable)
     for b in range(bm.num_blocks):
-        assert (b in set(free)) == (bm.refcount[b] == 0)
+        # a block nobody holds is either free or (retention) cached and evictable
+        assert (b in set(free) or b in set(bm.evictable)) == (bm.refcount[b] == 0)
+    for b in bm.evictable:
+        assert b in bm.block_key
     for req in bm.requests.values():
         n = len(req["tokens"])
         slots = len(req["table"]) * bm.block_size
         assert 0 <= slots - n <= bm.block_size - 1        # tail waste below one block
     for h, (blk, _, _) in bm.cache.items():
-        assert bm.block_key[blk] == h and bm.refcount[blk] > 0
+        assert bm.block_key[blk] == h and (bm.refcount[blk] > 0 or blk in bm.evictable)
 
 
 # -- data movement --------------------------------------------------------
@@ -262,6 +266,97 @@ def test_random_operation_sequences_keep_invariants():
                 elif op == 2:
                     r = live.pop(int(rng.integers(len(live))))
                     bm.free_request(r)
+                else:
+                    bm.append_slot(live[int(rng.integers(len(live)))], int(rng.integers(0, 3)))
+            except BlockManagerError:
+                pass
+            _invariants(bm)
+
+
+# -- retention of cached blocks (eviction) ---------------------------------
+
+def _fill(bm, toks):
+    r, cached = bm.add_request(toks)
+    for t in toks[cached:]:
+        bm.append_slot(r, t)
+    return r
+
+
+def test_retention_keeps_a_finished_prefix_for_the_next_request():
+    bm = NaiveBlockManager(6, 2, retain=True)
+    a = _fill(bm, [1, 2, 3, 4, 5])                 # blocks 0, 1 full, 2 partial
+    assert bm.block_table(a) == [0, 1, 2]
+    bm.free_request(a)
+    assert bm.evictable == [1, 0]                  # deepest first; the partial block is free
+    assert list(bm.free) == [3, 4, 5, 2]
+    b, cached = bm.add_request([1, 2, 3, 4, 9])
+    assert cached == 4 and bm.block_table(b) == [0, 1]
+    assert bm.evictable == [] and bm.refcount[:2] == [1, 1]
+    assert list(bm.free) == [3, 4, 5, 2]           # nothing was allocated for the hit
+    _invariants(bm)
+
+
+def test_retention_evicts_least_recently_released_leaves_first():
+    bm = NaiveBlockManager(4, 2, retain=True)
+    a = _fill(bm, [1, 2, 3, 4])                    # blocks 0, 1
+    b = _fill(bm, [7, 8, 9, 9])                    # blocks 2, 3
+    bm.free_request(a)
+    bm.free_request(b)
+    assert bm.evictable == [1, 0, 3, 2] and not bm.free
+    c = _fill(bm, [5, 5])                          # needs one block: evicts a's last block
+    assert bm.block_table(c) == [1]
+    assert bm.evictable == [0, 3, 2]
+    d, cached = bm.add_request([1, 2, 3, 4])       # a's first block still hits; its second is gone
+    assert cached == 2 and bm.block_table(d) == [0]
+    _invariants(bm)
+
+
+def test_retention_evicts_only_when_the_free_pool_is_empty():
+    bm = NaiveBlockManager(5, 2, retain=True)
+    a = _fill(bm, [1, 2])
+    bm.free_request(a)
+    assert bm.evictable == [0] and list(bm.free) == [1, 2, 3, 4]
+    b = _fill(bm, [6, 6, 6, 6, 6, 6, 6, 6])        # four new blocks: the free pool suffices
+    assert bm.block_table(b) == [1, 2, 3, 4] and bm.evictable == [0] and bm.is_cached(0)
+    bm.append_slot(b, 6)                           # a fifth block: only the evictable one is left
+    assert bm.block_table(b)[-1] == 0 and bm.evictable == []
+    assert not bm.is_cached(0)                     # evicted; registered again only once it fills
+    _invariants(bm)
+
+
+def test_turning_retention_off_returns_retained_blocks_to_the_pool():
+    bm = NaiveBlockManager(4, 2, retain=True)
+    a = _fill(bm, [1, 2, 3, 4])
+    bm.free_request(a)
+    assert bm.evictable == [1, 0]
+    bm.set_retention(False)
+    assert bm.evictable == [] and not bm.cache and not bm.block_key
+    assert list(bm.free) == [2, 3, 1, 0]
+    _invariants(bm)
+
+
+def test_random_operation_sequences_keep_invariants_with_retention():
+    rng = np.random.default_rng(13)
+    for trial in range(30):
+        B = int(rng.integers(1, 6))
+        nb = int(rng.integers(4, 40))
+        bm = NaiveBlockManager(nb, B, free_order=list(rng.permutation(nb)), retain=True)
+        live = []
+        for step in range(200):
+            op = rng.integers(0, 12)
+            try:
+                if op == 0 or not live:
+                    toks = rng.integers(0, 3, size=int(rng.integers(0, 3 * B + 1))).tolist()
+                    r, cached = bm.add_request(toks)
+                    live.append(r)
+                    assert cached % B == 0 and cached <= len(toks)
+                elif op == 1:
+                    live.append(bm.fork(live[int(rng.integers(len(live)))]))
+                elif op in (2, 3):
+                    r = live.pop(int(rng.integers(len(live))))
+                    bm.free_request(r)
+                elif op == 4 and rng.random() < 0.1:
+                    bm.set_retention(not bm.retain)
                 else:
                     bm.append_slot(live[int(rng.integers(len(live)))], int(rng.integers(0, 3)))
             except BlockManagerError:
