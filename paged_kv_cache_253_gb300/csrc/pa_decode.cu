@@ -62,6 +62,9 @@
 #ifndef PA_PT_MAX_TOKENS
 #define PA_PT_MAX_TOKENS 2048    // partition cap in tokens for batches of many sequences
 #endif
+#ifndef PA_BLOCK_PREFETCH
+#define PA_BLOCK_PREFETCH 1     // L2 prefetch of the block a warp reads that many blocks ahead
+#endif
 #ifndef PA_STAGES
 #define PA_STAGES 0             // cp.async ring depth per warp (0/1: direct register loads)
 #endif
@@ -544,6 +547,18 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
                 my_phys = mine < lb1 ? __ldg(table + mine) : -1;
             }
             const int phys = __shfl_sync(0xffffffffu, my_phys, i & 31);
+#if PA_BLOCK_PREFETCH > 0
+            // start the block this warp reads PA_BLOCK_PREFETCH blocks from now
+            // towards L2 (bulk prefetch: no registers, no shared memory)
+            if (i + PA_BLOCK_PREFETCH < nblk && (i & 31) + PA_BLOCK_PREFETCH < 32) {
+                const int pphys = __shfl_sync(0xffffffffu, my_phys, (i + PA_BLOCK_PREFETCH) & 31);
+                if (lane == 0 && pphys >= 0 && pphys < p.num_blocks) {
+                    const size_t ptile = (static_cast<size_t>(pphys) * p.Hkv + h) * tile_elems;
+                    pa_dev::prefetch_l2(kpool + ptile, static_cast<uint32_t>(tile_elems * 2));
+                    pa_dev::prefetch_l2(vpool + ptile, static_cast<uint32_t>(tile_elems * 2));
+                }
+            }
+#endif
             if (phys < 0 || phys >= p.num_blocks) {
                 if (lane == 0) record_error(p.err, PA_ERR_BAD_BLOCK_ID);
                 continue;
