@@ -53,12 +53,15 @@ def _ptr(a, ctype):
 
 
 def _kind(a) -> int:
-    """0 for float32 storage, 1 for raw bfloat16 bits (uint16)."""
+    """0 for float32 storage, 1 for raw bfloat16 bits (uint16), 2 for float64
+    (fp8 codes already turned into their values, see ``oracle.fp8``)."""
     if a.dtype == np.float32:
         return 0
     if a.dtype == np.uint16:
         return 1
-    raise TypeError("pool storage must be float32 or uint16 bf16 bits")
+    if a.dtype == np.float64:
+        return 2
+    raise TypeError("pool storage must be float32, uint16 bf16 bits or float64")
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:

@@ -25,8 +25,9 @@
  *
  * Pool layout used by the oracle (its own, the plain logical one):
  *   K[num_blocks][Hkv][block_size][D] and V likewise, stored as raw float32
- *   (kind 0) or raw bfloat16 bits (kind 1); every element is widened exactly
- *   to double before use, and all arithmetic is double.
+ *   (kind 0), raw bfloat16 bits (kind 1) or double (kind 2: e.g. fp8 codes
+ *   already multiplied by their scale); every element is widened exactly to
+ *   double before use, and all arithmetic is double.
  *
  * Softmax is the textbook two-pass form: max, then exp-sum, then the
  * weighted sum of values — no online rescaling, no blocking.
@@ -56,6 +57,7 @@ int oracle_translate(int64_t pos, int block_size, const int32_t *table,
  * float32, so its bits shifted left by 16 are that float32 exactly. */
 static double elem(const void *base, size_t i, int kind) {
     float f;
+    if (kind == 2) return ((const double *)base)[i];
     if (kind == 0) {
         f = ((const float *)base)[i];
     } else {
