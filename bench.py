@@ -80,17 +80,21 @@ def _kv_bytes(wl, lens, groups=None):
 def _algo_bytes(wl, lens):
     """Everything the decode kernel must move: KV + q + out + tables + lens."""
     S = wl.num_seqs
-    q = S * wl.num_q_heads * wl.head_dim * wl.elem_bytes
+    q = S * wl.num_q_heads * wl.head_dim * (4 if wl.input_dtype == "f32" else 2)
     out = S * wl.num_q_heads * wl.head_dim * 4
     blocks = sum(-(-int(x) // wl.block_size) for x in lens)
     return _kv_bytes(wl, lens) + q + out + blocks * 4 + S * 4
 
 
-def _traffic_from_profile():
-    """DRAM bytes per launch of the decode kernel from the committed ncu summary,
-    valid only while the kernel source is unchanged."""
+def _traffic_from_profile(wl):
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary
+    of this workload and pool type, valid only while the kernel source is
+    unchanged."""
+    if wl.name != "decode" or wl.dtype not in ("bf16", "fp8"):
+        return None
     src = os.path.join(ROOT, "paged_kv_cache_253_gb300", "csrc", "pa_decode.cu")
-    prof = os.path.join(ROOT, "profiles", "decode_kernel_decode_batch.md")
+    name = "decode_kernel_decode_batch" + ("_fp8" if wl.dtype == "fp8" else "") + ".md"
+    prof = os.path.join(ROOT, "profiles", name)
     try:
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         text = open(prof).read()
@@ -197,12 +201,16 @@ def _oracle_sample(wl, values, target_s=12.0, threads=None):
     return gbs, done_seq / spent, threads, desc
 
 
+def _dtype_kw(args):
+    return {"dtype": args.kv_dtype} if args.kv_dtype else {}
+
+
 def run_reference(args):
     world, rank, local = _dist()
     if rank != 0:
         return 0
     from paged_kv_cache_253_gb300 import workloads as wls
-    wl = wls.make_workload(args.workload)
+    wl = wls.make_workload(args.workload, **_dtype_kw(args))
     values = wls.generate_values(wl, "cpu")
     per_step = max(2.0, 40.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
@@ -242,7 +250,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
 
-    wl = wls.make_workload(args.workload)
+    wl = wls.make_workload(args.workload, **_dtype_kw(args))
     values = wls.generate_values(wl, f"cuda:{local}", seed=wl.seed + 1000 * rank)
     pool, bm, _ = runtime.replay_setup(wl, values, f"cuda:{local}")
     step = runtime.prepare_step(wl, values, pool, bm)
@@ -370,7 +378,7 @@ def run_ours(args):
         "launches_per_step": step.launches(),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": _traffic_from_profile(), "kernel": "decode (pa_decode)",
+                     "traffic": _traffic_from_profile(wl), "kernel": "decode (pa_decode)",
                      "algorithmic_bytes_per_launch": algo_bytes},
         "e2e": {"value": round(world * kv_bytes / (ems * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(ems, 5), "h2d_bytes_per_step": h2d,
@@ -398,6 +406,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode",
                     choices=["tiny", "decode", "prefix", "long", "mixed"])
+    ap.add_argument("--kv-dtype", default=None, choices=["f32", "bf16", "fp8"],
+                    help="pool element type (default: the workload's own; fp8 = e4m3 codes)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -43,8 +43,15 @@ extern "C" {
 typedef struct pa_pool pa_pool;
 typedef struct pa_bm pa_bm;
 
-/* Element type of the pool, of q/k/v inputs and (for out) of the output. */
-typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+/* Element type of the pool, of q/k/v inputs and (for out) of the output.
+ * PA_FP8E4M3 is a pool type only ([K] "Split the Cache Into Fixed Blocks": a
+ * block's bytes depend on the dtype): each key and value element is one e4m3
+ * byte (sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinity,
+ * largest magnitude 448) standing for code * the pool's K or V scale.  Such a
+ * pool takes bf16 k/v to append and bf16 queries, quantizing on the GPU:
+ * code = e4m3(fl32(x / scale)), to nearest, ties to even, beyond 448
+ * saturating to 448. */
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8E4M3 = 2 } pa_dtype;
 
 enum {
     PA_OK = 0,
@@ -94,9 +101,18 @@ int pa_pool_import(pa_pool *pool, const void *k_src, const void *v_src, void *st
 int pa_pool_info(const pa_pool *pool, int *num_blocks, int *block_size, int *kv_heads,
                  int *head_dim, int *dtype);
 
+/* Scales of a PA_FP8E4M3 pool: a K code c stands for e4m3(c) * k_scale, a V
+ * code for e4m3(c) * v_scale (both 1.0 at creation).  Appends quantize with the
+ * scales current at the call and decodes dequantize with those current at
+ * theirs, so set them before the first append.  Both must be finite and > 0
+ * (else PA_ERR_INVALID_ARG); another pool type gives PA_ERR_DTYPE.  Host only. */
+int pa_pool_set_kv_scales(pa_pool *pool, float k_scale, float v_scale);
+int pa_pool_kv_scales(const pa_pool *pool, float *k_scale, float *v_scale);
+
 /* Write each new token's keys and values into its slot ([Z] answer: a new
  * token "is written there"; [K] "Growth Needs Only Another Free Block").
- *   k, v          device [T][kv_heads][head_dim], pool dtype, row-major
+ *   k, v          device [T][kv_heads][head_dim], pool dtype (bf16 for an fp8 pool),
+ *                 row-major
  *   slot_mapping  device int64 [T]; slot = block * block_size + offset;
  *                 negative = skip; >= num_blocks * block_size records
  *                 PA_ERR_BAD_SLOT and is skipped
@@ -125,7 +141,8 @@ int pa_copy_blocks(pa_pool *pool, const int64_t *pairs, int num_pairs, void *str
  *                                         j = 0 .. context_lens[s]-1, where
  *   K_s[j] is the key in block block_tables[s][j / block_size] at offset
  *   j % block_size;   out[s][h] = sum_j softmax(x)_j * V_s[j][kv].
- *   q             device [S][num_q_heads][head_dim], pool dtype
+ *   q             device [S][num_q_heads][head_dim], pool dtype (bf16 for an
+ *                 fp8 pool)
  *   block_tables  device int32 [S][max_blocks_per_seq]; entries past a
  *                 sequence's last block are never read
  *   context_lens  device int32 [S]; 0 gives an all-zero output row; larger
@@ -152,22 +169,29 @@ int pa_copy_blocks(pa_pool *pool, const int64_t *pairs, int num_pairs, void *str
  * S <= 16384.
  * Workspace: the pool keeps a device workspace for the split partials; a
  * call that needs more than it holds grows it (cudaMalloc, synchronous).
- * pa_decode_reserve sizes it ahead of time. */
+ * pa_decode_reserve sizes it ahead of time.
+ * fp8 pool: K and V above are the dequantized values (code * k_scale,
+ * code * v_scale).  On the tensor-core shapes (block_size % 16 == 0, head_dim
+ * 64/128/256, G <= 8) the codes are widened exactly to f16 and each query to
+ * f16 (exact for bf16 values of magnitude 2^-17 .. 65504), products are summed
+ * in fp32, k_scale is applied to the scores and v_scale to the sums; other
+ * shapes run the fp32 CUDA-core kernel on the dequantized values. */
 int pa_decode(pa_pool *pool, const void *q, int num_seqs, int num_q_heads,
               const int32_t *block_tables, int max_blocks_per_seq,
               const int32_t *context_lens, float scale, void *out, pa_dtype out_dtype,
               void *stream);
 
 /* Append then decode in one call: for each sequence s, its new token's keys
- * and values k[s], v[s] ([S][kv_heads][head_dim], pool dtype, device) are
+ * and values k[s], v[s] ([S][kv_heads][head_dim], pool dtype (bf16 for an
+ * fp8 pool), device) are
  * written to slot_mapping[s] (device int64 [S]; negative = no token), exactly
  * as pa_append_kv with T = S would, and then decode attention runs exactly as
  * pa_decode.  Each slot must be the slot of position context_lens[s] - 1 of
  * sequence s (the token the decode of s reads last); otherwise nothing is
  * written for it and PA_ERR_INVALID_ARG is recorded on the device.  On the
  * bf16 tensor-core path the write is done inside the decode kernel by the warp
- * that reads that block (one launch fewer per step); other shapes run
- * pa_append_kv and pa_decode back to back.  Copy-on-write copies, if any,
+ * that reads that block (one launch fewer per step); other shapes, and fp8
+ * pools, run pa_append_kv and pa_decode back to back.  Copy-on-write copies, if any,
  * must be issued before (pa_copy_blocks). */
 int pa_append_decode(pa_pool *pool, const void *k, const void *v, const int64_t *slot_mapping,
                      const void *q, int num_seqs, int num_q_heads, const int32_t *block_tables,

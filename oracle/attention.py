@@ -87,7 +87,7 @@ def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, num_kv_he
     """Paged decode attention in float64.
 
     q            [S, Hq, D]              any float dtype (upcast to float64)
-    k_pool,v_pool[num_blocks, Hkv, B, D] float32, or uint16 bfloat16 bits
+    k_pool,v_pool[num_blocks, Hkv, B, D] float32, uint16 bfloat16 bits, or float64
     block_tables [S, max_blocks]         int32
     context_lens [S]                     int32 — tokens each query sees
     Returns out [S, Hq, D] float64.  ``threads`` splits the batch by sequence

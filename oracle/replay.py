@@ -6,12 +6,18 @@ the oracle's own bit-level pools in the order the events happen, then runs the
 decode step (each batch entry appends its token, then attends over all of its
 cached tokens, its new one included) and the float64 attention.
 
+An fp8 workload's pools hold e4m3 codes: each appended bf16 row is quantized
+with the pool's K or V scale when it is written, and the attention reads the
+codes' values times the scales (the e4m3 format and its rounding are in
+fp8.py).
+
 The only thing shared with the GPU side is the workload description and the
 seeded values; the bookkeeping, the data movement and the attention are all
 the oracle's own.
 """
 import numpy as np
 
+from . import fp8
 from .attention import paged_decode
 from .block_manager import NaiveBlockManager
 from .kvcache import append_kv, copy_blocks
@@ -25,6 +31,23 @@ def values_to_numpy(t):
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
     return t.numpy().astype(np.float32, copy=False)
+
+
+def _bf16_bits_to_f32(b):
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _stored(wl, t, which):
+    """Rows as the pool stores them: the input bits, or for an fp8 pool the
+    e4m3 codes of the bf16 values under the K (which=0) or V (which=1) scale."""
+    x = values_to_numpy(t)
+    if wl.dtype != "fp8":
+        return x
+    out = np.empty(x.shape, dtype=np.uint8)
+    step = max(1, (1 << 22) // max(1, int(np.prod(x.shape[1:]))))     # bounded temporaries
+    for lo in range(0, x.shape[0], step):
+        out[lo:lo + step] = fp8.quantize(_bf16_bits_to_f32(x[lo:lo + step]), wl.kv_scales[which])
+    return out
 
 
 class OracleState:
@@ -45,12 +68,12 @@ def replay(wl, values, *, run_step=True):
     """Replay ``wl``'s setup script (and its decode-step appends if run_step)."""
     st = OracleState()
     bm = NaiveBlockManager(wl.num_blocks, wl.block_size, wl.free_order)
-    store = np.float32 if wl.dtype == "f32" else np.uint16
+    store = {"f32": np.float32, "bf16": np.uint16, "fp8": np.uint8}[wl.dtype]
     shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
     K = np.zeros(shape, store)
     V = np.zeros(shape, store)
-    hk = values_to_numpy(values["hist_k"])
-    hv = values_to_numpy(values["hist_v"])
+    hk = _stored(wl, values["hist_k"], 0)
+    hv = _stored(wl, values["hist_v"], 1)
     row = 0
     pend_slots, pend_rows, pend_set = [], [], set()
 
@@ -88,8 +111,8 @@ def replay(wl, values, *, run_step=True):
     flush()
 
     if run_step:
-        nk = values_to_numpy(values["new_k"])
-        nv = values_to_numpy(values["new_v"])
+        nk = _stored(wl, values["new_k"], 0)
+        nv = _stored(wl, values["new_v"], 1)
         slots = []
         for i, rid in enumerate(wl.batch.tolist()):
             slot, src, dst = bm.append_slot(rid, int(wl.step_tokens[i]))
@@ -116,10 +139,19 @@ def attention(wl, values, st, seqs=None, threads=1):
     """float64 decode attention for all batch entries (or the listed ones)."""
     q = values_to_numpy(values["q"])
     if q.dtype == np.uint16:
-        q = (q.astype(np.uint32) << 16).view(np.float32)
+        q = _bf16_bits_to_f32(q)
     bt, lens = st.block_tables, st.context_lens
     if seqs is not None:
         seqs = np.asarray(seqs, dtype=np.int64)
         q, bt, lens = q[seqs], bt[seqs], lens[seqs]
-    return paged_decode(q, st.k_pool, st.v_pool, bt, lens, wl.scale, wl.num_kv_heads,
-                        threads=threads)
+    kp, vp = st.k_pool, st.v_pool
+    if wl.dtype == "fp8":
+        # the values the codes stand for, of the blocks these tables reach
+        # (renumbered so that only those are widened to float64)
+        used = np.unique(bt[bt >= 0])
+        renum = np.full(kp.shape[0], -1, dtype=np.int32)
+        renum[used] = np.arange(len(used), dtype=np.int32)
+        bt = np.where(bt >= 0, renum[np.maximum(bt, 0)], -1).astype(np.int32)
+        kp = fp8.dequantize(kp[used], wl.kv_scales[0])
+        vp = fp8.dequantize(vp[used], wl.kv_scales[1])
+    return paged_decode(q, kp, vp, bt, lens, wl.scale, wl.num_kv_heads, threads=threads)

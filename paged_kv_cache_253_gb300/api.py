@@ -11,9 +11,11 @@ import torch
 
 from . import _lib as L
 
-_TORCH = {L.PA_F32: torch.float32, L.PA_BF16: torch.bfloat16}
+# pool element type -> (torch type of k/v/q inputs, torch type of the stored elements)
+_TORCH = {L.PA_F32: (torch.float32, torch.float32), L.PA_BF16: (torch.bfloat16, torch.bfloat16),
+          L.PA_FP8E4M3: (torch.bfloat16, torch.uint8)}
 _CODE = {torch.float32: L.PA_F32, torch.bfloat16: L.PA_BF16, "f32": L.PA_F32,
-         "bf16": L.PA_BF16}
+         "bf16": L.PA_BF16, "fp8": L.PA_FP8E4M3, "fp8e4m3": L.PA_FP8E4M3}
 
 
 def _stream():
@@ -40,7 +42,9 @@ class KVPool:
     """A pool of fixed-size physical KV blocks on one GPU (one layer).
 
     K is [num_blocks, kv_heads, block_size, head_dim]; V is stored transposed
-    per tile, [num_blocks, kv_heads, head_dim, block_size].
+    per tile, [num_blocks, kv_heads, head_dim, block_size].  dtype "fp8" keeps
+    one e4m3 code per element (stored as uint8; a code stands for its value
+    times the pool's K or V scale) and takes bf16 k, v and q.
     """
 
     def __init__(self, num_blocks, block_size, kv_heads, head_dim, dtype="bf16", device=None):
@@ -49,7 +53,8 @@ class KVPool:
             raise ValueError("KVPool lives on a CUDA device")
         self.device = dev if dev.index is not None else torch.device("cuda", torch.cuda.current_device())
         self.dtype_code = _CODE[dtype]
-        self.dtype = _TORCH[self.dtype_code]
+        self.dtype, self.storage_dtype = _TORCH[self.dtype_code]
+        self.fp8 = self.dtype_code == L.PA_FP8E4M3
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         self.kv_heads, self.head_dim = int(kv_heads), int(head_dim)
         h = ctypes.c_void_p()
@@ -58,6 +63,17 @@ class KVPool:
                                      self.head_dim, self.dtype_code, ctypes.byref(h)),
                     "pa_pool_create")
         self.handle = h
+
+    def set_kv_scales(self, k_scale, v_scale):
+        """Scales of an fp8 pool (set them before the first append)."""
+        L.check(L.pa_pool_set_kv_scales(self.handle, float(k_scale), float(v_scale)),
+                "pa_pool_set_kv_scales")
+
+    def kv_scales(self):
+        k, v = ctypes.c_float(), ctypes.c_float()
+        L.check(L.pa_pool_kv_scales(self.handle, ctypes.byref(k), ctypes.byref(v)),
+                "pa_pool_kv_scales")
+        return k.value, v.value
 
     def close(self):
         if getattr(self, "handle", None):
@@ -171,16 +187,16 @@ class KVPool:
     def export(self):
         """Copies of (K, V) as device tensors in the pool's own layout."""
         k = torch.empty((self.num_blocks, self.kv_heads, self.block_size, self.head_dim),
-                        dtype=self.dtype, device=self.device)
+                        dtype=self.storage_dtype, device=self.device)
         v = torch.empty((self.num_blocks, self.kv_heads, self.head_dim, self.block_size),
-                        dtype=self.dtype, device=self.device)
+                        dtype=self.storage_dtype, device=self.device)
         L.check(L.pa_pool_export(self.handle, ctypes.c_void_p(k.data_ptr()),
                                  ctypes.c_void_p(v.data_ptr()), _stream()), "pa_pool_export")
         return k, v
 
     def import_(self, k, v):
-        L.check(L.pa_pool_import(self.handle, _dev(k, self.dtype, "k", self.device),
-                                 _dev(v, self.dtype, "v", self.device), _stream()),
+        L.check(L.pa_pool_import(self.handle, _dev(k, self.storage_dtype, "k", self.device),
+                                 _dev(v, self.storage_dtype, "v", self.device), _stream()),
                 "pa_pool_import")
 
 

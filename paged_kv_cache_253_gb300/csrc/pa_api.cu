@@ -22,8 +22,6 @@ void count_launch() { g_launch_counter.fetch_add(1, std::memory_order_relaxed); 
 
 namespace {
 
-constexpr double kLog2e = 1.4426950408889634;
-
 size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 
 struct DeviceGuard {
@@ -38,7 +36,7 @@ struct DeviceGuard {
     }
 };
 
-size_t elem_size(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
+size_t elem_size(pa_dtype t) { return pool_elem_size(t); }
 
 // Workspace: [header: ticket + schedule, 256-aligned][part_acc][part_ml]
 size_t workspace_bytes(const pa_detail::DecodePlan& plan, int S, int Hkv, int G, int D,
@@ -85,7 +83,7 @@ int pa_pool_create(int num_blocks, int block_size, int kv_heads, int head_dim, p
     if (!out || num_blocks <= 0 || block_size <= 0 || block_size > 1024 || kv_heads <= 0 ||
         head_dim <= 0 || head_dim > 256 || head_dim % 4 != 0)
         return PA_ERR_INVALID_ARG;
-    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_DTYPE;
+    if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_FP8E4M3) return PA_ERR_DTYPE;
     *out = nullptr;
     pa_pool* p = new (std::nothrow) pa_pool();
     if (!p) return PA_ERR_OUT_OF_MEMORY;
@@ -177,6 +175,24 @@ int pa_pool_info(const pa_pool* pool, int* num_blocks, int* block_size, int* kv_
     if (kv_heads) *kv_heads = pool->kv_heads;
     if (head_dim) *head_dim = pool->head_dim;
     if (dtype) *dtype = pool->dtype;
+    return PA_OK;
+}
+
+int pa_pool_set_kv_scales(pa_pool* pool, float k_scale, float v_scale) {
+    if (!pool) return PA_ERR_INVALID_ARG;
+    if (pool->dtype != PA_FP8E4M3) return PA_ERR_DTYPE;
+    // finite and positive (NaN fails both comparisons)
+    if (!(k_scale > 0.f && k_scale <= 3.4028235e38f) || !(v_scale > 0.f && v_scale <= 3.4028235e38f))
+        return PA_ERR_INVALID_ARG;
+    pool->k_scale = k_scale;
+    pool->v_scale = v_scale;
+    return PA_OK;
+}
+
+int pa_pool_kv_scales(const pa_pool* pool, float* k_scale, float* v_scale) {
+    if (!pool) return PA_ERR_INVALID_ARG;
+    if (k_scale) *k_scale = pool->k_scale;
+    if (v_scale) *v_scale = pool->v_scale;
     return PA_OK;
 }
 
@@ -332,7 +348,7 @@ static int decode_impl(pa_pool* pool, const void* q, int num_seqs, int num_q_hea
     p.part_ml = reinterpret_cast<float*>(
         static_cast<char*>(pool->ws) + cb + round256(plan.max_items * G * pool->head_dim * sizeof(float)));
     p.err = pool->err;
-    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    decode_scales(pool, scale, &p);
     p.S = num_seqs;
     p.Hq = num_q_heads;
     p.Hkv = pool->kv_heads;

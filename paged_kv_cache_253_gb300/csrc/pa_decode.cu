@@ -289,14 +289,14 @@ __device__ void finish_item(const DecodeParams& p, int item, int s, int h, int n
         for (int idx = tid; idx < GD; idx += kThreads) {
             const int n = idx / p.D, d = idx - n * p.D;
             const float l = res_l[n];
-            store_out(p, out0 + idx, l > 0.f ? res_acc[n * stride + d] / l : 0.f);
+            store_out(p, out0 + idx, l > 0.f ? res_acc[n * stride + d] * p.v_scale / l : 0.f);
         }
         return;
     }
     float* pacc = p.part_acc + static_cast<size_t>(item) * GD;
     for (int idx = tid; idx < GD; idx += kThreads) {
         const int n = idx / p.D, d = idx - n * p.D;
-        pacc[idx] = res_acc[n * stride + d];
+        pacc[idx] = res_acc[n * stride + d] * p.v_scale;
     }
     if (tid < p.G) {
         p.part_ml[(static_cast<size_t>(item) * p.G + tid) * 2 + 0] = res_m[tid];
@@ -338,8 +338,9 @@ struct WarpAcc {
     float m0, m1, l0, l1;                 // running max / sum (log2 units), heads 2c, 2c+1
 };
 
-// One 16-token tile: scores, online-softmax update, value product.
-template <int D>
+// One 16-token tile: scores, online-softmax update, value product.  F8: the
+// fragments hold f16 pairs (widened e4m3 codes, f16 queries) instead of bf16.
+template <int D, bool F8 = false>
 __device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D / 32],
                                             const uint4 (&k1)[D / 32], uint2 (&v0)[D / 16],
                                             uint2 (&v1)[D / 16], int nvalid, float sl, int r0,
@@ -348,8 +349,13 @@ __device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D /
     float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};   // two chains
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-        pa_dev::mma_bf16_16816(sc, k0[j].x, k1[j].x, k0[j].y, k1[j].y, a.qf[j].x, a.qf[j].y);
-        pa_dev::mma_bf16_16816(sd, k0[j].z, k1[j].z, k0[j].w, k1[j].w, a.qf[j].z, a.qf[j].w);
+        if constexpr (F8) {
+            pa_dev::mma_f16_16816(sc, k0[j].x, k1[j].x, k0[j].y, k1[j].y, a.qf[j].x, a.qf[j].y);
+            pa_dev::mma_f16_16816(sd, k0[j].z, k1[j].z, k0[j].w, k1[j].w, a.qf[j].z, a.qf[j].w);
+        } else {
+            pa_dev::mma_bf16_16816(sc, k0[j].x, k1[j].x, k0[j].y, k1[j].y, a.qf[j].x, a.qf[j].y);
+            pa_dev::mma_bf16_16816(sd, k0[j].z, k1[j].z, k0[j].w, k1[j].w, a.qf[j].z, a.qf[j].w);
+        }
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) sc[i] += sd[i];
@@ -388,16 +394,47 @@ __device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D /
         a.o[t][0] *= cr0; a.o[t][1] *= cr1;
         a.o[t][2] *= cr0; a.o[t][3] *= cr1;
     }
-    const uint32_t h01 = pa_dev::pack_bf16(p0, p1), h23 = pa_dev::pack_bf16(p2, p3);
-    const uint32_t e01 = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(h01), p1 - pa_dev::bf16_hi(h01));
-    const uint32_t e23 = pa_dev::pack_bf16(p2 - pa_dev::bf16_lo(h23), p3 - pa_dev::bf16_hi(h23));
+    uint32_t h01, h23, e01, e23;          // probabilities as a rounded pair plus the remainder
+    if constexpr (F8) {
+        h01 = pa_dev::pack_f16(p0, p1);
+        h23 = pa_dev::pack_f16(p2, p3);
+        e01 = pa_dev::pack_f16(p0 - pa_dev::f16_lo(h01), p1 - pa_dev::f16_hi(h01));
+        e23 = pa_dev::pack_f16(p2 - pa_dev::f16_lo(h23), p3 - pa_dev::f16_hi(h23));
+    } else {
+        h01 = pa_dev::pack_bf16(p0, p1);
+        h23 = pa_dev::pack_bf16(p2, p3);
+        e01 = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(h01), p1 - pa_dev::bf16_hi(h01));
+        e23 = pa_dev::pack_bf16(p2 - pa_dev::bf16_lo(h23), p3 - pa_dev::bf16_hi(h23));
+    }
     const uint32_t bh0 = pa_dev::movmatrix_trans(h01), bh1 = pa_dev::movmatrix_trans(h23);
     const uint32_t be0 = pa_dev::movmatrix_trans(e01), be1 = pa_dev::movmatrix_trans(e23);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, bh0, bh1);
-        pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, be0, be1);
+        if constexpr (F8) {
+            pa_dev::mma_f16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, bh0, bh1);
+            pa_dev::mma_f16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, be0, be1);
+        } else {
+            pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, bh0, bh1);
+            pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, be0, be1);
+        }
     }
+}
+
+// Eight e4m3 codes (8 bytes) widened to four f16 pairs, and four to two.
+__device__ __forceinline__ uint4 widen8(uint2 c) {
+    return make_uint4(pa_dev::e4m3x2_to_f16x2(c.x), pa_dev::e4m3x2_to_f16x2(c.x >> 16),
+                      pa_dev::e4m3x2_to_f16x2(c.y), pa_dev::e4m3x2_to_f16x2(c.y >> 16));
+}
+__device__ __forceinline__ uint2 widen4(uint32_t c) {
+    return make_uint2(pa_dev::e4m3x2_to_f16x2(c), pa_dev::e4m3x2_to_f16x2(c >> 16));
+}
+// Eight bf16 values re-rounded to f16 (exact for magnitudes 2^-17 .. 65504).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+    return pa_dev::pack_f16(pa_dev::bf16_lo(x), pa_dev::bf16_hi(x));
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x) {
+    return make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                      bf16x2_to_f16x2(x.w));
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
@@ -418,11 +455,17 @@ __device__ __forceinline__ void cp_async_wait() {
 // ahead of the unit being computed, so each warp keeps several tiles in
 // flight.  K rows are stored with 16-byte chunk c of odd rows at c ^ 4, which
 // makes the fragment reads below bank-conflict free.
-template <int D, bool FUSE>
+//
+// F8 (fp8 pool, direct loads only): the same fragments are read as e4m3
+// codes, half the bytes (8 per K chunk, 4 per V^T row piece), and widened to
+// f16 pairs in registers; the queries are re-rounded to f16 once per item.
+template <int D, bool FUSE, bool F8 = false>
 __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, int tok0,
                                           int tok1, int L, unsigned char* ring, float* sm_o,
                                           float* sm_m, float* sm_l) {
+    static_assert(!(F8 && FUSE), "an fp8 pool appends in its own (quantizing) kernel");
     constexpr int NJ = D / 32, NT = D / 16;
+    constexpr int ES = F8 ? 1 : 2;        // bytes per pool element
     constexpr int OS = D + 4;             // padded row stride of the merge buffer
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -433,9 +476,11 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
         const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
                                (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G + g) * D;
 #pragma unroll
-        for (int j = 0; j < NJ; ++j)
+        for (int j = 0; j < NJ; ++j) {
             a.qf[j] = g < p.G ? __ldg(reinterpret_cast<const uint4*>(qrow + (4 * j + c) * 8))
                               : make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (F8) a.qf[j] = bf16x8_to_f16x8(a.qf[j]);
+        }
     }
 #pragma unroll
     for (int t = 0; t < NT; ++t) a.o[t][0] = a.o[t][1] = a.o[t][2] = a.o[t][3] = 0.f;
@@ -451,6 +496,7 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
     const int nblk = lb1 > lb0 + warp ? (lb1 - lb0 - warp + kWarps - 1) / kWarps : 0;
 
 #if PA_STAGES > 1
+    static_assert(!F8, "the staged ring holds bf16 tiles");
     constexpr int S = PA_STAGES;
     constexpr int UNIT = 64 * D;          // bytes per stage: K 16 x D + V^T D x 16, bf16
     const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
@@ -553,9 +599,11 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
             if (i + PA_BLOCK_PREFETCH < nblk && (i & 31) + PA_BLOCK_PREFETCH < 32) {
                 const int pphys = __shfl_sync(0xffffffffu, my_phys, (i + PA_BLOCK_PREFETCH) & 31);
                 if (lane == 0 && pphys >= 0 && pphys < p.num_blocks) {
-                    const size_t ptile = (static_cast<size_t>(pphys) * p.Hkv + h) * tile_elems;
-                    pa_dev::prefetch_l2(kpool + ptile, static_cast<uint32_t>(tile_elems * 2));
-                    pa_dev::prefetch_l2(vpool + ptile, static_cast<uint32_t>(tile_elems * 2));
+                    const size_t ptile = (static_cast<size_t>(pphys) * p.Hkv + h) * tile_elems * ES;
+                    pa_dev::prefetch_l2(static_cast<const char*>(p.k) + ptile,
+                                        static_cast<uint32_t>(tile_elems * ES));
+                    pa_dev::prefetch_l2(static_cast<const char*>(p.v) + ptile,
+                                        static_cast<uint32_t>(tile_elems * ES));
                 }
             }
 #endif
@@ -609,9 +657,90 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
             }
         }
     };
-    // only the warp that writes the new token needs loads that see it
-    if (own_new) walk(std::true_type{});
-    else walk(std::false_type{});
+    // fp8 pool: the warp's 16-token tiles one after another, each tile's raw
+    // codes (K: 8-byte pieces, V^T: 4-byte pieces, 32 registers) loaded one
+    // tile ahead of the tile being widened and computed, so that every warp
+    // keeps two tiles' loads in flight (at one byte per element a tile is half
+    // the bytes of a bf16 tile, and one tile in flight per warp left HBM idle).
+    auto walk_f8 = [&]() {
+        const unsigned char* kb = static_cast<const unsigned char*>(p.k);
+        const unsigned char* vb = static_cast<const unsigned char*>(p.v);
+        const int nunits = nblk * nsub;
+        int my_phys = -1;
+        uint2 rk0[NJ], rk1[NJ];
+        uint32_t rv0[NT], rv1[NT];
+        int r_valid = 0;                          // tokens of the loaded tile (0: none)
+        auto load = [&](int u) {
+            const int i = u / nsub, sub = u - i * nsub;
+            if (sub == 0 && (i & 31) == 0) {
+                const int mine = lb0 + warp + kWarps * (i + lane);
+                my_phys = mine < lb1 ? __ldg(table + mine) : -1;
+            }
+            const int phys = __shfl_sync(0xffffffffu, my_phys, i & 31);
+#if PA_BLOCK_PREFETCH > 0
+            if (sub == 0 && i + PA_BLOCK_PREFETCH < nblk && (i & 31) + PA_BLOCK_PREFETCH < 32) {
+                const int pphys = __shfl_sync(0xffffffffu, my_phys, (i + PA_BLOCK_PREFETCH) & 31);
+                if (lane == 0 && pphys >= 0 && pphys < p.num_blocks) {
+                    const size_t ptile = (static_cast<size_t>(pphys) * p.Hkv + h) * tile_elems;
+                    pa_dev::prefetch_l2(kb + ptile, static_cast<uint32_t>(tile_elems));
+                    pa_dev::prefetch_l2(vb + ptile, static_cast<uint32_t>(tile_elems));
+                }
+            }
+#endif
+            const int lb = lb0 + warp + kWarps * i;
+            const int nv = min(16, L - (lb * B + sub * 16));
+            r_valid = 0;
+            if (phys < 0 || phys >= p.num_blocks) {
+                if (lane == 0 && sub == 0) record_error(p.err, PA_ERR_BAD_BLOCK_ID);
+                return;
+            }
+            if (nv <= 0) return;
+            const size_t tile = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems;
+            const unsigned char* kt = kb + tile + static_cast<size_t>(sub) * 16 * D;
+            const unsigned char* vt = vb + tile + sub * 16 + 4 * c;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                rk0[j] = pa_dev::ld_stream8(kt + r0 * D + (4 * j + c) * 8);
+                rk1[j] = pa_dev::ld_stream8(kt + r1 * D + (4 * j + c) * 8);
+            }
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                rv0[t] = pa_dev::ld_stream4(vt + static_cast<size_t>(16 * t + g) * B);
+                rv1[t] = pa_dev::ld_stream4(vt + static_cast<size_t>(16 * t + g + 8) * B);
+            }
+            r_valid = nv;
+        };
+        // head_dim 256 has no registers to spare for a second tile: no lookahead
+        constexpr bool kAhead = D <= 128;
+        if (kAhead && nunits > 0) load(0);
+        for (int u = 0; u < nunits; ++u) {
+            if constexpr (!kAhead) load(u);
+            uint2 ck0[NJ], ck1[NJ];
+            uint32_t cv0[NT], cv1[NT];
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) { ck0[j] = rk0[j]; ck1[j] = rk1[j]; }
+#pragma unroll
+            for (int t = 0; t < NT; ++t) { cv0[t] = rv0[t]; cv1[t] = rv1[t]; }
+            const int nvalid = r_valid;
+            if (kAhead && u + 1 < nunits) load(u + 1);
+            if (nvalid > 0) {
+                uint4 k0[NJ], k1[NJ];
+                uint2 v0[NT], v1[NT];
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) { k0[j] = widen8(ck0[j]); k1[j] = widen8(ck1[j]); }
+#pragma unroll
+                for (int t = 0; t < NT; ++t) { v0[t] = widen4(cv0[t]); v1[t] = widen4(cv1[t]); }
+                tile_update<D, true>(a, k0, k1, v0, v1, nvalid, sl, r0, r1, c);
+            }
+        }
+    };
+    if constexpr (F8) {
+        walk_f8();
+    } else {
+        // only the warp that writes the new token needs loads that see it
+        if (own_new) walk(std::true_type{});
+        else walk(std::false_type{});
+    }
 #endif
     float l0 = a.l0, l1 = a.l1;
 #pragma unroll
@@ -881,7 +1010,7 @@ __device__ __forceinline__ size_t warp_ring_offset(int D) {
     return static_cast<size_t>(threadIdx.x >> 5) * PA_STAGES * 64 * D;
 }
 
-template <int D, bool SHARED, bool FUSE>
+template <int D, bool SHARED, bool FUSE, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, SHARED ? 2 : PA_MIN_CTAS)
 decode_fast_kernel(const DecodeParams p) {
     constexpr int OS = D + 4;
@@ -917,7 +1046,7 @@ decode_fast_kernel(const DecodeParams p) {
         const int PTq = sc.pt(s);
         const int nP = max(1, (max(0, L - start) + PTq - 1) / PTq);
         const int tok0 = start + part * PTq, tok1 = min(L, tok0 + PTq);
-        fast_item<D, FUSE>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
+        fast_item<D, FUSE, F8>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
         __syncthreads();
         // merge the warps' softmax states (in place into warp 0's buffer)
         for (int idx = threadIdx.x; idx < p.G * D; idx += kThreads) {
@@ -954,6 +1083,10 @@ decode_fast_kernel(const DecodeParams p) {
 template <typename E>
 __device__ __forceinline__ float load_elem(const E* base, size_t i);
 template <>
+__device__ __forceinline__ float load_elem<uint8_t>(const uint8_t* base, size_t i) {   // e4m3 code
+    return pa_dev::f16_lo(pa_dev::e4m3x2_to_f16x2(__ldg(base + i)));
+}
+template <>
 __device__ __forceinline__ float load_elem<float>(const float* base, size_t i) {
     return __ldg(base + i);
 }
@@ -963,8 +1096,10 @@ __device__ __forceinline__ float load_elem<uint16_t>(const uint16_t* base, size_
 }
 
 // Items of at most pt_fixed tokens.  Shared memory: q [G][D], scores/probs
-// [G][PT], result [G][D+4].
-template <typename E>
+// [G][PT], result [G][D+4].  QE: query element type; E: pool element type
+// (an fp8 pool's codes are read as their e4m3 values; its scales are folded
+// into scale_log2 and v_scale).
+template <typename QE, typename E>
 __global__ void __launch_bounds__(kThreads) decode_simple_kernel(const DecodeParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int PTm = p.pt_fixed;
@@ -980,7 +1115,7 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(const DecodePar
     int* s_start = s_flag + 4;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const E* q = static_cast<const E*>(p.q);
+    const QE* q = static_cast<const QE*>(p.q);
     const E* kp = static_cast<const E*>(p.k);
     const E* vp = static_cast<const E*>(p.v);
     pa_dev::wait_prior_grid();
@@ -996,7 +1131,7 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(const DecodePar
         const int tok0 = part * PTq, nt = max(0, min(L, tok0 + PTq) - tok0);
         const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
         for (int i = tid; i < p.G * p.D; i += kThreads)
-            qs[i] = load_elem<E>(q, (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G) * p.D + i);
+            qs[i] = load_elem<QE>(q, (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G) * p.D + i);
         __syncthreads();
         for (int i = tid; i < p.G * nt; i += kThreads) {
             const int n = i / nt, j = i - n * nt;
@@ -1156,13 +1291,19 @@ namespace pa_detail {
 int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) {
     const int Hkv = pool->kv_heads, D = pool->head_dim, B = pool->block_size;
     const int G = Hq / Hkv;
-    const bool fast = pool->dtype == PA_BF16 && (D == 64 || D == 128 || D == 256) &&
-                      B % 16 == 0 && G <= 8;
-    if (!plan->shared && fast && plan_stream(pool, S, Hq, max_blocks, plan)) return PA_OK;
+    const bool fp8 = pool->dtype == PA_FP8E4M3;
+    const bool tc_shape = (D == 64 || D == 128 || D == 256) && B % 16 == 0 && G <= 8;
+    const bool fast = tc_shape && (pool->dtype == PA_BF16 || (fp8 && PA_STAGES <= 1));
+    if (fp8) {                  // appends quantize in their own kernel; no shared-prefix items
+        plan->fuse = false;
+        plan->shared = plan->tc = false;
+    }
+    if (!plan->shared && fast && !fp8 && plan_stream(pool, S, Hq, max_blocks, plan)) return PA_OK;
     plan->stream = false;
     plan->fast = fast;
     plan->pool = pool;
     plan->bf16 = pool->dtype == PA_BF16;
+    plan->fp8 = fp8;
     plan->threads = kThreads;
     int occ = 0;
     if (fast) {
@@ -1181,6 +1322,12 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
             if (D == 64) occ = occupancy(decode_fast_kernel<64, true, false>, plan->smem);
             else if (D == 128) occ = occupancy(decode_fast_kernel<128, true, false>, plan->smem);
             else occ = occupancy(decode_fast_kernel<256, true, false>, plan->smem);
+        } else if (fp8) {
+#if PA_STAGES <= 1
+            if (D == 64) occ = occupancy(decode_fast_kernel<64, false, false, true>, plan->smem);
+            else if (D == 128) occ = occupancy(decode_fast_kernel<128, false, false, true>, plan->smem);
+            else occ = occupancy(decode_fast_kernel<256, false, false, true>, plan->smem);
+#endif
         } else if (plan->fuse) {
             if (D == 64) occ = occupancy(decode_fast_kernel<64, false, true>, plan->smem);
             else if (D == 128) occ = occupancy(decode_fast_kernel<128, false, true>, plan->smem);
@@ -1195,8 +1342,9 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
         plan->pt_fixed = PT;
         plan->pt_min = PT;
         plan->smem = simple_smem(G, D, PT, S);
-        occ = pool->dtype == PA_BF16 ? occupancy(decode_simple_kernel<uint16_t>, plan->smem)
-                                     : occupancy(decode_simple_kernel<float>, plan->smem);
+        occ = fp8 ? occupancy(decode_simple_kernel<uint16_t, uint8_t>, plan->smem)
+              : pool->dtype == PA_BF16 ? occupancy(decode_simple_kernel<uint16_t, uint16_t>, plan->smem)
+                                       : occupancy(decode_simple_kernel<float, float>, plan->smem);
     }
     if (occ <= 0) return PA_ERR_UNSUPPORTED;
     plan->grid = pool->num_sms * occ;
@@ -1243,6 +1391,14 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
         if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, true, false>, grid, block, plan.smem, st, p);
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, true, false>, grid, block, plan.smem, st, p);
         else e = launch_pdl(decode_fast_kernel<256, true, false>, grid, block, plan.smem, st, p);
+    } else if (plan.fast && plan.fp8) {
+#if PA_STAGES <= 1
+        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, false, true>, grid, block, plan.smem, st, p);
+        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, false, true>, grid, block, plan.smem, st, p);
+        else e = launch_pdl(decode_fast_kernel<256, false, false, true>, grid, block, plan.smem, st, p);
+#else
+        e = cudaErrorNotSupported;
+#endif
     } else if (plan.fast && plan.fuse) {
         if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, true>, grid, block, plan.smem, st, p);
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, true>, grid, block, plan.smem, st, p);
@@ -1251,10 +1407,12 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
         if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, false>, grid, block, plan.smem, st, p);
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, false>, grid, block, plan.smem, st, p);
         else e = launch_pdl(decode_fast_kernel<256, false, false>, grid, block, plan.smem, st, p);
+    } else if (plan.fp8) {
+        e = launch_pdl(decode_simple_kernel<uint16_t, uint8_t>, grid, block, plan.smem, st, p);
     } else if (plan.bf16) {
-        e = launch_pdl(decode_simple_kernel<uint16_t>, grid, block, plan.smem, st, p);
+        e = launch_pdl(decode_simple_kernel<uint16_t, uint16_t>, grid, block, plan.smem, st, p);
     } else {
-        e = launch_pdl(decode_simple_kernel<float>, grid, block, plan.smem, st, p);
+        e = launch_pdl(decode_simple_kernel<float, float>, grid, block, plan.smem, st, p);
     }
     count_launch();
     if (e != cudaSuccess) return PA_ERR_CUDA;

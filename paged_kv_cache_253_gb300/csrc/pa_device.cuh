@@ -1,10 +1,11 @@
 // Small device helpers shared by the kernels: error recording, streaming
-// loads, bf16 tensor-core instructions (inline PTX).
+// loads, bf16/f16 tensor-core instructions and e4m3 conversions (inline PTX).
 #pragma once
 
 #include <cstdint>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "pa.h"
 
@@ -27,6 +28,12 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 __device__ __forceinline__ uint2 ld_stream8(const void* p) {
     uint2 r;
     asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream4(const void* p) {
+    uint32_t r;
+    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
     return r;
 }
 
@@ -72,6 +79,34 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The same with f16 inputs (the fp8 pool's widened codes and f16 queries).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two e4m3 codes (low byte = first element) widened to an f16 pair; exact,
+// since every e4m3 value is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    uint32_t y;
+    const uint16_t x = static_cast<uint16_t>(two_codes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(y) : "h"(x));
+    return y;
+}
+
+// Two fp32 values rounded to e4m3 codes (nearest, ties to even; magnitudes
+// beyond 448, infinities included, give +-448; NaN gives a NaN code), packed
+// with `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+    uint16_t y;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(y) : "f"(hi), "f"(lo));
+    return y;
+}
+
 // Transpose an 8x8 matrix of 16-bit elements held one row-pair per lane.
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
@@ -89,6 +124,17 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float f16_lo(uint32_t x) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(x & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t x) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(x >> 16)));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) {

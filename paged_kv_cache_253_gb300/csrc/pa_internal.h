@@ -16,6 +16,7 @@ struct pa_pool {
     int device = 0;
     int num_blocks = 0, block_size = 0, kv_heads = 0, head_dim = 0;
     pa_dtype dtype = PA_BF16;
+    float k_scale = 1.f, v_scale = 1.f;   // fp8 pools: a code stands for e4m3(code) * scale
     void* k = nullptr;          // K [num_blocks][kv_heads][block_size][head_dim]
     void* v = nullptr;          // V [num_blocks][kv_heads][head_dim][block_size]
     int* err = nullptr;         // device error word (first recorded PA_ERR_*)
@@ -50,7 +51,8 @@ struct DecodeParams {
     int* sched;                 // [S + 3] PT, item count, first item of each sequence
     int* unit_cnt;              // [S * Hkv] pieces of each unit finished (stream-K), zero between launches
     int* err;
-    float scale_log2;           // scale * log2(e)
+    float scale_log2;           // scale * log2(e) (* k_scale for an fp8 pool)
+    float v_scale;              // factor on the value sums (fp8 pool's v_scale, else 1)
     int S, Hq, Hkv, G, D, B, num_blocks, max_blocks;
     int out_bf16;
     int items_target;           // wanted number of work items (fast path)
@@ -86,6 +88,18 @@ struct DecodeParams {
     int sk_stages;
     int sk_stage_bytes;
 };
+
+// Bytes of one K or V element of the pool.
+inline size_t pool_elem_size(pa_dtype t) { return t == PA_FP8E4M3 ? 1 : t == PA_BF16 ? 2 : 4; }
+
+// Score factor of a decode in log2 units (an fp8 pool's k_scale folded in)
+// and the factor on the value sums.
+inline void decode_scales(const pa_pool* pool, float scale, DecodeParams* p) {
+    const bool f8 = pool->dtype == PA_FP8E4M3;
+    p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 *
+                                       (f8 ? static_cast<double>(pool->k_scale) : 1.0));
+    p->v_scale = f8 ? pool->v_scale : 1.f;
+}
 
 // Decode workspace header: ticket[2], 2 spare ints, the published schedule
 // (S + 3 ints used of S + 4), then one arrival counter per (sequence, KV head)
@@ -130,8 +144,9 @@ struct DecodePlan {
     bool stream = false;        // stream-K split pass with TMA-fed per-warp rings
     int sk_stages = 0, sk_stage_bytes = 0;
     pa_pool* pool = nullptr;
-    bool fast;                  // bf16 tensor-core path
+    bool fast;                  // tensor-core path (bf16 pool, or fp8 codes widened to f16)
     bool bf16;                  // pool element type is bf16
+    bool fp8;                   // pool element type is e4m3
     int grid, threads;
     size_t smem;
     int items_target, pt_min, pt_max = 0, pt_fixed;

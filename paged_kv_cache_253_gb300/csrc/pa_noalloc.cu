@@ -117,7 +117,7 @@ extern "C" int pa_decode_noalloc(pa_pool* pool, const void* q, int num_seqs, int
     p.part_acc = reinterpret_cast<float*>(static_cast<char*>(base) + counters);
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(base) + counters + acc);
     p.err = pool->err;
-    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    decode_scales(pool, scale, &p);
     p.S = num_seqs;
     p.Hq = num_q_heads;
     p.Hkv = Hkv;

@@ -20,7 +20,7 @@ from .api import BlockManager, KVPool
 
 
 def _dtype(wl):
-    return torch.float32 if wl.dtype == "f32" else torch.bfloat16
+    return torch.float32 if wl.input_dtype == "f32" else torch.bfloat16
 
 
 class _Writer:
@@ -74,6 +74,8 @@ def replay_setup(wl, values, device=None):
     """Returns (pool, bm, setup copy pairs) with the pool holding the history."""
     device = torch.device(device) if device is not None else torch.device("cuda")
     pool = KVPool(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim, wl.dtype, device)
+    if wl.dtype == "fp8":
+        pool.set_kv_scales(*wl.kv_scales)
     bm = BlockManager(wl.num_blocks, wl.block_size, wl.free_order)
     hk = values["hist_k"].to(device).contiguous()
     hv = values["hist_v"].to(device).contiguous()
@@ -148,8 +150,9 @@ class DecodeStep:
         return self.out
 
     def launches(self):
-        """Kernels per step: [copy] + [append] + decode split + merge."""
-        fused = self.fused and not self.sharing()
+        """Kernels per step: [copy] + [append] + decode split + merge (an fp8
+        pool's append is always its own launch)."""
+        fused = self.fused and not self.sharing() and not self.pool.fp8
         return (1 if self.num_pairs else 0) + (0 if fused else 1) + 2
 
 

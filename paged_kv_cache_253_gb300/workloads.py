@@ -51,7 +51,7 @@ class Workload:
     num_q_heads: int
     num_kv_heads: int
     head_dim: int
-    dtype: str                      # "f32" or "bf16"
+    dtype: str                      # "f32", "bf16" or "fp8" (e4m3 pool, bf16 inputs)
     num_blocks: int
     free_order: np.ndarray          # int32 permutation of range(num_blocks)
     events: list                    # ("add", rid, tokens, salt) | ("fork", rid, parent)
@@ -62,6 +62,7 @@ class Workload:
     seed: int
     shared_groups: list = field(default_factory=list)  # [rid, ...] lists forked together
     description: str = ""
+    kv_scales: tuple = (1.0, 1.0)   # fp8 pool: (k_scale, v_scale), float32 values
 
     @property
     def num_seqs(self) -> int:
@@ -73,7 +74,13 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
-        return 4 if self.dtype == "f32" else 2
+        """Bytes of one pool element."""
+        return {"f32": 4, "bf16": 2, "fp8": 1}[self.dtype]
+
+    @property
+    def input_dtype(self) -> str:
+        """Element type of q and of the appended keys and values."""
+        return "f32" if self.dtype == "f32" else "bf16"
 
 
 def _tokens(rng, n):
@@ -102,14 +109,33 @@ def _independent(name, rng, lengths, B, hq, hkv, d, dtype, pool_factor, seed, de
                     seed=seed, description=desc)
 
 
+# Scales of an fp8 pool: N(0,1) keys and values then span about +-7 of e4m3's
+# +-448 (no saturation in practice); two unequal values that are not powers
+# of two, so that the division before rounding is not exact and a K/V mix-up
+# shows.
+FP8_KV_SCALES = (0.0173, 0.0141)
+
+
 def make_workload(name: str, seed: int = None, **kw) -> Workload:
     """Build one of the named workloads.
 
     Keyword overrides shrink a workload for parity tests (``num_seqs``,
     ``min_len``/``max_len``, ``prefix_len``, ``suffix_min``/``suffix_max``,
     ``num_prefixes``, ``share_frac``, ``num_q_heads``, ``num_kv_heads``,
-    ``head_dim``, ``block_size``, ``dtype``, ``pool_factor``, ``lengths``).
+    ``head_dim``, ``block_size``, ``dtype``, ``pool_factor``, ``lengths``,
+    ``kv_scales`` for dtype "fp8").
     """
+    wl = _make(name, seed, **kw)
+    if wl.dtype == "fp8":
+        ks, vs = kw.get("kv_scales", FP8_KV_SCALES)
+        wl.kv_scales = (float(np.float32(ks)), float(np.float32(vs)))
+        wl.description += ", fp8 e4m3 pool"
+    elif wl.dtype not in ("f32", "bf16"):
+        raise ValueError(f"unknown dtype {wl.dtype!r}")
+    return wl
+
+
+def _make(name, seed, **kw):
     if name not in WORKLOAD_NAMES:
         raise ValueError(f"unknown workload {name!r}")
     if seed is None:
@@ -238,14 +264,15 @@ def generate_values(wl: Workload, device="cpu", seed: int = None):
     new_k/new_v [S,Hkv,D] (the step's appended token per batch entry).
 
     Values are N(0,1) draws in float32 from a torch generator on ``device``,
-    rounded once to the workload dtype; both sides read those same values.
+    rounded once to the workload's input dtype (bf16 for an fp8 pool); both
+    sides read those same values.
     """
     import torch
     if seed is None:
         seed = wl.seed
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
-    dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+    dt = torch.float32 if wl.input_dtype == "f32" else torch.bfloat16
     S, hq, hkv, d = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
     n_hist = wl.num_history_tokens
 

@@ -8,10 +8,16 @@ from paged_kv_cache_253_gb300 import runtime, workloads
 
 BF16_TOL = 5e-3     # max-abs, bf16 K/V/Q with fp32 accumulation
 F32_TOL = 1e-5      # max-abs, fp32 pool
+# fp8 pool, against attention over the codes' exact values: the codes widen
+# exactly to f16, bf16 queries to f16 exactly (|q| >= 2^-17), the
+# probabilities enter as an f16 pair (hi + remainder, ~22 bits) and every sum
+# is fp32 — so fp32 rounding, not the 8-bit storage, sets the error; values
+# reach |v_scale * 448| ~ 6.3, hence a bound a few times F32_TOL.
+FP8_TOL = 5e-5
 
 
 def tol(wl):
-    return F32_TOL if wl.dtype == "f32" else BF16_TOL
+    return {"f32": F32_TOL, "fp8": FP8_TOL}.get(wl.dtype, BF16_TOL)
 
 
 def bits(t):

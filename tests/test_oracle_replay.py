@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 
 from oracle import attention as oa
+from oracle import fp8
 from oracle import replay as orp
 from paged_kv_cache_253_gb300 import workloads as wls
 
@@ -61,6 +62,40 @@ def test_replay_equals_contiguous(name, kw):
     contig = oa.contiguous_decode(q, ks, vs, wl.scale, wl.num_kv_heads)
     np.testing.assert_array_equal(paged, contig)
     assert st.context_lens.tolist() == [k.shape[0] for k in ks]
+
+
+FP8_CASES = [
+    ("decode", dict(num_seqs=5, min_len=1, max_len=70, num_q_heads=8, num_kv_heads=2,
+                    head_dim=16, dtype="fp8")),
+    ("mixed", dict(num_seqs=20, median=30, min_len=1, max_len=90, prefix_min=20,
+                   prefix_max=50, num_q_heads=8, num_kv_heads=2, head_dim=16, dtype="fp8")),
+]
+
+
+@pytest.mark.parametrize("name,kw", FP8_CASES, ids=[c[0] for c in FP8_CASES])
+def test_fp8_replay_equals_contiguous_over_quantized_rows(name, kw):
+    """An fp8 pool holds each appended row's codes under its own scale (K and V
+    differ), and the paged attention reads their values: equal to contiguous
+    attention over the same rows quantized one by one, here."""
+    wl = wls.make_workload(name, **kw)
+    assert wl.kv_scales[0] != wl.kv_scales[1]
+    values = wls.generate_values(wl, "cpu")
+    st = orp.replay(wl, values)
+    assert st.k_pool.dtype == np.uint8
+    paged = orp.attention(wl, values, st)
+    ks, vs = _histories(wl, values)
+    ks = [fp8.dequantize(fp8.quantize(oa.bf16_bits_to_f32(k), wl.kv_scales[0]), wl.kv_scales[0])
+          for k in ks]
+    vs = [fp8.dequantize(fp8.quantize(oa.bf16_bits_to_f32(v), wl.kv_scales[1]), wl.kv_scales[1])
+          for v in vs]
+    q = oa.bf16_bits_to_f32(orp.values_to_numpy(values["q"]))
+    contig = oa.contiguous_decode(q, ks, vs, wl.scale, wl.num_kv_heads)
+    np.testing.assert_array_equal(paged, contig)
+    # the same step over the unquantized bf16 rows differs by quantization error only
+    wl16 = wls.make_workload(name, **{**kw, "dtype": "bf16"})
+    ref16 = orp.attention(wl16, values, orp.replay(wl16, values))
+    err = np.abs(paged - ref16).max()
+    assert 1e-4 < err < 0.1, err
 
 
 def test_tiny_workload_shape():
