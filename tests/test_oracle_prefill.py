@@ -1,0 +1,124 @@
+"""Pins for the paged prefill oracle (CPU only).
+
+The prefill of a whole sequence is causal self-attention, so torch's
+scaled_dot_product_attention in float64 with is_causal (grouped heads
+expanded) is an independent reference; a chunk must give the same rows as the
+whole-sequence prefill (its queries see the cached prefix and the chunk up to
+themselves); a fresh sequence's first query returns its own value; a key or
+value after a query's position never changes that query's output."""
+import numpy as np
+import pytest
+
+from oracle import attention as oatt
+from oracle import prefill as opf
+
+
+def _pool(rng, lengths, B, hkv, D, extra=3):
+    """Random float32 pool, one scattered table per sequence; also the
+    contiguous keys/values of each sequence."""
+    nb = sum(-(-L // B) for L in lengths) + extra
+    k = rng.standard_normal((nb, hkv, B, D)).astype(np.float32)
+    v = rng.standard_normal((nb, hkv, B, D)).astype(np.float32)
+    order = rng.permutation(nb)
+    width = max(1, max(-(-L // B) for L in lengths))
+    tables = np.full((len(lengths), width), -1, dtype=np.int32)
+    kseq, vseq, o = [], [], 0
+    for s, L in enumerate(lengths):
+        nbk = -(-L // B)
+        tables[s, :nbk] = order[o:o + nbk]
+        o += nbk
+        blocks = tables[s, :nbk]
+        kseq.append(k[blocks].transpose(0, 2, 1, 3).reshape(-1, hkv, D)[:L])
+        vseq.append(v[blocks].transpose(0, 2, 1, 3).reshape(-1, hkv, D)[:L])
+    return k, v, tables, kseq, vseq
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (6, 2)])
+def test_whole_sequence_prefill_matches_sdpa_causal(hq, hkv):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(hq * 10 + hkv)
+    B, D = 4, 16
+    lengths = [1, 7, 13]
+    k, v, tables, kseq, vseq = _pool(rng, lengths, B, hkv, D)
+    T = sum(lengths)
+    q = rng.standard_normal((T, hq, D))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    scale = 0.37
+    out = opf.paged_prefill(q, k, v, tables, cu, np.asarray(lengths, np.int32), scale, hkv)
+    G = hq // hkv
+    for s, L in enumerate(lengths):
+        qs = torch.from_numpy(q[cu[s]:cu[s + 1]]).permute(1, 0, 2)            # [hq, L, D]
+        ks = torch.from_numpy(kseq[s].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+        vs = torch.from_numpy(vseq[s].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qs, ks, vs, is_causal=True,
+                                                               scale=scale)
+        np.testing.assert_allclose(out[cu[s]:cu[s + 1]], ref.permute(1, 0, 2).numpy(),
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_chunks_equal_rows_of_the_whole_prefill():
+    rng = np.random.default_rng(5)
+    B, hq, hkv, D = 4, 4, 2, 8
+    lengths = [11, 20]
+    k, v, tables, _, _ = _pool(rng, lengths, B, hkv, D)
+    L = np.asarray(lengths, np.int32)
+    q_all = rng.standard_normal((sum(lengths), hq, D))
+    cu_all = np.array([0, 11, 31], np.int32)
+    whole = opf.paged_prefill(q_all, k, v, tables, cu_all, L, 0.5, hkv)
+    # chunks: the last 4 tokens of sequence 0, the last 9 of sequence 1
+    n = [4, 9]
+    rows = np.concatenate([np.arange(11 - 4, 11), 11 + np.arange(20 - 9, 20)])
+    cu = np.array([0, 4, 13], np.int32)
+    chunk = opf.paged_prefill(q_all[rows], k, v, tables, cu, L, 0.5, hkv)
+    np.testing.assert_array_equal(chunk, whole[rows])
+    seq, pos = opf.query_positions(cu, L)
+    assert seq.tolist() == [0] * 4 + [1] * 9
+    assert pos.tolist() == list(range(7, 11)) + list(range(11, 20))
+    assert n == np.diff(cu).tolist()
+
+
+def test_first_query_returns_its_own_value_and_one_token_chunk_is_decode():
+    rng = np.random.default_rng(6)
+    B, hq, hkv, D = 4, 4, 2, 8
+    lengths = [9, 5]
+    k, v, tables, kseq, vseq = _pool(rng, lengths, B, hkv, D)
+    q = rng.standard_normal((sum(lengths), hq, D))
+    cu = np.array([0, 9, 14], np.int32)
+    out = opf.paged_prefill(q, k, v, tables, cu, np.asarray(lengths, np.int32), 1.0, hkv)
+    G = hq // hkv
+    for s in range(2):
+        first = out[cu[s]]
+        for h in range(hq):
+            np.testing.assert_array_equal(first[h], vseq[s][0, h // G].astype(np.float64))
+    # a one-token chunk at the end of each context is the decode of that context
+    qd = rng.standard_normal((2, hq, D))
+    one = opf.paged_prefill(qd, k, v, tables, np.array([0, 1, 2], np.int32),
+                            np.asarray(lengths, np.int32), 0.8, hkv)
+    dec = oatt.paged_decode(qd, k, v, tables, np.asarray(lengths, np.int32), 0.8, hkv)
+    np.testing.assert_array_equal(one, dec)
+
+
+def test_later_keys_do_not_reach_earlier_queries():
+    rng = np.random.default_rng(7)
+    B, hq, hkv, D = 4, 2, 1, 8
+    lengths = [10]
+    k, v, tables, _, _ = _pool(rng, lengths, B, hkv, D, extra=0)
+    q = rng.standard_normal((6, hq, D))
+    cu = np.array([0, 6], np.int32)                    # positions 4 .. 9
+    L = np.asarray(lengths, np.int32)
+    before = opf.paged_prefill(q, k, v, tables, cu, L, 1.0, hkv)
+    # change the key and value at position 7 (block tables[0][1], offset 3)
+    k2, v2 = k.copy(), v.copy()
+    b = tables[0][7 // B]
+    k2[b, :, 7 % B] += 3.0
+    v2[b, :, 7 % B] -= 5.0
+    after = opf.paged_prefill(q, k2, v2, tables, cu, L, 1.0, hkv)
+    np.testing.assert_array_equal(after[:3], before[:3])          # positions 4, 5, 6
+    assert np.all(np.abs(after[3:] - before[3:]).max(axis=(1, 2)) > 1e-3)   # 7, 8, 9
+
+
+def test_bad_chunks_are_rejected():
+    with pytest.raises(ValueError):
+        opf.query_positions([0, 5], [4])                # chunk longer than the context
+    with pytest.raises(ValueError):
+        opf.query_positions([1, 5], [9])
