@@ -382,18 +382,26 @@ __device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D /
     const float mn0 = fmaxf(a.m0, mx0), mn1 = fmaxf(a.m1, mx1);
     const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
     const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float cr0 = pa_dev::ex2(a.m0 - ms0), cr1 = pa_dev::ex2(a.m1 - ms1);
     const float p0 = pa_dev::ex2(x0 - ms0), p1 = pa_dev::ex2(x1 - ms1);
     const float p2 = pa_dev::ex2(x2 - ms0), p3 = pa_dev::ex2(x3 - ms1);
-    a.l0 = a.l0 * cr0 + (p0 + p2);
-    a.l1 = a.l1 * cr1 + (p1 + p3);
+    // Rescale the running sums only when some head's maximum moved: otherwise
+    // the factor is exactly 1 (an unchanged -inf maximum leaves sums that are
+    // still 0), so skipping it changes no bit; past the first tiles of an item
+    // the maximum rarely moves.
+    if (__any_sync(0xffffffffu, mn0 != a.m0 || mn1 != a.m1)) {
+        const float cr0 = pa_dev::ex2(a.m0 - ms0), cr1 = pa_dev::ex2(a.m1 - ms1);
+        a.l0 *= cr0;
+        a.l1 *= cr1;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            a.o[t][0] *= cr0; a.o[t][1] *= cr1;
+            a.o[t][2] *= cr0; a.o[t][3] *= cr1;
+        }
+    }
+    a.l0 += p0 + p2;
+    a.l1 += p1 + p3;
     a.m0 = mn0;
     a.m1 = mn1;
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        a.o[t][0] *= cr0; a.o[t][1] *= cr1;
-        a.o[t][2] *= cr0; a.o[t][3] *= cr1;
-    }
     uint32_t h01, h23, e01, e23;          // probabilities as a rounded pair plus the remainder
     if constexpr (F8) {
         h01 = pa_dev::pack_f16(p0, p1);
