@@ -41,14 +41,26 @@ METRIC = "paged-decode KV GB/s (% of GB300 HBM peak) and decode tokens/s per ste
 L2_FLUSH_BYTES = 256 << 20
 
 
-def _peaks():
+def _peaks(key="hbm_gbs"):
+    """A measured peak (HBM GB/s, or bf16 dense TFLOP/s as a burst) and its kind."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}[key], "fallback"
+
+
+def _prefill_flops(wl, lens):
+    """Algorithmic FLOPs of one prefill launch: every chunk query row (token,
+    query head) takes 2 D FLOPs per visible key for Q K^T and 2 D for P V; the
+    query at position p sees p + 1 keys."""
+    total = 0
+    for L, n in zip(lens, wl.chunk_lens):
+        L, n = int(L), int(n)
+        total += n * (L - n) + n * (n + 1) // 2          # sum over the chunk of (position + 1)
+    return 4 * wl.head_dim * wl.num_q_heads * total
 
 
 def _dist():
@@ -186,7 +198,10 @@ def _oracle_sample(wl, values, target_s=12.0, threads=None):
             pos = 0
         pick = order[pos:pos + n]
         t0 = time.perf_counter()
-        orp.attention(wl, values, st, seqs=pick, threads=threads)
+        if wl.chunk_lens is not None:
+            orp.prefill_attention(wl, values, st, seqs=pick, threads=threads)
+        else:
+            orp.attention(wl, values, st, seqs=pick, threads=threads)
         dt = time.perf_counter() - t0
         spent += dt
         done_tok += int(lens[pick].sum())
@@ -196,7 +211,8 @@ def _oracle_sample(wl, values, target_s=12.0, threads=None):
         n = max(1, min(len(order), int(n * 2)))
     per_tok = wl.num_kv_heads * wl.head_dim * 2 * wl.elem_bytes
     gbs = done_tok * per_tok / spent / 1e9
-    desc = (f"{done_seq} sequence decodes ({done_tok} cached tokens) drawn from the same "
+    kind = "chunk prefills" if wl.chunk_lens is not None else "decodes"
+    desc = (f"{done_seq} sequence {kind} ({done_tok} cached tokens) drawn from the same "
             f"{wl.num_seqs}-sequence batch, float64 oracle, {threads} threads, {spent:.1f} s")
     return gbs, done_seq / spent, threads, desc
 
@@ -253,7 +269,9 @@ def run_ours(args):
     wl = wls.make_workload(args.workload, **_dtype_kw(args))
     values = wls.generate_values(wl, f"cuda:{local}", seed=wl.seed + 1000 * rank)
     pool, bm, _ = runtime.replay_setup(wl, values, f"cuda:{local}")
-    step = runtime.prepare_step(wl, values, pool, bm)
+    prefill = wl.chunk_lens is not None
+    step = runtime.prepare_prefill(wl, values, pool, bm) if prefill else \
+        runtime.prepare_step(wl, values, pool, bm)
     lens = step.context_lens.cpu().numpy()
     # unique bytes: a shared span counts once per group whichever decode path runs
     all_groups = bm.prefix_groups(wl.batch)
@@ -293,7 +311,10 @@ def run_ours(args):
         return [a.elapsed_time(b) for a, b in evs]
 
     def decode_only():
-        step.decode()
+        if prefill:
+            step.attend()
+        else:
+            step.decode()
 
     if dist:
         dist.barrier()
@@ -317,7 +338,8 @@ def run_ours(args):
     # ---- end to end: host buffers, pinned, through the public API ----
     # The step's inputs live in one pinned host buffer (256-byte-aligned views)
     # and go up in one copy; the result comes back in one copy.
-    names = ("q", "new_k", "new_v", "slots", "pairs", "block_tables", "context_lens")
+    names = ("q", "new_k", "new_v", "slots", "pairs", "block_tables", "context_lens") + \
+        (("cu_seqlens_q",) if prefill else ())
     src = {k: getattr(step, k).cpu() for k in names}
     offs, total = {}, 0
     for k in names:
@@ -359,6 +381,19 @@ def run_ours(args):
 
     peak, peak_kind = _peaks()
     achieved = algo_bytes / (dms * 1e-3) / 1e9
+    if prefill:
+        flops = _prefill_flops(wl, lens)
+        tpeak, tpeak_kind = _peaks("bf16_tflops")
+        tflops = flops / (dms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak,
+                    "peak_kind": tpeak_kind + " bf16 dense burst", "unit": "TFLOP/s",
+                    "frac": round(tflops / tpeak, 4), "traffic": None,
+                    "kernel": "prefill (pa_prefill)", "algorithmic_flops_per_launch": flops}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                    "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "traffic": _traffic_from_profile(wl), "kernel": "decode (pa_decode)",
+                    "algorithmic_bytes_per_launch": algo_bytes}
     value = world * kv_bytes / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -373,13 +408,10 @@ def run_ours(args):
                    "copy_pairs_per_step": step.num_pairs,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_frac_of_" + peak_kind: round(value / world / peak, 4),
-        "tokens_per_s": round(world * wl.num_seqs / (ms * 1e-3), 1),
+        "tokens_per_s": round(world * wl.num_step_tokens / (ms * 1e-3), 1),
         "decode_ms": round(dms, 5),
         "launches_per_step": step.launches(),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": _traffic_from_profile(wl), "kernel": "decode (pa_decode)",
-                     "algorithmic_bytes_per_launch": algo_bytes},
+        "roofline": roofline,
         "e2e": {"value": round(world * kv_bytes / (ems * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(ems, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -405,7 +437,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode",
-                    choices=["tiny", "decode", "prefix", "long", "mixed"])
+                    choices=["tiny", "decode", "prefix", "long", "mixed", "prefill"])
     ap.add_argument("--kv-dtype", default=None, choices=["f32", "bf16", "fp8"],
                     help="pool element type (default: the workload's own; fp8 = e4m3 codes)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

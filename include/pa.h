@@ -258,6 +258,39 @@ int pa_decode_noalloc(pa_pool *pool, const void *q, int num_seqs, int num_q_head
                       const int32_t *context_lens, float scale, void *out,
                       pa_dtype out_dtype, void *stream);
 
+/* Paged prefill attention of one chunk of new tokens per sequence.  The pages
+ * name the prefill step only through what a prefix-cache hit saves ([Z]
+ * answer and [K] "Prefix Sharing Is a Natural Extension": "the prefill for that
+ * span is skipped"); this library's reading: a chunk's keys and values are
+ * appended first (pa_append_kv, the slots of positions L-n .. L-1), then chunk
+ * token i of sequence s, at position L-n+i with L = context_lens[s] and
+ * n = cu_seqlens_q[s+1] - cu_seqlens_q[s], attends to every cached key of s at
+ * positions 0 .. L-n+i (the whole cached prefix, and the chunk causally):
+ *   out[t][h] = sum_j softmax_j(scale * <q[t][h], K_s[j][h/G]>) * V_s[j][h/G]
+ * over j <= its position, K_s / V_s found through block_tables[s] as in
+ * pa_decode.
+ *   q             device bf16 [T][num_q_heads][head_dim], the chunks packed
+ *                 sequence after sequence (T = num_tokens)
+ *   cu_seqlens_q  device int32 [S+1]: sequence s owns query rows
+ *                 cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1; cu_seqlens_q[0] = 0
+ *   max_q_len     host int: no chunk is longer (sizes the launch)
+ *   block_tables  device int32 [S][max_blocks_per_seq]
+ *   context_lens  device int32 [S]: L after the chunk's append, L >= n
+ *   out           device [T][num_q_heads][head_dim] of out_dtype (8-byte aligned)
+ * Requires a bf16 pool (else PA_ERR_DTYPE), block_size % 16 == 0 and
+ * head_dim 64/128/256 (else PA_ERR_UNSUPPORTED).  One kernel launch: one CTA per
+ * (64 query rows, KV head, sequence) streams the keys up to its last row's
+ * position through shared memory once for all its rows (mma.sync tensor
+ * cores).  On the device: a malformed cu_seqlens_q (decreasing, beyond T, a
+ * chunk longer than its context or than max_q_len) records PA_ERR_INVALID_ARG,
+ * a context beyond the table PA_ERR_BAD_LENGTH, a block id outside the pool
+ * PA_ERR_BAD_BLOCK_ID; those sequences' rows are left unwritten. */
+int pa_prefill(pa_pool *pool, const void *q, int num_tokens, int num_q_heads,
+               const int32_t *cu_seqlens_q, int num_seqs, int max_q_len,
+               const int32_t *block_tables, int max_blocks_per_seq,
+               const int32_t *context_lens, float scale, void *out, pa_dtype out_dtype,
+               void *stream);
+
 /* Synchronize `stream`, then return and clear the first error the pool's
  * kernels recorded since the last call (PA_OK if none). */
 int pa_get_error(pa_pool *pool, void *stream);

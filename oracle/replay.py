@@ -21,6 +21,7 @@ from . import fp8
 from .attention import paged_decode
 from .block_manager import NaiveBlockManager
 from .kvcache import append_kv, copy_blocks
+from .prefill import paged_prefill
 
 
 def values_to_numpy(t):
@@ -61,6 +62,7 @@ class OracleState:
         self.step_slots = None
         self.block_tables = None
         self.context_lens = None
+        self.cu_seqlens_q = None       # prefill step: query rows of each batch entry
         self.bm = None
 
 
@@ -114,14 +116,20 @@ def replay(wl, values, *, run_step=True):
         nk = _stored(wl, values["new_k"], 0)
         nv = _stored(wl, values["new_v"], 1)
         slots = []
+        # decode: one token per batch entry; prefill: each entry's chunk, in order
+        per_entry = wl.chunk_lens if wl.chunk_lens is not None else np.ones(wl.num_seqs, np.int64)
+        r = 0
         for i, rid in enumerate(wl.batch.tolist()):
-            slot, src, dst = bm.append_slot(rid, int(wl.step_tokens[i]))
-            if src >= 0:
-                copy_blocks(K, V, [(src, dst)])
-                st.step_pairs.append((src, dst))
-            append_kv(K, V, nk[i:i + 1], nv[i:i + 1], [slot])
-            slots.append(slot)
+            for _ in range(int(per_entry[i])):
+                slot, src, dst = bm.append_slot(rid, int(wl.step_tokens[r]))
+                if src >= 0:
+                    copy_blocks(K, V, [(src, dst)])
+                    st.step_pairs.append((src, dst))
+                append_kv(K, V, nk[r:r + 1], nv[r:r + 1], [slot])
+                slots.append(slot)
+                r += 1
         st.step_slots = np.asarray(slots, dtype=np.int64)
+        st.cu_seqlens_q = np.concatenate([[0], np.cumsum(per_entry)]).astype(np.int32)
 
     S = wl.num_seqs
     tables = [bm.block_table(r) for r in wl.batch.tolist()]
@@ -155,3 +163,21 @@ def attention(wl, values, st, seqs=None, threads=1):
         kp = fp8.dequantize(kp[used], wl.kv_scales[0])
         vp = fp8.dequantize(vp[used], wl.kv_scales[1])
     return paged_decode(q, kp, vp, bt, lens, wl.scale, wl.num_kv_heads, threads=threads)
+
+
+def prefill_attention(wl, values, st, seqs=None, threads=1):
+    """float64 prefill attention of the step's chunk queries, for all batch
+    entries or the listed ones (rows of those entries, entry after entry)."""
+    q = values_to_numpy(values["q"])
+    if q.dtype == np.uint16:
+        q = _bf16_bits_to_f32(q)
+    cu, bt, lens = st.cu_seqlens_q, st.block_tables, st.context_lens
+    if seqs is not None:
+        seqs = np.asarray(seqs, dtype=np.int64)
+        rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs]) if len(seqs) else \
+            np.zeros(0, np.int64)
+        n = cu[seqs + 1] - cu[seqs]
+        q, bt, lens = q[rows], bt[seqs], lens[seqs]
+        cu = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    return paged_prefill(q, st.k_pool, st.v_pool, bt, cu, lens, wl.scale, wl.num_kv_heads,
+                         threads=threads)

@@ -56,6 +56,8 @@ SIGNATURES = {
                                  c_void_p]),
     "pa_decode_noalloc": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_void_p,
                                   c_float, c_void_p, c_int, c_void_p]),
+    "pa_prefill": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_void_p,
+                           c_int, c_void_p, c_float, c_void_p, c_int, c_void_p]),
     "pa_get_error": (c_int, [c_void_p, c_void_p]),
     "pa_error_string": (ctypes.c_char_p, [c_int]),
     "pa_launch_count": (ctypes.c_uint64, []),

@@ -170,6 +170,35 @@ class KVPool:
                 "pa_decode_shared")
         return out
 
+    def prefill(self, q, cu_seqlens_q, block_tables, context_lens, scale, max_q_len=None,
+                out=None, out_dtype=torch.float32):
+        """Chunked prefill: the packed chunk queries q [T, Hq, D] (sequence s owns
+        rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1) attend to the cached prefix
+        and causally to their chunk.  The chunk's keys and values must already
+        be appended.  max_q_len (longest chunk) is read from cu_seqlens_q when
+        not given (one device-to-host copy)."""
+        T, hq, d = q.shape
+        S = int(cu_seqlens_q.shape[0]) - 1
+        if d != self.head_dim or S < 0:
+            raise ValueError("q head_dim / cu_seqlens_q [S+1]")
+        if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+            raise ValueError("block_tables [S, max_blocks] / context_lens [S]")
+        if max_q_len is None:
+            max_q_len = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if S else 0
+        if out is None:
+            out = torch.empty((T, hq, d), dtype=out_dtype, device=self.device)
+        if tuple(out.shape) != (T, hq, d):
+            raise ValueError("out must be [T, Hq, D]")
+        L.check(L.pa_prefill(self.handle, _dev(q, self.dtype, "q", self.device), T, hq,
+                             _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q", self.device), S,
+                             int(max_q_len),
+                             _dev(block_tables, torch.int32, "block_tables", self.device),
+                             int(block_tables.shape[1]),
+                             _dev(context_lens, torch.int32, "context_lens", self.device),
+                             float(scale), _dev(out, out.dtype, "out", self.device),
+                             _CODE[out.dtype], _stream()), "pa_prefill")
+        return out
+
     def reserve(self, max_seqs, max_q_heads):
         L.check(L.pa_decode_reserve(self.handle, int(max_seqs), int(max_q_heads)),
                 "pa_decode_reserve")

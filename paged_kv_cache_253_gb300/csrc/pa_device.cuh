@@ -37,6 +37,19 @@ __device__ __forceinline__ uint32_t ld_stream4(const void* p) {
     return r;
 }
 
+// 16-byte asynchronous global -> shared copies (cp.async, L2 only) and their
+// commit / wait groups.
+__device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream-serialisation attribute may start while the previous kernel in the
 // stream drains.  wait_prior_grid() blocks until that kernel has completed and

@@ -195,3 +195,64 @@ def prepare_step(wl, values, pool, bm, out_dtype=torch.float32, shared="auto", f
         scale=wl.scale,
         out=torch.empty((S, wl.num_q_heads, wl.head_dim), dtype=out_dtype, device=dev),
         groups=groups, fused=fused)
+
+
+@dataclass
+class PrefillStep:
+    """Device inputs of one chunked-prefill step and the calls that run it."""
+    pool: KVPool
+    q: torch.Tensor                # [T, Hq, D]
+    new_k: torch.Tensor            # [T, Hkv, D]
+    new_v: torch.Tensor
+    slots: torch.Tensor            # int64 [T]
+    pairs: torch.Tensor            # int64 [P, 2]
+    cu_seqlens_q: torch.Tensor     # int32 [S + 1]
+    max_q_len: int
+    block_tables: torch.Tensor     # int32 [S, W]
+    context_lens: torch.Tensor     # int32 [S], after the chunk's append
+    scale: float
+    out: torch.Tensor              # [T, Hq, D]
+
+    @property
+    def num_pairs(self):
+        return int(self.pairs.shape[0])
+
+    def sharing(self):
+        return False
+
+    def attend(self):
+        return self.pool.prefill(self.q, self.cu_seqlens_q, self.block_tables, self.context_lens,
+                                 self.scale, max_q_len=self.max_q_len, out=self.out)
+
+    def run(self):
+        if self.num_pairs:
+            self.pool.copy_blocks(self.pairs)
+        self.pool.append_kv(self.new_k, self.new_v, self.slots)
+        self.attend()
+        return self.out
+
+    def launches(self):
+        """Kernels per step: [copy] + append + prefill."""
+        return (1 if self.num_pairs else 0) + 2
+
+
+def prepare_prefill(wl, values, pool, bm, out_dtype=torch.float32):
+    """Reserve the slots of every chunk token (entry after entry, each entry's
+    tokens in order) and upload the step's inputs."""
+    dev = pool.device
+    reqs = np.repeat(np.asarray(wl.batch, dtype=np.int32), wl.chunk_lens)
+    slots, pairs = bm.append_slots(reqs, wl.step_tokens)
+    tables, lens = bm.batch_tables(wl.batch)
+    cu = np.zeros(len(wl.chunk_lens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(wl.chunk_lens)
+    T = int(cu[-1])
+    return PrefillStep(
+        pool=pool, q=values["q"].to(dev).contiguous(),
+        new_k=values["new_k"].to(dev).contiguous(), new_v=values["new_v"].to(dev).contiguous(),
+        slots=torch.as_tensor(slots, device=dev),
+        pairs=torch.as_tensor(pairs.reshape(-1, 2), device=dev),
+        cu_seqlens_q=torch.as_tensor(cu, device=dev),
+        max_q_len=int(np.max(wl.chunk_lens)) if len(wl.chunk_lens) else 0,
+        block_tables=torch.as_tensor(tables, device=dev),
+        context_lens=torch.as_tensor(lens, device=dev), scale=wl.scale,
+        out=torch.empty((T, wl.num_q_heads, wl.head_dim), dtype=out_dtype, device=dev))

@@ -33,6 +33,9 @@ Workloads (sizes from the pages' problem statement for this build):
            [16, 16384]), 64 q / 8 KV heads; 30 % of the requests are forks
            of one of 4 prompts of U[512, 2048] tokens that diverge in the
            timed step
+  prefill  16 sequences with cached prefixes U[0, 4096] and a chunk of
+           U[128, 512] new tokens each (chunked prefill: the step appends the
+           chunk and runs its queries), 32 q / 8 KV heads, head_dim 128, bf16
 """
 from dataclasses import dataclass, field
 import math
@@ -41,7 +44,7 @@ import numpy as np
 
 VOCAB = 32000
 
-WORKLOAD_NAMES = ("tiny", "decode", "prefix", "long", "mixed")
+WORKLOAD_NAMES = ("tiny", "decode", "prefix", "long", "mixed", "prefill")
 
 
 @dataclass
@@ -63,10 +66,18 @@ class Workload:
     shared_groups: list = field(default_factory=list)  # [rid, ...] lists forked together
     description: str = ""
     kv_scales: tuple = (1.0, 1.0)   # fp8 pool: (k_scale, v_scale), float32 values
+    # prefill step: batch entry i appends chunk_lens[i] tokens (step_tokens holds
+    # them all, entry after entry) and runs their queries; None: one decode token
+    chunk_lens: np.ndarray = None
 
     @property
     def num_seqs(self) -> int:
         return int(len(self.batch))
+
+    @property
+    def num_step_tokens(self) -> int:
+        """Tokens the timed step appends (and queries it runs)."""
+        return int(self.chunk_lens.sum()) if self.chunk_lens is not None else self.num_seqs
 
     @property
     def num_history_tokens(self) -> int:
@@ -202,6 +213,34 @@ def _make(name, seed, **kw):
                         shared_groups=[list(range(S))],
                         description=f"{S} requests forked from a {plen}-token prompt")
 
+    if name == "prefill":
+        S = kw.get("num_seqs", 16)
+        hq, hkv = kw.get("num_q_heads", 32), kw.get("num_kv_heads", 8)
+        plo, phi = kw.get("min_len", 0), kw.get("max_len", 4096)
+        clo, chi = kw.get("chunk_min", 128), kw.get("chunk_max", 512)
+        prefix = kw.get("lengths")
+        if prefix is None:
+            prefix = rng.integers(plo, phi + 1, size=S).tolist()
+        chunks = kw.get("chunks")
+        if chunks is None:
+            chunks = rng.integers(clo, chi + 1, size=len(prefix)).tolist()
+        events = []
+        for rid, L in enumerate(prefix):
+            toks = _tokens(rng, L)
+            events.append(("add", rid, toks, 0))
+            events.append(("extend", rid, toks))
+        chunk_lens = np.asarray(chunks, dtype=np.int32)
+        need = sum(_blocks_for(int(L) + int(c), B) for L, c in zip(prefix, chunks))
+        nb = int(math.ceil(need * kw.get("pool_factor", 1.1))) + 1
+        return Workload(name=name, block_size=B, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                        dtype=dtype, num_blocks=nb,
+                        free_order=rng.permutation(nb).astype(np.int32), events=events,
+                        batch=np.arange(len(prefix), dtype=np.int32),
+                        step_tokens=_tokens(rng, int(chunk_lens.sum())),
+                        scale=1.0 / math.sqrt(d), seed=seed, chunk_lens=chunk_lens,
+                        description=f"{len(prefix)} sequences, cached prefixes U[{plo},{phi}], "
+                                    f"chunks U[{clo},{chi}]")
+
     # mixed
     S = kw.get("num_seqs", 512)
     hq, hkv = kw.get("num_q_heads", 64), kw.get("num_kv_heads", 8)
@@ -259,9 +298,11 @@ def _make(name, seed, **kw):
 
 
 def generate_values(wl: Workload, device="cpu", seed: int = None):
-    """Seeded float inputs: q [S,Hq,D], hist_k/hist_v [N_hist,Hkv,D] (the keys and
+    """Seeded float inputs: q [T,Hq,D], hist_k/hist_v [N_hist,Hkv,D] (the keys and
     values of every token the setup script appends, in script order) and
-    new_k/new_v [S,Hkv,D] (the step's appended token per batch entry).
+    new_k/new_v [T,Hkv,D] (the tokens the step appends: one per batch entry for
+    a decode step, T = S; each entry's chunk, entry after entry, for a prefill
+    step, T = sum of chunk_lens).
 
     Values are N(0,1) draws in float32 from a torch generator on ``device``,
     rounded once to the workload's input dtype (bf16 for an fp8 pool); both
@@ -279,5 +320,6 @@ def generate_values(wl: Workload, device="cpu", seed: int = None):
     def draw(*shape):
         return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(dt)
 
-    return dict(q=draw(S, hq, d), hist_k=draw(n_hist, hkv, d), hist_v=draw(n_hist, hkv, d),
-                new_k=draw(S, hkv, d), new_v=draw(S, hkv, d))
+    T = wl.num_step_tokens          # one query / new token per decode entry, a chunk per prefill entry
+    return dict(q=draw(T, hq, d), hist_k=draw(n_hist, hkv, d), hist_v=draw(n_hist, hkv, d),
+                new_k=draw(T, hkv, d), new_v=draw(T, hkv, d))

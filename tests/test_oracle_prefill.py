@@ -122,3 +122,39 @@ def test_bad_chunks_are_rejected():
         opf.query_positions([0, 5], [4])                # chunk longer than the context
     with pytest.raises(ValueError):
         opf.query_positions([1, 5], [9])
+
+
+def test_prefill_workload_replay_equals_contiguous_causal():
+    """The prefill workload's replay (cached prefix, then each entry's chunk
+    appended in order) gives each chunk query causal attention over its own
+    request's tokens, here checked against SDPA on the request's history."""
+    torch = pytest.importorskip("torch")
+    from oracle import replay as orp
+    from paged_kv_cache_253_gb300 import workloads as wls
+    wl = wls.make_workload("prefill", num_seqs=3, lengths=[0, 5, 17], chunks=[6, 1, 9],
+                           num_q_heads=4, num_kv_heads=2, head_dim=16, block_size=4)
+    values = wls.generate_values(wl, "cpu")
+    st = orp.replay(wl, values)
+    assert st.cu_seqlens_q.tolist() == [0, 6, 7, 16]
+    assert st.context_lens.tolist() == [6, 6, 26]
+    out = orp.prefill_attention(wl, values, st)
+    hk = oatt.bf16_bits_to_f32(orp.values_to_numpy(values["hist_k"]))
+    hv = oatt.bf16_bits_to_f32(orp.values_to_numpy(values["hist_v"]))
+    nk = oatt.bf16_bits_to_f32(orp.values_to_numpy(values["new_k"]))
+    nv = oatt.bf16_bits_to_f32(orp.values_to_numpy(values["new_v"]))
+    q = oatt.bf16_bits_to_f32(orp.values_to_numpy(values["q"]))
+    hist = [0, 0, 5]
+    for s, (P, n) in enumerate(zip([0, 5, 17], [6, 1, 9])):
+        ks = np.concatenate([hk[hist[s]:hist[s] + P], nk[st.cu_seqlens_q[s]:st.cu_seqlens_q[s + 1]]])
+        vs = np.concatenate([hv[hist[s]:hist[s] + P], nv[st.cu_seqlens_q[s]:st.cu_seqlens_q[s + 1]]])
+        qs = q[st.cu_seqlens_q[s]:st.cu_seqlens_q[s + 1]]
+        # causal attention of the chunk rows, as the last n rows of a full square mask
+        L = P + n
+        mask = np.tril(np.ones((L, L), dtype=bool))[P:]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(qs.astype(np.float64)).permute(1, 0, 2),
+            torch.from_numpy(ks.astype(np.float64)).permute(1, 0, 2).repeat_interleave(2, 0),
+            torch.from_numpy(vs.astype(np.float64)).permute(1, 0, 2).repeat_interleave(2, 0),
+            attn_mask=torch.from_numpy(mask), scale=wl.scale)
+        np.testing.assert_allclose(out[st.cu_seqlens_q[s]:st.cu_seqlens_q[s + 1]],
+                                   ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-12)
