@@ -279,9 +279,14 @@ int pa_decode_noalloc(pa_pool *pool, const void *q, int num_seqs, int num_q_head
  *   out           device [T][num_q_heads][head_dim] of out_dtype (8-byte aligned)
  * Requires a bf16 pool (else PA_ERR_DTYPE), block_size % 16 == 0 and
  * head_dim 64/128/256 (else PA_ERR_UNSUPPORTED).  One kernel launch: one CTA per
- * (64 query rows, KV head, sequence) streams the keys up to its last row's
- * position through shared memory once for all its rows (mma.sync tensor
- * cores).  On the device: a malformed cu_seqlens_q (decreasing, beyond T, a
+ * (query rows, KV head, sequence) streams the keys up to its last row's
+ * position through shared memory once for all its rows: 128 rows on the
+ * tcgen05 tensor cores (TMA-staged keys/values, TMEM accumulators) for 16-token
+ * blocks, head_dim 128 and a 16-byte-aligned out; 64 rows on mma.sync otherwise
+ * (or when the environment sets PA_PREFILL_MMA_SYNC=1).  Positions past a
+ * sequence's length in its last block must hold finite values (they do in any
+ * pool written through this library with finite inputs): the tcgen05 form
+ * multiplies them by zero probabilities.  On the device: a malformed cu_seqlens_q (decreasing, beyond T, a
  * chunk longer than its context or than max_q_len) records PA_ERR_INVALID_ARG,
  * a context beyond the table PA_ERR_BAD_LENGTH, a block id outside the pool
  * PA_ERR_BAD_BLOCK_ID; those sequences' rows are left unwritten. */

@@ -89,6 +89,22 @@ struct DecodeParams {
     int sk_stage_bytes;
 };
 
+// Everything one prefill launch needs (pa_prefill), passed by value.
+struct PrefillParams {
+    const uint16_t* q;          // [T][Hq][D] bf16
+    const uint16_t* k;          // pool K
+    const uint16_t* v;          // pool V^T tiles
+    const int32_t* cu_q;        // [S + 1] first query row of each sequence
+    const int32_t* tables;      // [S][max_blocks]
+    const int32_t* lens;        // [S] context length after the chunk's append
+    void* out;                  // [T][Hq][D]
+    int* err;
+    float scale_log2;
+    int T, S, Hq, Hkv, G, B, num_blocks, max_blocks;
+    int max_q;                  // longest chunk the launch was sized for
+    int out_bf16;
+};
+
 // Bytes of one K or V element of the pool.
 inline size_t pool_elem_size(pa_dtype t) { return t == PA_FP8E4M3 ? 1 : t == PA_BF16 ? 2 : 4; }
 
@@ -169,5 +185,11 @@ bool shared_tc_eligible(const pa_pool* pool, int G);
 int shared_tc_rows();
 int shared_tc_chunk_tokens();     // shared tokens per item (a multiple of 16)
 int launch_shared_tc(pa_pool* pool, const DecodeParams& p, cudaStream_t st);
+
+// tcgen05 prefill (pa_shared_tc.cu): one CTA per (128 query rows, KV head,
+// sequence); bf16 pools of 16-token blocks, head_dim 128.
+bool prefill_tc_eligible(const pa_pool* pool);
+int prefill_tc_rows();
+int launch_prefill_tc(pa_pool* pool, const PrefillParams& p, dim3 grid, cudaStream_t st);
 
 }  // namespace pa_detail

@@ -17,6 +17,7 @@
 // causal and length masks, online softmax per row, O += P V with P as a bf16
 // high + low pair.  Each row's normalised output is written directly.
 #include <cstdint>
+#include <cstdlib>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -33,21 +34,6 @@ constexpr int kRowsP = kWarpsP * 16;      // query rows per CTA
 constexpr int kStagesP = 8;               // staged 16-token units
 constexpr int kPerSyncP = 4;              // units consumed per barrier (even: 32-token steps)
 static_assert(kStagesP > kPerSyncP && kPerSyncP % 2 == 0, "prefill pipeline shape");
-
-struct PrefillParams {
-    const uint16_t* q;          // [T][Hq][D] bf16
-    const uint16_t* k;          // pool K
-    const uint16_t* v;          // pool V^T tiles
-    const int32_t* cu_q;        // [S + 1] first query row of each sequence
-    const int32_t* tables;      // [S][max_blocks]
-    const int32_t* lens;        // [S] context length after the chunk's append
-    void* out;                  // [T][Hq][D]
-    int* err;
-    float scale_log2;
-    int T, S, Hq, Hkv, G, B, num_blocks, max_blocks;
-    int max_q;                  // longest chunk the launch was sized for
-    int out_bf16;
-};
 
 template <int D>
 __global__ void __launch_bounds__(kThreadsP, 2) prefill_kernel(const PrefillParams p) {
@@ -343,9 +329,20 @@ extern "C" int pa_prefill(pa_pool* pool, const void* q, int num_tokens, int num_
     p.max_blocks = max_blocks_per_seq;
     p.max_q = max_q_len;
     p.out_bf16 = out_dtype == PA_BF16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // tcgen05 form (128 rows per CTA, TMA-staged K/V^T) where the pool's TMA
+    // views apply; PA_PREFILL_MMA_SYNC=1 in the environment selects the
+    // mma.sync form instead (for comparison)
+    const char* force_sync = std::getenv("PA_PREFILL_MMA_SYNC");
+    if (pa_detail::prefill_tc_eligible(pool) && reinterpret_cast<uintptr_t>(out) % 16 == 0 &&
+        !(force_sync && force_sync[0] == '1')) {
+        const int rows = pa_detail::prefill_tc_rows();
+        const dim3 tgrid(static_cast<unsigned>((static_cast<int64_t>(max_q_len) * G + rows - 1) / rows),
+                         static_cast<unsigned>(Hkv), static_cast<unsigned>(num_seqs));
+        return pa_detail::launch_prefill_tc(pool, p, tgrid, st);
+    }
     const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(Hkv),
                     static_cast<unsigned>(num_seqs));
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (D == 64) return launch_prefill_d<64>(p, grid, st);
     if (D == 128) return launch_prefill_d<128>(p, grid, st);
     return launch_prefill_d<256>(p, grid, st);

@@ -98,10 +98,7 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     bool ok = true;
 
     const int G = p.G, B = p.B, Hkv = p.Hkv;
-    const uint16_t* kpool = static_cast<const uint16_t*>(p.k);
-    const uint16_t* vpool = static_cast<const uint16_t*>(p.v);
     const uint16_t* qg = static_cast<const uint16_t*>(p.q);
-    const size_t tile_elems = static_cast<size_t>(B) * kD;
     const float sl = p.scale_log2;
 
     for (int item = blockIdx.x; ok && item < p.n_shared_items; item += gridDim.x) {
@@ -332,9 +329,307 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     if (warp == 0) pa_tc::tmem_free<kTmemCols>(tmem);
 }
 
+// ------------------------------------------------------------ prefill ---
+//
+// Chunked prefill on the same machinery: one CTA per (128 query rows, KV
+// head, sequence), a row being one (chunk token, query head of the group)
+// pair, so a tile holds 128/G chunk tokens.  The tile's keys [0, last row's
+// position] stream through the two TMA stages in 64-token steps exactly as a
+// shared span does (S in TMEM, per-row softmax by the thread owning the TMEM
+// lane, P as bf16 high + low in TMEM, O += P.V in TMEM); the causal mask is
+// applied to the scores (a row at position p keeps keys 0 .. p), and each row's
+// normalised output is written directly.  Block ids come from the sequence's
+// table as each step is staged.
+__global__ void __launch_bounds__(kThreads, 2)
+prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap) {
+    extern __shared__ unsigned char tc_raw[];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tile = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    const bool reporter = tid == 0 && tile == 0 && h == 0;
+    pa_dev::wait_prior_grid();
+    pa_dev::allow_next_grid();
+
+    // the item (uniform over the CTA: every early return happens before any
+    // barrier, mbarrier or TMEM is touched)
+    const int q0 = __ldg(p.cu_q + s), q1 = __ldg(p.cu_q + s + 1);
+    const int n = q1 - q0;
+    const int L = __ldg(p.lens + s);
+    if (q0 < 0 || n < 0 || q1 > p.T || L < n || n > p.max_q) {
+        if (reporter) pa_dev::record_error(p.err, PA_ERR_INVALID_ARG);
+        return;
+    }
+    if (L > p.max_blocks * 16) {
+        if (reporter) pa_dev::record_error(p.err, PA_ERR_BAD_LENGTH);
+        return;
+    }
+    const int G = p.G, Hkv = p.Hkv;
+    const int r_lo = tile * kRows;
+    if (r_lo >= n * G) return;
+    const int P0 = L - n;
+    const int rows_end = min(n * G, r_lo + kRows);
+    const int kv_end = P0 + (rows_end - 1) / G + 1;        // keys [0, kv_end) reach some row
+    const int nsteps = (kv_end + kStep - 1) / kStep;
+
+    const uint32_t raw_s = pa_tc::smem_u32(tc_raw);
+    unsigned char* base = tc_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sbase = pa_tc::smem_u32(base);
+    uint64_t* bar_s = reinterpret_cast<uint64_t*>(base + kMiscOff);
+    uint64_t* bar_pv = bar_s + 1;
+    uint64_t* bar_full = bar_s + 2;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kMiscOff + 32);
+    if (tid == 0) {
+        pa_tc::mbar_init(bar_s, 1);
+        pa_tc::mbar_init(bar_pv, 1);
+        pa_tc::mbar_init(bar_full, 1);
+        pa_tc::mbar_init(bar_full + 1, 1);
+        pa_tc::mbar_init_fence();
+    }
+    // zeroed stages: block slots a step leaves unloaded must hold finite values
+    for (uint32_t o = tid * 16; o < 2 * kStageBytes; o += kThreads * 16)
+        *reinterpret_cast<uint4*>(base + kStageOff + o) = make_uint4(0u, 0u, 0u, 0u);
+    pa_tc::fence_smem_to_async();
+    if (warp == 0) pa_tc::tmem_alloc<kTmemCols>(tslot);
+    pa_tc::fence_before_sync();
+    __syncthreads();
+    pa_tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tS = tmem, tO = tmem + 64, tPh = tmem + 192, tPl = tmem + 224;
+    const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t ph_s = 0, ph_pv = 0, ph_full0 = 0, ph_full1 = 0;
+    bool ok = true;
+
+    // this thread's row: TMEM lane tid
+    const int r = r_lo + tid;
+    const int qi = r / G;
+    const bool row_ok = r < rows_end;
+    const int pos = row_ok ? P0 + qi : -1;
+    const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
+    const float sl = p.scale_log2;
+
+    // Q tile: 128 rows x 16 chunks of 16 B, zero rows past the chunk
+    for (int idx = tid; idx < kRows * 16; idx += kThreads) {
+        const int rr = idx >> 4, c16 = idx & 15;
+        const int gr = r_lo + rr;
+        const bool v = gr < rows_end;
+        const uint16_t* src = p.q + (v ? ((static_cast<size_t>(q0 + gr / G) * p.Hq +
+                                           static_cast<size_t>(h) * G + gr % G) * kD + c16 * 8)
+                                       : 0);
+        pa_tc::cp16(sbase + kQOff + (c16 >> 3) * 16384 + pa_tc::sw128_off(rr, c16 & 7), src,
+                    v ? 16u : 0u);
+    }
+    pa_tc::cp_commit();
+
+    // One thread stages step j: its (up to) four 16-token blocks, K as two
+    // 64-d boxes and V^T as one box each, on the stage's mbarrier.
+    auto load_step = [&](int j) {
+        if (tid != 0) return;
+        const int st = j & 1;
+        const uint32_t kst = sbase + kStageOff + st * kStageBytes;
+        int phys[kStep / 16];
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int b = 0; b < kStep / 16; ++b) {
+            const int tok = j * kStep + 16 * b;
+            phys[b] = -1;
+            if (tok < kv_end) {
+                const int x = __ldg(table + tok / 16);
+                if (x < 0 || x >= p.num_blocks) pa_dev::record_error(p.err, PA_ERR_BAD_BLOCK_ID);
+                else phys[b] = x;
+            }
+            if (phys[b] >= 0) bytes += 2 * 2048 + 4096;
+        }
+        pa_tc::mbar_expect_tx(bar_full + st, bytes);
+#pragma unroll
+        for (int b = 0; b < kStep / 16; ++b) {
+            if (phys[b] < 0) continue;
+            const int yk = (phys[b] * Hkv + h) * 16, yv = (phys[b] * Hkv + h) * kD;
+            pa_tc::tma_load_2d(kst + b * 2048, &kmap, 0, yk, bar_full + st);
+            pa_tc::tma_load_2d(kst + 8192 + b * 2048, &kmap, 64, yk, bar_full + st);
+            pa_tc::tma_load_2d(kst + 16384 + b * 4096, &vmap, 0, yv, bar_full + st);
+        }
+    };
+
+    load_step(0);
+    float m_ref = -INFINITY, l = 0.f;
+    for (int j = 0; j < nsteps && ok; ++j) {
+        const int st = j & 1;
+        if (j > 0) {                                       // P.V of step j-1 done
+            const bool w = pa_tc::mbar_wait(bar_pv, ph_pv, kWaitLimit);
+            if (!__syncthreads_and(w)) { ok = false; break; }
+            ph_pv ^= 1u;
+        }
+        if (j + 1 < nsteps) load_step(j + 1);
+        if (j == 0) pa_tc::cp_wait<0>();
+        {
+            const bool w = pa_tc::mbar_wait(bar_full + st, st ? ph_full1 : ph_full0, kWaitLimit);
+            if (st) ph_full1 ^= 1u; else ph_full0 ^= 1u;
+            if (!__syncthreads_and(w)) { ok = false; break; }
+        }
+        pa_tc::fence_smem_to_async();
+        pa_tc::fence_before_sync();
+        __syncthreads();
+        pa_tc::fence_after_sync();
+        const uint32_t kst = sbase + kStageOff + st * kStageBytes;
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint64_t a = pa_tc::sw128_desc(sbase + kQOff + (kk >> 2) * 16384 + (kk & 3) * 32);
+                const uint64_t b = pa_tc::sw128_desc(kst + (kk >> 2) * 8192 + (kk & 3) * 32);
+                pa_tc::mma_bf16(tS, a, b, kIdescQK, kk > 0);
+            }
+            pa_tc::commit(bar_s);
+        }
+        {
+            const bool w = pa_tc::mbar_wait(bar_s, ph_s, kWaitLimit);
+            if (!__syncthreads_and(w)) { ok = false; break; }
+        }
+        ph_s ^= 1u;
+        pa_tc::fence_after_sync();
+        float sc[64];
+        {
+            float a32[32], b32[32];
+            pa_tc::tmem_ld32(tS + lane_sel, a32);
+            pa_tc::tmem_ld32(tS + lane_sel + 32, b32);
+            pa_tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                sc[i] = a32[i];
+                sc[32 + i] = b32[i];
+            }
+        }
+        // causal mask: key j*64 + i is visible to this row iff it is at or
+        // before the row's position (pos < kv_end, so this also ends the keys);
+        // a block whose id is outside the pool was not loaded and is skipped
+        const int kbase = j * kStep;
+        int skip = 0;
+#pragma unroll
+        for (int b = 0; b < kStep / 16; ++b) {
+            if (kbase + 16 * b < kv_end) {
+                const int x = __ldg(table + (kbase >> 4) + b);
+                if (x < 0 || x >= p.num_blocks) skip |= 1 << b;
+            }
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            sc[i] = kbase + i <= pos && !((skip >> (i >> 4)) & 1) ? sc[i] * sl : -INFINITY;
+            mx = fmaxf(mx, sc[i]);
+        }
+        const bool first = m_ref == -INFINITY;
+        const bool raise = !first && mx > m_ref + 8.f;
+        if (first) m_ref = mx;
+        if (__any_sync(0xffffffffu, raise)) {
+            const float corr = raise ? exp2_approx(m_ref - mx) : 1.f;
+            if (raise) {
+                l *= corr;
+                m_ref = mx;
+            }
+#pragma unroll
+            for (int cc = 0; cc < kD / 32; ++cc) {
+                float o[32];
+                pa_tc::tmem_ld32(tO + lane_sel + cc * 32, o);
+                pa_tc::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] *= corr;
+                pa_tc::tmem_st32(tO + lane_sel + cc * 32, o);
+            }
+            pa_tc::tmem_wait_st();
+        }
+        const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+        float sum = 0.f;
+        {
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float p0 = exp2_approx(sc[2 * e] - ref);
+                const float p1 = exp2_approx(sc[2 * e + 1] - ref);
+                sum += p0 + p1;
+                hi[e] = pa_dev::pack_bf16(p0, p1);
+                lo[e] = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(hi[e]), p1 - pa_dev::bf16_hi(hi[e]));
+            }
+            pa_tc::tmem_st32u(tPh + lane_sel, hi);
+            pa_tc::tmem_st32u(tPl + lane_sel, lo);
+            pa_tc::tmem_wait_st();
+        }
+        l += sum;
+        pa_tc::fence_before_sync();
+        __syncthreads();
+        pa_tc::fence_after_sync();
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < kStep / 16; ++kk) {
+                const uint64_t b = pa_tc::sw32_desc(kst + 16384 + kk * 4096);
+                pa_tc::mma_bf16_ta(tO, tPh + kk * 8, b, kIdescPV, j > 0 || kk > 0);
+                pa_tc::mma_bf16_ta(tO, tPl + kk * 8, b, kIdescPV, true);
+            }
+            pa_tc::commit(bar_pv);
+        }
+    }
+    if (ok) {
+        const bool w = pa_tc::mbar_wait(bar_pv, ph_pv, kWaitLimit);
+        ok = __syncthreads_and(w);
+        ph_pv ^= 1u;
+    }
+    if (ok) {
+        pa_tc::fence_after_sync();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const size_t orow = row_ok ? (static_cast<size_t>(q0 + qi) * p.Hq +
+                                      static_cast<size_t>(h) * G + r % G) * kD : 0;
+#pragma unroll
+        for (int cc = 0; cc < kD / 32; ++cc) {
+            float o[32];
+            pa_tc::tmem_ld32(tO + lane_sel + cc * 32, o);
+            pa_tc::tmem_wait_ld();
+            if (!row_ok) continue;
+            if (p.out_bf16) {
+                uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + orow + cc * 32);
+#pragma unroll
+                for (int i = 0; i < 32; i += 8)
+                    *reinterpret_cast<uint4*>(dst + i / 2) =
+                        make_uint4(pa_dev::pack_bf16(o[i] * inv, o[i + 1] * inv),
+                                   pa_dev::pack_bf16(o[i + 2] * inv, o[i + 3] * inv),
+                                   pa_dev::pack_bf16(o[i + 4] * inv, o[i + 5] * inv),
+                                   pa_dev::pack_bf16(o[i + 6] * inv, o[i + 7] * inv));
+            } else {
+                float* dst = static_cast<float*>(p.out) + orow + cc * 32;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4*>(dst + i) =
+                        make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+            }
+        }
+    }
+    if (!ok && tid == 0) pa_dev::record_error(p.err, PA_ERR_CUDA);
+    pa_tc::cp_wait<0>();
+    pa_tc::fence_before_sync();
+    __syncthreads();
+    pa_tc::fence_after_sync();
+    if (warp == 0) pa_tc::tmem_free<kTmemCols>(tmem);
+}
+
 }  // namespace
 
 namespace pa_detail {
+
+bool prefill_tc_eligible(const pa_pool* pool) {
+    return pool->dtype == PA_BF16 && pool->head_dim == kD && pool->block_size == 16 &&
+           static_cast<long long>(pool->num_blocks) * pool->kv_heads * kD < (1LL << 31);
+}
+
+int prefill_tc_rows() { return kRows; }
+
+int launch_prefill_tc(pa_pool* pool, const PrefillParams& p, dim3 grid, cudaStream_t st) {
+    const int rc = ensure_tensor_maps(pool);
+    if (rc != PA_OK) return rc;
+    if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    const cudaError_t e = launch_pdl(prefill_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, p,
+                                     pool->kmap, pool->vmap);
+    count_launch();
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
 
 bool shared_tc_eligible(const pa_pool* pool, int G) {
     // TMA coordinates are 32-bit: value rows num_blocks * Hkv * D must stay below 2^31

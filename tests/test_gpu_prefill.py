@@ -64,15 +64,26 @@ SMALL = [
 ]
 
 
+@pytest.fixture(params=["default", "mma_sync"])
+def form(request, monkeypatch):
+    """The default dispatch (tcgen05 for bf16 pools of 16-token blocks and
+    head_dim 128, mma.sync otherwise) and the mma.sync kernel forced."""
+    if request.param == "mma_sync":
+        monkeypatch.setenv("PA_PREFILL_MMA_SYNC", "1")
+    else:
+        monkeypatch.delenv("PA_PREFILL_MMA_SYNC", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("kw", SMALL, ids=[f"case{i}" for i in range(len(SMALL))])
-def test_small_parity(kw):
+def test_small_parity(kw, form):
     wl = wls.make_workload("prefill", **kw)
     values = wls.generate_values(wl, "cuda")
     err, _ = _check(wl, values)
-    print(f"prefill {kw}: max-abs {err:.3g}")
+    print(f"prefill [{form}] {kw}: max-abs {err:.3g}")
 
 
-def test_bf16_output_is_the_fp32_output_rounded():
+def test_bf16_output_is_the_fp32_output_rounded(form):
     wl = wls.make_workload("prefill", lengths=[9, 0], chunks=[20, 37], **D128)
     values = wls.generate_values(wl, "cuda")
     _, step = _check(wl, values)
@@ -82,7 +93,7 @@ def test_bf16_output_is_the_fp32_output_rounded():
     assert torch.equal(out16, step.out.to(torch.bfloat16))
 
 
-def test_two_chunks_equal_one():
+def test_two_chunks_equal_one(form):
     """A prompt prefilled as one chunk, and as two chunks with the second
     after the first's append, gives the second chunk's rows the same outputs
     (up to fp32 summation order: the tiles differ)."""
@@ -100,7 +111,7 @@ def test_two_chunks_equal_one():
     assert (a - b).abs().max().item() <= 1e-5
 
 
-def test_device_errors_are_recorded_not_faulted():
+def test_device_errors_are_recorded_not_faulted(form):
     wl = wls.make_workload("prefill", lengths=[10, 4], chunks=[8, 6], **D128)
     values = wls.generate_values(wl, "cuda")
     pool, _, step = _run(wl, values)
@@ -134,7 +145,7 @@ def test_device_errors_are_recorded_not_faulted():
     assert pool.get_error() == 0
 
 
-def test_full_size_parity():
+def test_full_size_parity(form):
     """The prefill workload (16 sequences, cached prefixes up to 4096, chunks of
     128..512) at full size: bookkeeping and pools bit-exact, attention on every
     row of sampled sequences."""
@@ -142,4 +153,4 @@ def test_full_size_parity():
     values = wls.generate_values(wl, "cuda")
     seqs = [0, 7, wl.num_seqs - 1]
     err, _ = _check(wl, values, seqs=seqs, threads=16)
-    print(f"prefill full size: max-abs over sequences {seqs}: {err:.3g}")
+    print(f"prefill [{form}] full size: max-abs over sequences {seqs}: {err:.3g}")
