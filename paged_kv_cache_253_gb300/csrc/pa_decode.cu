@@ -467,7 +467,9 @@ __device__ __forceinline__ void cp_async_wait() {
 // F8 (fp8 pool, direct loads only): the same fragments are read as e4m3
 // codes, half the bytes (8 per K chunk, 4 per V^T row piece), and widened to
 // f16 pairs in registers; the queries are re-rounded to f16 once per item.
-template <int D, bool FUSE, bool F8 = false>
+// BS > 0: the pool's block size is known to be BS at compile time (16-token
+// blocks: one 16-token tile per block, constant value-row strides).
+template <int D, bool FUSE, bool F8 = false, int BS = 0>
 __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, int tok0,
                                           int tok1, int L, unsigned char* ring, float* sm_o,
                                           float* sm_m, float* sm_l) {
@@ -477,7 +479,7 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
     constexpr int OS = D + 4;             // padded row stride of the merge buffer
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
-    const int B = p.B, nsub = B / 16;
+    const int B = BS > 0 ? BS : p.B, nsub = B / 16;
 
     WarpAcc<D> a;
     {
@@ -1054,7 +1056,10 @@ decode_fast_kernel(const DecodeParams p) {
         const int PTq = sc.pt(s);
         const int nP = max(1, (max(0, L - start) + PTq - 1) / PTq);
         const int tok0 = start + part * PTq, tok1 = min(L, tok0 + PTq);
-        fast_item<D, FUSE, F8>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
+        if (p.B == 16)
+            fast_item<D, FUSE, F8, 16>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
+        else
+            fast_item<D, FUSE, F8>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
         __syncthreads();
         // merge the warps' softmax states (in place into warp 0's buffer)
         for (int idx = threadIdx.x; idx < p.G * D; idx += kThreads) {
