@@ -1056,7 +1056,10 @@ decode_fast_kernel(const DecodeParams p) {
         const int PTq = sc.pt(s);
         const int nP = max(1, (max(0, L - start) + PTq - 1) / PTq);
         const int tok0 = start + part * PTq, tok1 = min(L, tok0 + PTq);
-        if (p.B == 16)
+        // the compile-time 16-token walk pays off for fp8 codes (13 % fewer
+        // instructions, 5 % faster); the bf16 walk, bound by load latency, ran
+        // 1.5 us slower with it on the decode batch (measured on GB300)
+        if (F8 && p.B == 16)
             fast_item<D, FUSE, F8, 16>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
         else
             fast_item<D, FUSE, F8>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
