@@ -53,6 +53,11 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.pa_append_kv(None, None, None, None, 0, None) == lib.PA_ERR_INVALID_ARG
     assert lib.pa_decode(None, None, 1, 8, None, 1, None, 1.0, None, 0, None) == \
         lib.PA_ERR_INVALID_ARG
+    assert lib.pa_prefill(None, None, 4, 8, None, 1, 4, None, 1, None, 1.0, None, 0, None) == \
+        lib.PA_ERR_INVALID_ARG
+    assert lib.pa_pool_set_kv_scales(None, 1.0, 1.0) == lib.PA_ERR_INVALID_ARG
+    assert lib.pa_pool_kv_scales(None, None, None) == lib.PA_ERR_INVALID_ARG
+    assert lib.PA_FP8E4M3 == 2
 
 
 def test_fnv_vectors(lib):
