@@ -191,7 +191,7 @@ def _oracle_sample(wl, values, target_s=12.0, threads=None):
     lens = st.context_lens
     order = np.random.default_rng(wl.seed).permutation(wl.num_seqs)
     # grow the sample until it takes about target_s (cycling over the batch)
-    n, spent, done_tok, done_seq, calls = 1, 0.0, 0, 0, 0
+    n, spent, done_tok, done_seq, done_q, calls = 1, 0.0, 0, 0, 0, 0
     pos = 0
     while spent < target_s:
         if pos >= len(order):
@@ -206,6 +206,8 @@ def _oracle_sample(wl, values, target_s=12.0, threads=None):
         spent += dt
         done_tok += int(lens[pick].sum())
         done_seq += len(pick)
+        # query tokens served: one per decode, a whole chunk per prefill
+        done_q += int(wl.chunk_lens[pick].sum()) if wl.chunk_lens is not None else len(pick)
         pos += len(pick)
         calls += 1
         n = max(1, min(len(order), int(n * 2)))
@@ -214,7 +216,7 @@ def _oracle_sample(wl, values, target_s=12.0, threads=None):
     kind = "chunk prefills" if wl.chunk_lens is not None else "decodes"
     desc = (f"{done_seq} sequence {kind} ({done_tok} cached tokens) drawn from the same "
             f"{wl.num_seqs}-sequence batch, float64 oracle, {threads} threads, {spent:.1f} s")
-    return gbs, done_seq / spent, threads, desc
+    return gbs, done_q / spent, threads, desc
 
 
 def _dtype_kw(args):
