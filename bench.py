@@ -70,6 +70,23 @@ def _dist():
     return world, rank, local
 
 
+def max_over_ranks(dist, values, device):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the job's
+    time); the values unchanged when there is no process group."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(world, units_per_rank, ms):
+    """Whole-job rate: the units every rank processed in the slowest rank's time
+    (weak scaling: each rank holds its own replica of the workload)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def _workload_desc(wl):
     return (f"{wl.name}: {wl.description}; block_size {wl.block_size}, {wl.num_q_heads} q / "
             f"{wl.num_kv_heads} KV heads, head_dim {wl.head_dim}, {wl.dtype}, "
@@ -230,7 +247,7 @@ def run_reference(args):
     from paged_kv_cache_253_gb300 import workloads as wls
     wl = wls.make_workload(args.workload, **_dtype_kw(args))
     values = wls.generate_values(wl, "cpu")
-    per_step = max(2.0, 40.0 / max(1, args.steps + args.warmup))
+    per_step = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         _oracle_sample(wl, values, target_s=per_step / 4)
     vals, toks, descs = [], [], []
@@ -330,10 +347,7 @@ def run_ours(args):
         dist.barrier()
     ms = sum(step_ms) / len(step_ms)
     dms = sum(dec_ms) / len(dec_ms)
-    if dist:
-        t = torch.tensor([ms, dms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, dms = t.tolist()
+    ms, dms = max_over_ranks(dist, [ms, dms], f"cuda:{local}")
     if pool.get_error():
         raise RuntimeError("device error during the timed steps")
 
@@ -376,10 +390,7 @@ def run_ours(args):
         if i >= args.warmup:
             e2e_ms.append(a.elapsed_time(c))
     ems = sum(e2e_ms) / len(e2e_ms)
-    if dist:
-        t = torch.tensor([ems], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ems = t.item()
+    (ems,) = max_over_ranks(dist, [ems], f"cuda:{local}")
 
     peak, peak_kind = _peaks()
     achieved = algo_bytes / (dms * 1e-3) / 1e9
@@ -396,7 +407,7 @@ def run_ours(args):
                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                     "traffic": _traffic_from_profile(wl), "kernel": "decode (pa_decode)",
                     "algorithmic_bytes_per_launch": algo_bytes}
-    value = world * kv_bytes / (ms * 1e-3) / 1e9
+    value = job_throughput(world, kv_bytes, ms) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
@@ -410,11 +421,11 @@ def run_ours(args):
                    "copy_pairs_per_step": step.num_pairs,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_frac_of_" + peak_kind: round(value / world / peak, 4),
-        "tokens_per_s": round(world * wl.num_step_tokens / (ms * 1e-3), 1),
+        "tokens_per_s": round(job_throughput(world, wl.num_step_tokens, ms), 1),
         "decode_ms": round(dms, 5),
         "launches_per_step": step.launches(),
         "roofline": roofline,
-        "e2e": {"value": round(world * kv_bytes / (ems * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(job_throughput(world, kv_bytes, ems) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(ems, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
@@ -443,6 +454,8 @@ def main():
     ap.add_argument("--kv-dtype", default=None, choices=["f32", "bf16", "fp8"],
                     help="pool element type (default: the workload's own; fp8 = e4m3 codes)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=40.0,
+                    help="--impl reference: total oracle seconds over warm-up and timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
