@@ -19,6 +19,13 @@
  *     library never frees caller memory.
  *   - Streams: `stream` is a cudaStream_t passed as void*.  NULL means the
  *     legacy default stream.  Every GPU call is asynchronous on it.
+ *   - CUDA graphs: once the pool's workspace holds the batch (a first call of
+ *     the same shape, or pa_decode_reserve), pa_append_kv, pa_copy_blocks,
+ *     pa_decode, pa_append_decode, pa_decode_noalloc and pa_prefill only
+ *     launch kernels on `stream`, so they may be captured into a graph and
+ *     replayed.  pa_decode_shared uploads its group description with a
+ *     pageable copy when the description changes, pa_get_error synchronises:
+ *     keep those two out of a capture.
  *
  * Pool layout (owned by the pool, created zeroed):
  *   K: [num_blocks][kv_heads][block_size][head_dim]   keys, one row per token
