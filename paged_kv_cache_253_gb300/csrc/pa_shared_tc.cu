@@ -454,12 +454,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
     float m_ref = -INFINITY, l = 0.f;
     for (int j = 0; j < nsteps && ok; ++j) {
         const int st = j & 1;
-        if (j > 0) {                                       // P.V of step j-1 done
-            const bool w = pa_tc::mbar_wait(bar_pv, ph_pv, kWaitLimit);
-            if (!__syncthreads_and(w)) { ok = false; break; }
-            ph_pv ^= 1u;
-        }
-        if (j + 1 < nsteps) load_step(j + 1);
+        // S = Q.K^T of this step is issued as soon as its keys have landed,
+        // behind the previous step's P.V in the tensor pipe: it writes only the
+        // S columns (read out before that P.V was issued) and reads this
+        // step's stage, so it need not wait for that P.V to finish
         if (j == 0) pa_tc::cp_wait<0>();
         {
             const bool w = pa_tc::mbar_wait(bar_full + st, st ? ph_full1 : ph_full0, kWaitLimit);
@@ -480,6 +478,14 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
             }
             pa_tc::commit(bar_s);
         }
+        // the previous P.V must be done before its stage is refilled, before P
+        // is overwritten and before O is rescaled
+        if (j > 0) {
+            const bool w = pa_tc::mbar_wait(bar_pv, ph_pv, kWaitLimit);
+            if (!__syncthreads_and(w)) { ok = false; break; }
+            ph_pv ^= 1u;
+        }
+        if (j + 1 < nsteps) load_step(j + 1);
         {
             const bool w = pa_tc::mbar_wait(bar_s, ph_s, kWaitLimit);
             if (!__syncthreads_and(w)) { ok = false; break; }
