@@ -84,3 +84,30 @@ def test_paged_attention_over_fp8_values_equals_contiguous():
     vseq = [np.concatenate([v[b] .transpose(1, 0, 2) for b in t[t >= 0]])[:L] for t, L in zip(tables, lens)]
     ref = oatt.contiguous_decode(q, kseq, vseq, 0.3, hkv)
     assert np.array_equal(out, ref)
+
+
+def test_encoder_is_the_brute_force_nearest_value():
+    """For values across every binade (and exact midpoints), the code is the
+    finite e4m3 value nearest to y, the even code on a tie, +-448 beyond 448:
+    checked against a search over all 254 finite codes."""
+    rng = np.random.default_rng(11)
+    codes = np.arange(256, dtype=np.uint8)
+    vals = fp8.e4m3_decode(codes)
+    fin = ~np.isnan(vals)
+    fc, fv = codes[fin], vals[fin]
+    mags = np.exp2(rng.uniform(-12, 9.5, 20000))
+    pos = np.sort(np.unique(np.abs(fv)))
+    mids = (pos[:-1] + pos[1:]) / 2                         # exact in float32
+    y = np.concatenate([mags, -mags, mids, -mids]).astype(np.float32)
+    got = fp8.e4m3_encode(y)
+    yy = np.minimum(np.abs(y.astype(np.float64)), 448.0) * np.where(np.signbit(y), -1.0, 1.0)
+    d = np.abs(yy[:, None] - fv[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best
+    # among equally near codes take the even one (the sign of zero follows y)
+    even = cand & ((fc[None, :] & 1) == 0)
+    pick = np.where(even.any(axis=1, keepdims=True), even, cand)
+    sign_ok = (fc[None, :] >> 7) == np.signbit(y)[:, None]
+    pick = pick & np.where((fv[None, :] == 0), sign_ok, True)
+    want = fc[np.argmax(pick, axis=1)]
+    assert np.array_equal(got, want)
