@@ -158,3 +158,49 @@ def test_prefill_workload_replay_equals_contiguous_causal():
             attn_mask=torch.from_numpy(mask), scale=wl.scale)
         np.testing.assert_allclose(out[st.cu_seqlens_q[s]:st.cu_seqlens_q[s + 1]],
                                    ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_after_a_fork_copies_the_shared_partial_block():
+    """Two requests share a 10-token prompt (block size 4: the third block is
+    partly filled and shared); each then prefills its own chunk.  The first
+    chunk token of the first request copies the shared partial block (the
+    second request, the last holder, writes in place), and each request's
+    queries see only its own chunk on top of the shared prompt."""
+    torch = pytest.importorskip("torch")
+    from oracle import replay as orp
+    from paged_kv_cache_253_gb300 import workloads as wls
+    rng = np.random.default_rng(12)
+    prompt = rng.integers(0, 100, size=10).astype(np.int32)
+    chunks = np.array([5, 3], np.int32)
+    wl = wls.Workload(name="prefill", block_size=4, num_q_heads=4, num_kv_heads=2, head_dim=8,
+                      dtype="bf16", num_blocks=12,
+                      free_order=rng.permutation(12).astype(np.int32),
+                      events=[("add", 0, prompt, 0), ("extend", 0, prompt), ("fork", 1, 0)],
+                      batch=np.array([0, 1], np.int32),
+                      step_tokens=rng.integers(0, 100, size=8).astype(np.int32),
+                      scale=0.35, seed=12, chunk_lens=chunks)
+    values = wls.generate_values(wl, "cpu")
+    st = orp.replay(wl, values)
+    assert len(st.step_pairs) == 1                       # one copy-on-write, by request 0
+    t0, t1 = st.block_tables
+    assert t0[0] == t1[0] and t0[1] == t1[1] and t0[2] != t1[2]
+    assert st.context_lens.tolist() == [15, 13]
+    out = orp.prefill_attention(wl, values, st)
+    hk = oatt.bf16_bits_to_f32(orp.values_to_numpy(values["hist_k"]))
+    hv = oatt.bf16_bits_to_f32(orp.values_to_numpy(values["hist_v"]))
+    nk = oatt.bf16_bits_to_f32(orp.values_to_numpy(values["new_k"]))
+    nv = oatt.bf16_bits_to_f32(orp.values_to_numpy(values["new_v"]))
+    q = oatt.bf16_bits_to_f32(orp.values_to_numpy(values["q"]))
+    cu = [0, 5, 8]
+    for s in range(2):
+        ks = np.concatenate([hk, nk[cu[s]:cu[s + 1]]]).astype(np.float64)
+        vs = np.concatenate([hv, nv[cu[s]:cu[s + 1]]]).astype(np.float64)
+        L, n = 10 + chunks[s], chunks[s]
+        mask = np.tril(np.ones((L, L), dtype=bool))[L - n:]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[cu[s]:cu[s + 1]].astype(np.float64)).permute(1, 0, 2),
+            torch.from_numpy(ks).permute(1, 0, 2).repeat_interleave(2, 0),
+            torch.from_numpy(vs).permute(1, 0, 2).repeat_interleave(2, 0),
+            attn_mask=torch.from_numpy(mask), scale=0.35)
+        np.testing.assert_allclose(out[cu[s]:cu[s + 1]], ref.permute(1, 0, 2).numpy(),
+                                   rtol=1e-12, atol=1e-12)
