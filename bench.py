@@ -4,17 +4,23 @@ A step is one pass of the hot path over one batch: copy-on-write block copies
 (when the step has any), KV append of every sequence's new token, and paged
 decode attention over every cached token, new one included.
 
-Default workload: the decode batch (64 sequences, context lengths U[128, 2048],
-block_size 16, 32 query / 8 KV heads, head_dim 128, bf16, pool 1.25x the
-blocks needed, scattered block tables).  Other workloads: --workload
-{prefix,long,mixed,tiny}.
+Default workload: long context (8 sequences, context lengths U[32768, 131072],
+block_size 16, 32 query / 8 KV heads, head_dim 128, bf16, pool 1.1x demand,
+scattered block tables; about 2.7 GB of keys and values per step, the largest
+of the single-GPU workloads).  Other workloads: --workload
+{decode,prefix,mixed,prefill,tiny}.
 
 value      = unique KV bytes the decode reads per step / device step time (GB/s),
              inputs resident in HBM, L2 flushed between steps (a 256 MiB write, then a
              read pass long enough that L2 holds only clean lines).
 e2e        = the same bytes / step time through the public API with host
              buffers: pinned host->device copies of the step's inputs, the
-             three library calls, device->host copy of the output.
+             library calls, device->host copy of the output.  The host block
+             manager's bookkeeping for the step (slot reservation, tables,
+             sharing groups) runs before the timed region; its own host time
+             is reported beside the line as host_bookkeeping_ms.
+graph_ms_per_step = the same step captured once into a CUDA graph and
+             replayed (L2 flushed between replays, outside the graph).
 roofline   = the decode kernel alone: algorithmic bytes per launch / its
              CUDA-event time, against the measured HBM copy bandwidth.
 cpu_baseline = the float64 oracle on the host cores on a bounded sample.
@@ -115,21 +121,40 @@ def _algo_bytes(wl, lens):
     return _kv_bytes(wl, lens) + q + out + blocks * 4 + S * 4
 
 
+# committed ncu summary of each workload's attention call (profiles/<name>.md)
+TRAFFIC_PROFILES = {
+    ("decode", "bf16"): "decode_kernel_decode_batch.md",
+    ("decode", "fp8"): "decode_kernel_decode_batch_fp8.md",
+    ("long", "bf16"): "decode_kernel_long_context.md",
+    ("mixed", "bf16"): "decode_kernel_mixed.md",
+    ("prefix", "bf16"): "decode_call_prefix.md",
+}
+
+
+def source_digest(names):
+    """sha256[:16] over the named csrc files, concatenated in the given order."""
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_cache_253_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def _traffic_from_profile(wl):
-    """DRAM bytes per launch of the decode kernel from the committed ncu summary
-    of this workload and pool type, valid only while the kernel source is
-    unchanged."""
-    if wl.name != "decode" or wl.dtype not in ("bf16", "fp8"):
+    """DRAM bytes (read + write) per attention call from the committed ncu
+    summary of this workload and pool type (captured at full size, or scaled
+    from a smaller capture as the summary states); valid only while the kernel
+    sources it names are unchanged (else None)."""
+    name = TRAFFIC_PROFILES.get((wl.name, wl.dtype))
+    if name is None:
         return None
-    src = os.path.join(ROOT, "paged_kv_cache_253_gb300", "csrc", "pa_decode.cu")
-    name = "decode_kernel_decode_batch" + ("_fp8" if wl.dtype == "fp8" else "") + ".md"
-    prof = os.path.join(ROOT, "profiles", name)
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        text = open(prof).read()
+        text = open(os.path.join(ROOT, "profiles", name)).read()
+        m_src = re.search(r"sources:\s*`([^`]+)`", text)
+        srcs = m_src.group(1).split() if m_src else ["pa_decode.cu"]
         m_hash = re.search(r"source sha256\[:16\]:\s*`?([0-9a-f]{16})", text)
         m_tr = re.search(r"dram bytes per launch:\s*\|?\s*`?([0-9]+)", text)
-        if m_hash and m_tr and m_hash.group(1) == digest:
+        if m_hash and m_tr and m_hash.group(1) == source_digest(srcs):
             return int(m_tr.group(1))
     except OSError:
         pass
@@ -197,14 +222,15 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def _oracle_sample(wl, values, target_s=12.0, threads=None):
+def _oracle_sample(wl, values, target_s=12.0, threads=None, st=None):
     """Time the oracle (step appends + float64 decode) on a bounded sample of
     sequences; returns (GB/s of KV processed, tokens/s, threads, description)."""
     import numpy as np
     from oracle import replay as orp
     from oracle.attention import default_threads
     threads = threads or default_threads()
-    st = orp.replay(wl, values)
+    if st is None:
+        st = orp.replay(wl, values)
     lens = st.context_lens
     order = np.random.default_rng(wl.seed).permutation(wl.num_seqs)
     # grow the sample until it takes about target_s (cycling over the batch)
@@ -237,7 +263,10 @@ def _oracle_sample(wl, values, target_s=12.0, threads=None):
 
 
 def _dtype_kw(args):
-    return {"dtype": args.kv_dtype} if args.kv_dtype else {}
+    kw = {"dtype": args.kv_dtype} if args.kv_dtype else {}
+    if args.num_seqs:
+        kw["num_seqs"] = args.num_seqs
+    return kw
 
 
 def run_reference(args):
@@ -291,6 +320,7 @@ def run_ours(args):
     prefill = wl.chunk_lens is not None
     step = runtime.prepare_prefill(wl, values, pool, bm) if prefill else \
         runtime.prepare_step(wl, values, pool, bm)
+    host_ms = step.host_ms
     lens = step.context_lens.cpu().numpy()
     # unique bytes: a shared span counts once per group whichever decode path runs
     all_groups = bm.prefix_groups(wl.batch)
@@ -392,6 +422,30 @@ def run_ours(args):
     ems = sum(e2e_ms) / len(e2e_ms)
     (ems,) = max_over_ranks(dist, [ems], f"cuda:{local}")
 
+    # ---- the same step replayed from a CUDA graph ----
+    gms = None
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step.run()                                  # warm: workspace sized, descriptors uploaded
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step.run()
+        torch.cuda.synchronize()
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
+        gms = sum(timed(graph.replay, args.steps)) / args.steps
+        (gms,) = max_over_ranks(dist, [gms], f"cuda:{local}")
+        if pool.get_error():
+            raise RuntimeError("device error during the graph replays")
+    except RuntimeError as e:
+        if "device error" in str(e):
+            raise
+        gms = None
+
     peak, peak_kind = _peaks()
     achieved = algo_bytes / (dms * 1e-3) / 1e9
     if prefill:
@@ -427,15 +481,28 @@ def run_ours(args):
         "roofline": roofline,
         "e2e": {"value": round(job_throughput(world, kv_bytes, ems) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(ems, 5), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "note": "host block-manager bookkeeping (slots, tables, sharing groups) runs "
+                        "before the timed region; its host time is host_bookkeeping_ms"},
+        "host_bookkeeping_ms": round(host_ms, 4),
+        "graph_ms_per_step": None if gms is None else round(gms, 5),
+        "graph_value": None if gms is None else round(job_throughput(world, kv_bytes, gms) / 1e9, 2),
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, tps, threads, desc = _oracle_sample(wl, {k: v.cpu() for k, v in values.items()},
-                                                 target_s=args.cpu_seconds)
+        from oracle import replay as orp
+        cvals = {k: v.cpu() for k, v in values.items()}
+        st = orp.replay(wl, cvals)
+        gbs, tps, threads, desc = _oracle_sample(wl, cvals, target_s=args.cpu_seconds, st=st)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
                                 "kind": "oracle", "sample": desc}
+        if wl.name in ("tiny", "decode"):
+            # the same oracle on one host thread
+            gbs1, _, _, desc1 = _oracle_sample(wl, cvals, target_s=args.cpu_seconds / 2,
+                                               threads=1, st=st)
+            line["cpu_baseline_1thread"] = {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                                            "kind": "oracle", "sample": desc1}
     if rank == 0:
         print(json.dumps(line))
     if dist:
@@ -449,10 +516,13 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode",
+    ap.add_argument("--workload", default="long",
                     choices=["tiny", "decode", "prefix", "long", "mixed", "prefill"])
     ap.add_argument("--kv-dtype", default=None, choices=["f32", "bf16", "fp8"],
                     help="pool element type (default: the workload's own; fp8 = e4m3 codes)")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="shrink the workload to this many sequences (reduced cases for "
+                         "profiler captures; the bench lines use the full workloads)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=40.0,
                     help="--impl reference: total oracle seconds over warm-up and timed steps")

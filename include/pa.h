@@ -81,8 +81,9 @@ enum {
 
 /* Create a KV pool of `num_blocks` physical blocks of `block_size` token
  * positions each, for `kv_heads` heads of width `head_dim` ([K] "Split the
- * Cache Into Fixed Blocks": a block holds a fixed number of positions; its
- * bytes depend on heads, head width and dtype).  One pool holds one layer.
+ * Cache Into Fixed Blocks": every block has room for the same number of token
+ * positions, and its size in bytes follows from the heads, the head width and
+ * the element type).  One pool holds one layer.
  * Allocates and zeroes K and V on the current CUDA device (synchronously).
  * Limits: block_size in [1, 1024]; head_dim in [4, 256], a multiple of 4;
  * kv_heads >= 1.
@@ -116,8 +117,35 @@ int pa_pool_info(const pa_pool *pool, int *num_blocks, int *block_size, int *kv_
 int pa_pool_set_kv_scales(pa_pool *pool, float k_scale, float v_scale);
 int pa_pool_kv_scales(const pa_pool *pool, float *k_scale, float *v_scale);
 
-/* Write each new token's keys and values into its slot ([Z] answer: a new
- * token "is written there"; [K] "Growth Needs Only Another Free Block").
+/* Kernel-choice options of a pool.  The library reads no environment
+ * variables: every choice that is not automatic is set here, explicitly, by
+ * the caller (host only; it applies from the next call on this pool).  All
+ * options select among kernels that compute the same result within the
+ * stated tolerances; none changes what is computed.
+ *   PA_OPT_PARTITION_CAP   decode partitions of at most `value` tokens
+ *                          (rounded down to a multiple of block_size, never
+ *                          below the smallest partition); 0 = no cap;
+ *                          -1 (default) = automatic: 2048 tokens when the
+ *                          batch has more sequences than the GPU has SMs,
+ *                          else no cap.
+ *   PA_OPT_SHARED_KERNEL   shared-prefix items of pa_decode_shared: 0
+ *                          (default) = the tcgen05 kernel where the shape
+ *                          allows it, 1 = the mma.sync form.
+ *   PA_OPT_PREFILL_KERNEL  pa_prefill: 0 (default) = the tcgen05 kernel where
+ *                          the shape allows it, 1 = the mma.sync form.
+ * An unknown option or a value out of range returns PA_ERR_INVALID_ARG and
+ * changes nothing. */
+typedef enum {
+    PA_OPT_PARTITION_CAP = 0,
+    PA_OPT_SHARED_KERNEL = 1,
+    PA_OPT_PREFILL_KERNEL = 2
+} pa_option;
+int pa_pool_set_option(pa_pool *pool, pa_option option, int value);
+int pa_pool_get_option(const pa_pool *pool, pa_option option, int *value);
+
+/* Write each new token's keys and values into its slot ([Z] answer: the new
+ * token's data goes into the slot its request was given; [K] "Growth Needs
+ * Only Another Free Block").
  *   k, v          device [T][kv_heads][head_dim], pool dtype (bf16 for an fp8 pool),
  *                 row-major
  *   slot_mapping  device int64 [T]; slot = block * block_size + offset;
@@ -130,7 +158,8 @@ int pa_append_kv(pa_pool *pool, const void *k, const void *v, const int64_t *slo
 
 /* Copy-on-write block copies ([K] "Shared Blocks Must Not Be Changed in
  * Place": a private copy of the shared block is made before the diverging
- * write; [Z] "only a divergent block is ever copied, and only that block").
+ * write; [Z] "Most common mistake": the copy is limited to the one block
+ * where the requests diverge).
  *   pairs  device int64 [P][2] = (src, dst); each copies all kv_heads x
  *          block_size x head_dim elements of K and of V, bit for bit.
  * A pair whose block id is outside the pool records PA_ERR_BAD_BLOCK_ID; a
@@ -159,14 +188,9 @@ int pa_copy_blocks(pa_pool *pool, const int64_t *pairs, int num_pairs, void *str
  * Keys/values are read once per (sequence, KV head) for all G query heads;
  * long contexts are split over block ranges and merged by log-sum-exp in a
  * second kernel (two launches per call).  Batches with more sequences than
- * the GPU has SMs use partitions of at most 2048 tokens (environment
- * PA_PT_MAX=<tokens> overrides, 0 = no cap); the split never produces more
+ * the GPU has SMs use partitions of at most 2048 tokens (the pool's
+ * PA_OPT_PARTITION_CAP option overrides); the split never produces more
  * partials than the workspace holds.
- * Environment PA_DECODE_STREAM=1 selects, for bf16 pools with block_size 16,
- * head_dim 64 or 128, G <= 8 and S <= 4096, a one-launch stream-K split pass
- * (every warp an equal run of (sequence, head, block) tiles fed by TMA, pieces
- * of a sequence merged by the warp that finishes last); same results within
- * the bf16 tolerance.  The variable is read on every call.
  * Arithmetic: bf16 pools use bf16 tensor-core products with fp32
  * accumulation and fp32 softmax (the probabilities enter the value product
  * as a bf16 high part plus a bf16 low part); f32 pools use fp32 CUDA cores.
@@ -217,14 +241,14 @@ int pa_decode_reserve(pa_pool *pool, int max_seqs, int max_q_heads);
  *                       owns batch entries group_seqs[offsets[g] .. offsets[g+1])
  *   group_seqs          host int32: batch indices; each in at most one group
  *   group_shared_blocks host int32 [num_groups]: number of leading table
- *                       entries that are the same physical blocks for every
- *                       member and lie wholly inside every member's context
+ *                       entries that name one physical block in every
+ *                       member's table and lie wholly inside every member's context
  * For each group and KV head, tiles of up to 128 query rows (members x their
  * G heads) attend to 1024-token chunks of the shared span together on the
  * 5th-generation tensor cores (tcgen05: operands staged by TMA, accumulators
  * in tensor memory; bf16 pools with head_dim 128, block_size 16, G <= 8; other
- * tensor-core shapes use 64-row tiles on mma.sync, or PA_SHARED_MMA_SYNC=1 in
- * the environment selects those); each member's private suffix goes through
+ * tensor-core shapes use 64-row tiles on mma.sync, which the pool's
+ * PA_OPT_SHARED_KERNEL option also selects); each member's private suffix goes through
  * the ordinary split path, and the partials are merged by log-sum-exp.  Groups with fewer than two members
  * or no shared block are ignored; shapes outside the bf16 tensor-core path
  * (see pa_decode) fall back to pa_decode.  The device checks that members'
@@ -256,8 +280,14 @@ int pa_decode_shared(pa_pool *pool, const void *q, int num_seqs, int num_q_heads
  * GB300; when the array has less room than the partition cap would use, the
  * kernel takes longer partitions instead).
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture
- * begins.  All calls on a device share the one array, which keeps the last
+ * (cudaGetSymbolAddress, with that device current) and caches it.  Under lazy
+ * module loading (CUDA's default) that lookup is what loads the library's
+ * device code, so the 32 MiB are reserved during that first call: make it
+ * before the process's own allocator reserves the GPU's memory, and before
+ * any stream capture begins.  If the device has no room for it, the call
+ * returns PA_ERR_OUT_OF_MEMORY.  The cached address does not survive a
+ * cudaDeviceReset of that device: do not call this entry point on a device
+ * after resetting it.  All calls on a device share the one array, which keeps the last
  * call's contents: calls that overlap on the GPU (other streams, other pools,
  * other threads) race and give wrong results; serialise them. */
 int pa_decode_noalloc(pa_pool *pool, const void *q, int num_seqs, int num_q_heads,
@@ -267,8 +297,8 @@ int pa_decode_noalloc(pa_pool *pool, const void *q, int num_seqs, int num_q_head
 
 /* Paged prefill attention of one chunk of new tokens per sequence.  The pages
  * name the prefill step only through what a prefix-cache hit saves ([Z]
- * answer and [K] "Prefix Sharing Is a Natural Extension": "the prefill for that
- * span is skipped"); this library's reading: a chunk's keys and values are
+ * answer and [K] "Prefix Sharing Is a Natural Extension": a hit means that
+ * span needs no prefill); this library's reading: a chunk's keys and values are
  * appended first (pa_append_kv, the slots of positions L-n .. L-1), then chunk
  * token i of sequence s, at position L-n+i with L = context_lens[s] and
  * n = cu_seqlens_q[s+1] - cu_seqlens_q[s], attends to every cached key of s at
@@ -290,10 +320,13 @@ int pa_decode_noalloc(pa_pool *pool, const void *q, int num_seqs, int num_q_head
  * position through shared memory once for all its rows: 128 rows on the
  * tcgen05 tensor cores (TMA-staged keys/values, TMEM accumulators) for 16-token
  * blocks, head_dim 128 and a 16-byte-aligned out; 64 rows on mma.sync otherwise
- * (or when the environment sets PA_PREFILL_MMA_SYNC=1).  Positions past a
- * sequence's length in its last block must hold finite values (they do in any
- * pool written through this library with finite inputs): the tcgen05 form
- * multiplies them by zero probabilities.  On the device: a malformed cu_seqlens_q (decreasing, beyond T, a
+ * (or when the pool's PA_OPT_PREFILL_KERNEL option selects it).  Whatever
+ * bits a block holds at positions at or past the sequence's length (a block
+ * recycled from a finished request may hold anything, Inf and NaN included)
+ * never reach the output.  A non-finite key or value inside the chunk itself
+ * (a caller input) does reach the chunk's earlier rows, which weigh it by
+ * zero (0 * Inf is NaN), as it reaches every later row.
+ * On the device: a malformed cu_seqlens_q (decreasing, beyond T, a
  * chunk longer than its context or than max_q_len) records PA_ERR_INVALID_ARG,
  * a context beyond the table PA_ERR_BAD_LENGTH, a block id outside the pool
  * PA_ERR_BAD_BLOCK_ID; those sequences' rows are left unwritten. */
@@ -401,8 +434,8 @@ int pa_bm_is_cached(pa_bm *bm, int block);
 
 /* Retention of cached blocks after their last user leaves ([Z] follow-up on
  * how eviction interacts with the reference count, left unanswered there;
- * [K] "Prefix Reuse Also Needs Compatible Computation": systems decide "which
- * full blocks they retain for reuse").  Off by default (a freed block leaves
+ * [K] "Prefix Reuse Also Needs Compatible Computation": what a system keeps
+ * for later reuse is its own policy, over full blocks only).  Off by default (a freed block leaves
  * the hash table at once).  With on != 0:
  *   - a block still registered in the hash table whose count reaches zero
  *     stays registered and becomes evictable instead of joining the free

@@ -12,15 +12,15 @@ Plain Python lists and dicts for the host bookkeeping the pages describe:
 * copy-on-write — a write into a block that another request still points at
   allocates a fresh block, copies the old one, writes there and repoints only
   that entry of the writer's table (zenaique answer; kgptalkie "Shared Blocks
-  Must Not Be Changed in Place"; zenaique "Most common mistake": only a
-  divergent block is ever copied, and only that block);
+  Must Not Be Changed in Place"; zenaique "Most common mistake": the copy
+  is limited to the single block where the requests diverge);
 * parent-chained block hash and the hash -> physical block table — zenaique
-  answer ("a hash over its tokens chained with its parent block's hash"; a hit
-  reuses the cached block and skips that span's prefill), follow-up "Why must
-  the block hash chain the parent block's hash", "What besides token IDs must
-  enter the cache key" (here: a per-request salt), kgptalkie "Prefix reuse
-  also needs compatible computation" and "which full blocks they retain"
-  (only full blocks are hashed).
+  answer (each block's hash covers its own token ids and the hash of the
+  block before it; a hit reuses the cached block and saves that span's
+  prefill), its follow-ups on why the parent's hash is chained in and on what
+  else must enter the cache key (here: a per-request salt), and kgptalkie
+  "Prefix Reuse Also Needs Compatible Computation" (only full blocks are kept
+  for reuse, so only full blocks are hashed).
 
 Readings where the pages are silent (each listed in the design notes):
   - the free pool is a FIFO seeded with a caller-given order; freed blocks go
@@ -32,8 +32,8 @@ Readings where the pages are silent (each listed in the design notes):
     already registered the first registration stays;
   - a block leaves the hash table when its reference count reaches zero,
     unless retention is on.  Retention (the zenaique follow-up on how eviction
-    interacts with the reference count is left unanswered; kgptalkie says
-    systems decide "which full blocks they retain for reuse"): a registered
+    interacts with the reference count is left unanswered; kgptalkie leaves
+    what to keep for reuse to each system's policy): a registered
     block whose count reaches zero stays registered and evictable, in release
     order; a finished request releases its blocks last one first; a new block
     comes from the free pool while it has one, else the least recently

@@ -14,8 +14,9 @@
  *     decode query of each request scores every cached key of that request,
  *     found through its own block table in logical (token) order, applies
  *     softmax and mixes the matching values.  Paging changes only where the
- *     keys live, never the result ("The cache remains semantically the same";
- *     verification recipe under "A Tiny Block-Table Example").
+ *     keys live, never the result (the tutorial's verification recipe under
+ *     "A Tiny Block-Table Example": the output must not move when the
+ *     physical blocks do).
  *
  * Readings taken where the pages are silent:
  *   - grouped-query attention: query head h reads KV head h / (Hq / Hkv);

@@ -1,8 +1,8 @@
 """Paged prefill attention oracle (float64) — TEST INFRASTRUCTURE.
 
 kgptalkie "Day 28: PagedAttention / vLLM" and the zenaique prefix-sharing
-answer name the prefill step only through what a prefix-cache hit saves ("the
-prefill for that span is skipped"): a request's prompt tokens are processed
+answer name the prefill step only through what a prefix-cache hit saves (a
+hit means the cached span needs no prefill): a request's prompt tokens are processed
 before it decodes, and their keys and values fill its blocks.  This build's
 reading of one prefill chunk of a sequence (n new tokens, context length L
 after they are appended):

@@ -25,6 +25,7 @@ c_u8p = ctypes.POINTER(ctypes.c_uint8)
 c_intp = ctypes.POINTER(c_int)
 
 PA_F32, PA_BF16, PA_FP8E4M3 = 0, 1, 2
+PA_OPT_PARTITION_CAP, PA_OPT_SHARED_KERNEL, PA_OPT_PREFILL_KERNEL = 0, 1, 2
 
 ERRORS = {
     0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_DTYPE", -3: "PA_ERR_CUDA",
@@ -44,6 +45,8 @@ SIGNATURES = {
     "pa_pool_info": (c_int, [c_void_p, c_intp, c_intp, c_intp, c_intp, c_intp]),
     "pa_pool_set_kv_scales": (c_int, [c_void_p, c_float, c_float]),
     "pa_pool_kv_scales": (c_int, [c_void_p, ctypes.POINTER(c_float), ctypes.POINTER(c_float)]),
+    "pa_pool_set_option": (c_int, [c_void_p, c_int, c_int]),
+    "pa_pool_get_option": (c_int, [c_void_p, c_int, c_intp]),
     "pa_append_kv": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
     "pa_copy_blocks": (c_int, [c_void_p, c_void_p, c_int, c_void_p]),
     "pa_decode": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_void_p, c_float,

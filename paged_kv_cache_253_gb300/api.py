@@ -75,6 +75,22 @@ class KVPool:
                 "pa_pool_kv_scales")
         return k.value, v.value
 
+    OPTIONS = {"partition_cap": L.PA_OPT_PARTITION_CAP, "shared_kernel": L.PA_OPT_SHARED_KERNEL,
+               "prefill_kernel": L.PA_OPT_PREFILL_KERNEL}
+
+    def set_option(self, name, value):
+        """Kernel-choice option of this pool (pa_pool_set_option): partition_cap
+        (tokens; 0 none, -1 automatic), shared_kernel / prefill_kernel (0
+        tcgen05 where eligible, 1 mma.sync)."""
+        L.check(L.pa_pool_set_option(self.handle, self.OPTIONS[name], int(value)),
+                "pa_pool_set_option")
+
+    def get_option(self, name):
+        v = ctypes.c_int()
+        L.check(L.pa_pool_get_option(self.handle, self.OPTIONS[name], ctypes.byref(v)),
+                "pa_pool_get_option")
+        return v.value
+
     def close(self):
         if getattr(self, "handle", None):
             L.pa_pool_destroy(self.handle)

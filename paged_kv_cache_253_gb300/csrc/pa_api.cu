@@ -3,7 +3,6 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -39,9 +38,9 @@ struct DeviceGuard {
 size_t elem_size(pa_dtype t) { return pool_elem_size(t); }
 
 // Workspace: [header: ticket + schedule, 256-aligned][part_acc][part_ml]
-size_t workspace_bytes(const pa_detail::DecodePlan& plan, int S, int Hkv, int G, int D,
+size_t workspace_bytes(const pa_detail::DecodePlan& plan, int S, int G, int D,
                        size_t* counters_bytes) {
-    const size_t cb = decode_header_bytes(S, Hkv);
+    const size_t cb = decode_header_bytes(S);
     const size_t acc = round256(plan.max_items * G * D * sizeof(float));
     const size_t ml = round256(plan.max_items * G * 2 * sizeof(float));
     if (counters_bytes) *counters_bytes = cb;
@@ -196,6 +195,36 @@ int pa_pool_kv_scales(const pa_pool* pool, float* k_scale, float* v_scale) {
     return PA_OK;
 }
 
+int pa_pool_set_option(pa_pool* pool, pa_option option, int value) {
+    if (!pool) return PA_ERR_INVALID_ARG;
+    switch (option) {
+        case PA_OPT_PARTITION_CAP:
+            if (value < -1) return PA_ERR_INVALID_ARG;
+            pool->opt_partition_cap = value;
+            return PA_OK;
+        case PA_OPT_SHARED_KERNEL:
+            if (value != 0 && value != 1) return PA_ERR_INVALID_ARG;
+            pool->opt_shared_kernel = value;
+            return PA_OK;
+        case PA_OPT_PREFILL_KERNEL:
+            if (value != 0 && value != 1) return PA_ERR_INVALID_ARG;
+            pool->opt_prefill_kernel = value;
+            return PA_OK;
+        default:
+            return PA_ERR_INVALID_ARG;
+    }
+}
+
+int pa_pool_get_option(const pa_pool* pool, pa_option option, int* value) {
+    if (!pool || !value) return PA_ERR_INVALID_ARG;
+    switch (option) {
+        case PA_OPT_PARTITION_CAP: *value = pool->opt_partition_cap; return PA_OK;
+        case PA_OPT_SHARED_KERNEL: *value = pool->opt_shared_kernel; return PA_OK;
+        case PA_OPT_PREFILL_KERNEL: *value = pool->opt_prefill_kernel; return PA_OK;
+        default: return PA_ERR_INVALID_ARG;
+    }
+}
+
 int pa_append_kv(pa_pool* pool, const void* k, const void* v, const int64_t* slot_mapping,
                  int num_tokens, void* stream) {
     if (!pool || num_tokens < 0) return PA_ERR_INVALID_ARG;
@@ -218,9 +247,12 @@ int pa_copy_blocks(pa_pool* pool, const int64_t* pairs, int num_pairs, void* str
     return pa_detail::launch_copy(pool, pairs, num_pairs, static_cast<cudaStream_t>(stream));
 }
 
-static int check_decode_args(const pa_pool* pool, const void* q, int S, int Hq,
-                             const int32_t* tables, int max_blocks, const int32_t* lens,
-                             const void* out, pa_dtype out_dtype) {
+}  // extern "C"
+
+namespace pa_detail {
+
+int check_decode_args(const pa_pool* pool, const void* q, int S, int Hq, const int32_t* tables,
+                      int max_blocks, const int32_t* lens, const void* out, pa_dtype out_dtype) {
     if (!pool || S < 0 || Hq <= 0 || max_blocks < 0) return PA_ERR_INVALID_ARG;
     if (Hq % pool->kv_heads != 0 || Hq / pool->kv_heads > 16) return PA_ERR_UNSUPPORTED;
     if (out_dtype != PA_F32 && out_dtype != PA_BF16) return PA_ERR_DTYPE;
@@ -233,6 +265,10 @@ static int check_decode_args(const pa_pool* pool, const void* q, int S, int Hq,
     return PA_OK;
 }
 
+}  // namespace pa_detail
+
+extern "C" {
+
 int pa_decode_reserve(pa_pool* pool, int max_seqs, int max_q_heads) {
     if (!pool || max_seqs <= 0 || max_q_heads <= 0 || max_q_heads % pool->kv_heads)
         return PA_ERR_INVALID_ARG;
@@ -242,9 +278,8 @@ int pa_decode_reserve(pa_pool* pool, int max_seqs, int max_q_heads) {
     // the fp32 path's partial count grows with the table width; reserve for the fast path
     int rc = pa_detail::plan_decode(pool, max_seqs, max_q_heads, 1, &plan);
     if (rc != PA_OK) return rc;
-    return ensure_workspace(pool, workspace_bytes(plan, max_seqs, pool->kv_heads,
-                                                  max_q_heads / pool->kv_heads, pool->head_dim,
-                                                  nullptr));
+    return ensure_workspace(pool, workspace_bytes(plan, max_seqs, max_q_heads / pool->kv_heads,
+                                                  pool->head_dim, nullptr));
 }
 
 // Host plan of the shared-prefix items (see pa_decode_shared).
@@ -269,7 +304,7 @@ static int decode_impl(pa_pool* pool, const void* q, int num_seqs, int num_q_hea
                        const int32_t* block_tables, int max_blocks_per_seq,
                        const int32_t* context_lens, float scale, void* out, pa_dtype out_dtype,
                        void* stream, const SharedPlan* sh, const NewTokens* nt = nullptr) {
-    int rc = check_decode_args(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+    int rc = pa_detail::check_decode_args(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
                                context_lens, out, out_dtype);
     if (rc != PA_OK || num_seqs == 0) return rc;
     DeviceGuard g(pool->device);
@@ -289,7 +324,7 @@ static int decode_impl(pa_pool* pool, const void* q, int num_seqs, int num_q_hea
         plan.fuse = false;
     }
     size_t cb = 0;
-    size_t need = workspace_bytes(plan, num_seqs, pool->kv_heads, G, pool->head_dim, &cb);
+    size_t need = workspace_bytes(plan, num_seqs, G, pool->head_dim, &cb);
     const size_t sacc_off = need;
     const size_t sacc_bytes = sh ? round256(static_cast<size_t>(sh->slots) * pool->kv_heads * G *
                                             pool->head_dim * sizeof(float)) : 0;
@@ -343,7 +378,6 @@ static int decode_impl(pa_pool* pool, const void* q, int num_seqs, int num_q_hea
     p.out = out;
     p.ticket = static_cast<int*>(pool->ws);
     p.sched = p.ticket + 4;
-    p.unit_cnt = decode_unit_counters(p.ticket, num_seqs);
     p.part_acc = reinterpret_cast<float*>(static_cast<char*>(pool->ws) + cb);
     p.part_ml = reinterpret_cast<float*>(
         static_cast<char*>(pool->ws) + cb + round256(plan.max_items * G * pool->head_dim * sizeof(float)));
@@ -390,7 +424,7 @@ int pa_decode_shared(pa_pool* pool, const void* q, int num_seqs, int num_q_heads
                      const int32_t* context_lens, float scale, void* out, pa_dtype out_dtype,
                      const int32_t* group_seq_offsets, const int32_t* group_seqs,
                      const int32_t* group_shared_blocks, int num_groups, void* stream) {
-    int rc = check_decode_args(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+    int rc = pa_detail::check_decode_args(pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
                                context_lens, out, out_dtype);
     if (rc != PA_OK || num_seqs == 0) return rc;
     if (num_groups < 0 || (num_groups > 0 && (!group_seq_offsets || !group_seqs ||
@@ -420,10 +454,9 @@ int pa_decode_shared(pa_pool* pool, const void* q, int num_seqs, int num_q_heads
                            context_lens, scale, out, out_dtype, stream, nullptr);
     SharedPlan sh;
     sh.num_groups = static_cast<int>(keep.size());
-    // tcgen05 items take 128 query rows; the mma.sync variant 64 (PA_SHARED_MMA_SYNC=1
-    // in the environment selects it, for comparison)
-    const char* force_sync = std::getenv("PA_SHARED_MMA_SYNC");
-    sh.tc = pa_detail::shared_tc_eligible(pool, G) && !(force_sync && force_sync[0] == '1');
+    // tcgen05 items take 128 query rows; the mma.sync variant 64 (the pool's
+    // PA_OPT_SHARED_KERNEL option selects it)
+    sh.tc = pa_detail::shared_tc_eligible(pool, G) && pool->opt_shared_kernel == 0;
     sh.members_per_tile = std::max(1, (sh.tc ? pa_detail::shared_tc_rows() : 64) / G);
     // shared tokens per item: the tcgen05 kernel stages a 1024-token table slice,
     // the mma.sync variant one block id per lane (32 blocks)

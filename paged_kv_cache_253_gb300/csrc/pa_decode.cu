@@ -36,53 +36,23 @@
 #include <cfloat>
 #include <climits>
 #include <cmath>
-#include <cstdlib>
 #include <cstdint>
 #include <type_traits>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
-// Tuning knobs (compile-time; the defaults are the measured best on GB300).
-#ifndef PA_ITEMS_PER_CTA
-#define PA_ITEMS_PER_CTA 4      // target work items per resident CTA
-#endif
-#ifndef PA_PREFETCH
-#define PA_PREFETCH 0           // stream an item's K/V tiles into L2 when it starts
-#endif                          // (measured slower on GB300; kept as an option)
-#ifndef PA_DYNAMIC
-#define PA_DYNAMIC 1            // CTAs take items from a global counter, not round-robin
-#endif
-#ifndef PA_WARPS
-#define PA_WARPS 4              // warps per CTA sharing one item
-#endif
-#ifndef PA_MIN_CTAS
-#define PA_MIN_CTAS 3           // resident CTAs per SM the register budget aims at
-#endif
-#ifndef PA_PT_MAX_TOKENS
-#define PA_PT_MAX_TOKENS 2048    // partition cap in tokens for batches of many sequences
-#endif
-#ifndef PA_BLOCK_PREFETCH
-#define PA_BLOCK_PREFETCH 1     // L2 prefetch of the block a warp reads that many blocks ahead
-#endif
-#ifndef PA_STAGES
-#define PA_STAGES 0             // cp.async ring depth per warp (0/1: direct register loads)
-#endif
-
-#ifndef PA_SHARED_STAGES
-#define PA_SHARED_STAGES 8      // staged 16-token tiles per CTA for shared-prefix items
-#endif
-#ifndef PA_SHARED_UNITS_PER_SYNC
-#define PA_SHARED_UNITS_PER_SYNC 2
-#endif
-
+// Tuning constants (the measured best on GB300).
 namespace {
 
-constexpr int kWarps = PA_WARPS;
-constexpr int kPtMax = PA_PT_MAX_TOKENS;
+constexpr int kItemsPerCta = 4;         // target work items per resident CTA
+constexpr int kWarps = 4;               // warps per CTA sharing one item
+constexpr int kMinCtas = 3;             // resident CTAs per SM the register budget aims at
+constexpr int kPtMax = 2048;            // partition cap in tokens for batches of many sequences
+constexpr int kBlockPrefetch = 1;       // L2 prefetch of the block a warp reads this many blocks ahead
 constexpr int kGuideMinPT = 256;        // shortest partition of the guided tail, tokens
-constexpr int kSharedStages = PA_SHARED_STAGES;
-constexpr int kSharedUnitsPerSync = PA_SHARED_UNITS_PER_SYNC;
+constexpr int kSharedStages = 8;        // staged 16-token tiles per CTA for shared-prefix items
+constexpr int kSharedUnitsPerSync = 2;  // tiles consumed per barrier by shared-prefix items
 static_assert(kSharedStages > kSharedUnitsPerSync, "shared pipeline needs copies in flight");
 static_assert(kSharedUnitsPerSync % 2 == 0, "shared items consume 32-token tiles");
 constexpr int kThreads = kWarps * 32;
@@ -237,25 +207,18 @@ __device__ __forceinline__ int find_seq(const int* s_start, int S, int item) {
 // takes gridDim.x + (a global ticket), so CTAs that finish early keep working
 // and the launch ends about one item after the average CTA.  The ticket
 // counter lives in the workspace header.
-__device__ __forceinline__ int next_item(const DecodeParams& p, int item, int* s_next) {
-#if PA_DYNAMIC
+__device__ __forceinline__ int next_item(const DecodeParams& p, int* s_next) {
     if (threadIdx.x == 0) *s_next = static_cast<int>(gridDim.x) + atomicAdd(p.ticket, 1);
     __syncthreads();
     const int it = *s_next;
     __syncthreads();
     return it;
-#else
-    (void)p;
-    (void)s_next;
-    return item + static_cast<int>(gridDim.x);
-#endif
 }
 
 // The last CTA to stop resets the ticket counters for the next launch.  Every
 // other CTA has taken its last ticket before it counts itself out, so nothing
 // reads the counters after the reset.
 __device__ __forceinline__ void retire_cta(const DecodeParams& p) {
-#if PA_DYNAMIC
     if (threadIdx.x == 0) {
         __threadfence();
         if (atomicAdd(p.ticket + 1, 1) == static_cast<int>(gridDim.x) - 1) {
@@ -264,7 +227,6 @@ __device__ __forceinline__ void retire_cta(const DecodeParams& p) {
             __threadfence();
         }
     }
-#endif
 }
 
 // --------------------------------------------------------- item results ---
@@ -457,22 +419,18 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // The warp's share of one item: blocks lb0 + warp + kWarps*i of the
-// partition, each block cut into 16-token units.  With PA_STAGES > 1 every
-// unit's K tile (16 rows) and V^T tile (D rows of 16 tokens) are copied into
-// a per-warp ring of shared-memory stages with cp.async, PA_STAGES - 1 units
-// ahead of the unit being computed, so each warp keeps several tiles in
-// flight.  K rows are stored with 16-byte chunk c of odd rows at c ^ 4, which
-// makes the fragment reads below bank-conflict free.
+// partition, each block cut into 16-token units whose K and V^T fragments are
+// loaded straight from memory into registers.
 //
-// F8 (fp8 pool, direct loads only): the same fragments are read as e4m3
+// F8 (fp8 pool): the same fragments are read as e4m3
 // codes, half the bytes (8 per K chunk, 4 per V^T row piece), and widened to
 // f16 pairs in registers; the queries are re-rounded to f16 once per item.
 // BS > 0: the pool's block size is known to be BS at compile time (16-token
 // blocks: one 16-token tile per block, constant value-row strides).
 template <int D, bool FUSE, bool F8 = false, int BS = 0>
 __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, int tok0,
-                                          int tok1, int L, unsigned char* ring, float* sm_o,
-                                          float* sm_m, float* sm_l) {
+                                          int tok1, int L, float* sm_o, float* sm_m,
+                                          float* sm_l) {
     static_assert(!(F8 && FUSE), "an fp8 pool appends in its own (quantizing) kernel");
     constexpr int NJ = D / 32, NT = D / 16;
     constexpr int ES = F8 ? 1 : 2;        // bytes per pool element
@@ -505,81 +463,6 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
     const size_t tile_elems = static_cast<size_t>(B) * D;
     const int nblk = lb1 > lb0 + warp ? (lb1 - lb0 - warp + kWarps - 1) / kWarps : 0;
 
-#if PA_STAGES > 1
-    static_assert(!F8, "the staged ring holds bf16 tiles");
-    constexpr int S = PA_STAGES;
-    constexpr int UNIT = 64 * D;          // bytes per stage: K 16 x D + V^T D x 16, bf16
-    const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-    const int nunits = nblk * nsub;
-    int my_phys = -1;
-    unsigned valid = 0;                   // bit (u % S): stage holds unit u
-    auto issue = [&](int u) {
-        const int i = u / nsub, sub = u - i * nsub;
-        if (sub == 0 && (i & 31) == 0) {
-            const int mine = lb0 + warp + kWarps * (i + lane);
-            my_phys = mine < lb1 ? __ldg(table + mine) : -1;
-        }
-        const int phys = __shfl_sync(0xffffffffu, my_phys, i & 31);
-        const int lb = lb0 + warp + kWarps * i;
-        const int nv = L - (lb * B + sub * 16);
-        const int st = u % S;
-        valid &= ~(1u << st);
-        if (phys < 0 || phys >= p.num_blocks) {
-            if (lane == 0 && nv > 0) record_error(p.err, PA_ERR_BAD_BLOCK_ID);
-        } else if (nv > 0) {
-            const size_t tile = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems;
-            const uint16_t* kg = kpool + tile + static_cast<size_t>(sub) * 16 * D;
-            const uint16_t* vg = vpool + tile + sub * 16;
-            const uint32_t ks = ring_s + st * UNIT;
-            const uint32_t vs = ks + 32 * D;
-#pragma unroll
-            for (int q = lane; q < 2 * D; q += 32) {          // K: 16 rows x D/8 chunks
-                const int r = q / (D / 8), ch = q - r * (D / 8);
-                cp_async16(ks + r * (2 * D) + ((ch ^ ((r & 1) << 2)) << 4), kg + r * D + ch * 8);
-            }
-#pragma unroll
-            for (int q = lane; q < 2 * D; q += 32) {          // V^T: D rows x 2 chunks
-                const int d = q >> 1, half = q & 1;
-                cp_async16(vs + d * 32 + half * 16, vg + static_cast<size_t>(d) * B + half * 8);
-            }
-            valid |= 1u << st;
-        }
-        cp_async_commit();
-    };
-    for (int u = 0; u < S - 1; ++u) {
-        if (u < nunits) issue(u);
-        else cp_async_commit();
-    }
-    for (int u = 0; u < nunits; ++u) {
-        if (u + S - 1 < nunits) issue(u + S - 1);
-        else cp_async_commit();
-        cp_async_wait<S - 1>();
-        __syncwarp();
-        const int st = u % S;
-        const int i = u / nsub, sub = u - i * nsub;
-        const int nvalid = min(16, L - ((lb0 + warp + kWarps * i) * B + sub * 16));
-        if ((valid >> st) & 1u) {
-            const unsigned char* ks = ring + st * UNIT;
-            const unsigned char* vs = ks + 32 * D;
-            uint4 k0[NJ], k1[NJ];
-            uint2 v0[NT], v1[NT];
-#pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                const int ch = 4 * j + c;
-                k0[j] = *reinterpret_cast<const uint4*>(ks + r0 * (2 * D) + ((ch ^ ((r0 & 1) << 2)) << 4));
-                k1[j] = *reinterpret_cast<const uint4*>(ks + r1 * (2 * D) + ((ch ^ ((r1 & 1) << 2)) << 4));
-            }
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                v0[t] = *reinterpret_cast<const uint2*>(vs + (16 * t + g) * 32 + 8 * c);
-                v1[t] = *reinterpret_cast<const uint2*>(vs + (16 * t + g + 8) * 32 + 8 * c);
-            }
-            tile_update<D>(a, k0, k1, v0, v1, nvalid, sl, r0, r1, c);
-        }
-        __syncwarp();
-    }
-    cp_async_wait<0>();
-#else
     // Fused append: the warp that reads the block holding position L-1 first
     // writes the sequence's new token there (key row, value column), then
     // reads that block through L2 so it sees its own writes.
@@ -603,11 +486,10 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
                 my_phys = mine < lb1 ? __ldg(table + mine) : -1;
             }
             const int phys = __shfl_sync(0xffffffffu, my_phys, i & 31);
-#if PA_BLOCK_PREFETCH > 0
-            // start the block this warp reads PA_BLOCK_PREFETCH blocks from now
+            // start the block this warp reads kBlockPrefetch blocks from now
             // towards L2 (bulk prefetch: no registers, no shared memory)
-            if (i + PA_BLOCK_PREFETCH < nblk && (i & 31) + PA_BLOCK_PREFETCH < 32) {
-                const int pphys = __shfl_sync(0xffffffffu, my_phys, (i + PA_BLOCK_PREFETCH) & 31);
+            if (i + kBlockPrefetch < nblk && (i & 31) + kBlockPrefetch < 32) {
+                const int pphys = __shfl_sync(0xffffffffu, my_phys, (i + kBlockPrefetch) & 31);
                 if (lane == 0 && pphys >= 0 && pphys < p.num_blocks) {
                     const size_t ptile = (static_cast<size_t>(pphys) * p.Hkv + h) * tile_elems * ES;
                     pa_dev::prefetch_l2(static_cast<const char*>(p.k) + ptile,
@@ -616,7 +498,6 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
                                         static_cast<uint32_t>(tile_elems * ES));
                 }
             }
-#endif
             if (phys < 0 || phys >= p.num_blocks) {
                 if (lane == 0) record_error(p.err, PA_ERR_BAD_BLOCK_ID);
                 continue;
@@ -687,16 +568,14 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
                 my_phys = mine < lb1 ? __ldg(table + mine) : -1;
             }
             const int phys = __shfl_sync(0xffffffffu, my_phys, i & 31);
-#if PA_BLOCK_PREFETCH > 0
-            if (sub == 0 && i + PA_BLOCK_PREFETCH < nblk && (i & 31) + PA_BLOCK_PREFETCH < 32) {
-                const int pphys = __shfl_sync(0xffffffffu, my_phys, (i + PA_BLOCK_PREFETCH) & 31);
+            if (sub == 0 && i + kBlockPrefetch < nblk && (i & 31) + kBlockPrefetch < 32) {
+                const int pphys = __shfl_sync(0xffffffffu, my_phys, (i + kBlockPrefetch) & 31);
                 if (lane == 0 && pphys >= 0 && pphys < p.num_blocks) {
                     const size_t ptile = (static_cast<size_t>(pphys) * p.Hkv + h) * tile_elems;
                     pa_dev::prefetch_l2(kb + ptile, static_cast<uint32_t>(tile_elems));
                     pa_dev::prefetch_l2(vb + ptile, static_cast<uint32_t>(tile_elems));
                 }
             }
-#endif
             const int lb = lb0 + warp + kWarps * i;
             const int nv = min(16, L - (lb * B + sub * 16));
             r_valid = 0;
@@ -751,16 +630,12 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
         if (own_new) walk(std::true_type{});
         else walk(std::false_type{});
     }
-#endif
     float l0 = a.l0, l1 = a.l1;
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-#if PA_STAGES > 1
-    __syncthreads();                      // every warp is done with its ring: the merge buffer aliases it
-#endif
     float* mo = sm_o + warp * 8 * OS;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -1006,26 +881,21 @@ __device__ void shared_item(const DecodeParams& p, int grp, int h, int tile, int
     __syncthreads();                                // the stages are reused by the next item
 }
 
-// Bytes at the front of the fast kernel's shared memory: the cp.async rings
-// of all warps, which the merge buffer reuses between items.
-// (With shared-prefix items they also hold those items' staged tiles.)
+// Bytes at the front of the fast kernel's shared memory: the warps' merge
+// buffer, which shared-prefix items (mma.sync form) reuse for their staged tiles.
 __host__ __device__ constexpr size_t cmax(size_t a, size_t b) { return a > b ? a : b; }
 __host__ __device__ constexpr size_t fast_front_bytes(int D, bool shared) {
-    return cmax(cmax(PA_STAGES > 1 ? static_cast<size_t>(kWarps) * PA_STAGES * 64 * D : 0,
-                     static_cast<size_t>(kWarps) * 8 * (D + 4) * 4),
+    return cmax(static_cast<size_t>(kWarps) * 8 * (D + 4) * 4,
                 shared ? static_cast<size_t>(kSharedStages) * 64 * D : 0);
 }
 
-__device__ __forceinline__ size_t warp_ring_offset(int D) {
-    return static_cast<size_t>(threadIdx.x >> 5) * PA_STAGES * 64 * D;
-}
 
 template <int D, bool SHARED, bool FUSE, bool F8 = false>
-__global__ void __launch_bounds__(kThreads, SHARED ? 2 : PA_MIN_CTAS)
+__global__ void __launch_bounds__(kThreads, SHARED ? 2 : kMinCtas)
 decode_fast_kernel(const DecodeParams p) {
     constexpr int OS = D + 4;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    // [ring | merge buffer (aliases the ring when there is one)][m, l, ...][s_start]
+    // [merge buffer | shared-prefix stages][m, l, ...][s_start]
     unsigned char* ring = smem_raw;
     float* sm_o = reinterpret_cast<float*>(smem_raw);        // [kWarps][8][OS]
     float* sm_m = reinterpret_cast<float*>(smem_raw + fast_front_bytes(D, SHARED));  // [kWarps][8]
@@ -1040,7 +910,7 @@ decode_fast_kernel(const DecodeParams p) {
     const Sched sc = build_schedule(p, s_start, s_red);
     publish_schedule(p, sc, s_start);
     const int n_sh = SHARED ? p.n_shared_items : 0;
-    for (int item = blockIdx.x; item < n_sh + sc.total_items; item = next_item(p, item, s_flag + 1)) {
+    for (int item = blockIdx.x; item < n_sh + sc.total_items; item = next_item(p, s_flag + 1)) {
         if (SHARED && item < n_sh) {
             const int k = item / p.Hkv, hh = item - k * p.Hkv;
             shared_item<D>(p, p.sh_items[4 * k], hh, p.sh_items[4 * k + 1], p.sh_items[4 * k + 2],
@@ -1060,9 +930,9 @@ decode_fast_kernel(const DecodeParams p) {
         // instructions, 5 % faster); the bf16 walk, bound by load latency, ran
         // 1.5 us slower with it on the decode batch (measured on GB300)
         if (F8 && p.B == 16)
-            fast_item<D, FUSE, F8, 16>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
+            fast_item<D, FUSE, F8, 16>(p, s, h, tok0, tok1, L, sm_o, sm_m, sm_l);
         else
-            fast_item<D, FUSE, F8>(p, s, h, tok0, tok1, L, ring + warp_ring_offset(D), sm_o, sm_m, sm_l);
+            fast_item<D, FUSE, F8>(p, s, h, tok0, tok1, L, sm_o, sm_m, sm_l);
         __syncthreads();
         // merge the warps' softmax states (in place into warp 0's buffer)
         for (int idx = threadIdx.x; idx < p.G * D; idx += kThreads) {
@@ -1137,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(const DecodePar
     pa_dev::wait_prior_grid();
     const Sched sched = build_schedule(p, s_start, s_red);
     publish_schedule(p, sched, s_start);
-    for (int item = blockIdx.x; item < sched.total_items; item = next_item(p, item, s_flag + 1)) {
+    for (int item = blockIdx.x; item < sched.total_items; item = next_item(p, s_flag + 1)) {
         const int s = find_seq(s_start, p.S, item);
         const int local = item - s_start[s];
         const int part = local / p.Hkv, h = local - part * p.Hkv;
@@ -1309,13 +1179,11 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
     const int G = Hq / Hkv;
     const bool fp8 = pool->dtype == PA_FP8E4M3;
     const bool tc_shape = (D == 64 || D == 128 || D == 256) && B % 16 == 0 && G <= 8;
-    const bool fast = tc_shape && (pool->dtype == PA_BF16 || (fp8 && PA_STAGES <= 1));
+    const bool fast = tc_shape && (pool->dtype == PA_BF16 || fp8);
     if (fp8) {                  // appends quantize in their own kernel; no shared-prefix items
         plan->fuse = false;
         plan->shared = plan->tc = false;
     }
-    if (!plan->shared && fast && !fp8 && plan_stream(pool, S, Hq, max_blocks, plan)) return PA_OK;
-    plan->stream = false;
     plan->fast = fast;
     plan->pool = pool;
     plan->bf16 = pool->dtype == PA_BF16;
@@ -1330,20 +1198,18 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
         // of uneven sizes; partitions of at most kPtMax tokens then shorten the
         // launch's tail (measured on GB300: mixed lengths 473 -> 455 us; a few
         // long sequences, already many equal items, are better uncapped).
-        // PA_PT_MAX overrides the choice (0: no cap).
-        int pt_max = S > pool->num_sms ? kPtMax : 0;
-        if (const char* e = std::getenv("PA_PT_MAX")) pt_max = std::atoi(e);
+        // The pool's PA_OPT_PARTITION_CAP option overrides the choice (0: no cap).
+        const int pt_max = pool->opt_partition_cap >= 0 ? pool->opt_partition_cap
+                                                         : (S > pool->num_sms ? kPtMax : 0);
         plan->pt_max = pt_max > 0 ? std::max(plan->pt_min, pt_max / B * B) : 0;
         if (plan->shared && !plan->tc) {
             if (D == 64) occ = occupancy(decode_fast_kernel<64, true, false>, plan->smem);
             else if (D == 128) occ = occupancy(decode_fast_kernel<128, true, false>, plan->smem);
             else occ = occupancy(decode_fast_kernel<256, true, false>, plan->smem);
         } else if (fp8) {
-#if PA_STAGES <= 1
             if (D == 64) occ = occupancy(decode_fast_kernel<64, false, false, true>, plan->smem);
             else if (D == 128) occ = occupancy(decode_fast_kernel<128, false, false, true>, plan->smem);
             else occ = occupancy(decode_fast_kernel<256, false, false, true>, plan->smem);
-#endif
         } else if (plan->fuse) {
             if (D == 64) occ = occupancy(decode_fast_kernel<64, false, true>, plan->smem);
             else if (D == 128) occ = occupancy(decode_fast_kernel<128, false, true>, plan->smem);
@@ -1365,7 +1231,7 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
     if (occ <= 0) return PA_ERR_UNSUPPORTED;
     plan->grid = pool->num_sms * occ;
     if (fast) {
-        plan->items_target = plan->grid * PA_ITEMS_PER_CTA;
+        plan->items_target = plan->grid * kItemsPerCta;
         // items <= Hkv * (total / PT + S); PT >= total * Hkv / items_target keeps
         // that below min_items.  The extra items_target of room lets the
         // partition cap and the guided tail take effect; the kernel never
@@ -1390,7 +1256,6 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
     p.pt_max = plan.pt_max;
     p.max_items = static_cast<int>(std::min<size_t>(plan.max_items, 1u << 30));
     p.pt_fixed = plan.pt_fixed;
-    if (plan.stream) return launch_stream(plan, p, st);
     const dim3 grid(plan.grid), block(plan.threads);
     cudaError_t e;
     if (plan.fast && plan.shared && plan.tc) {
@@ -1408,13 +1273,9 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, true, false>, grid, block, plan.smem, st, p);
         else e = launch_pdl(decode_fast_kernel<256, true, false>, grid, block, plan.smem, st, p);
     } else if (plan.fast && plan.fp8) {
-#if PA_STAGES <= 1
         if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, false, true>, grid, block, plan.smem, st, p);
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, false, true>, grid, block, plan.smem, st, p);
         else e = launch_pdl(decode_fast_kernel<256, false, false, true>, grid, block, plan.smem, st, p);
-#else
-        e = cudaErrorNotSupported;
-#endif
     } else if (plan.fast && plan.fuse) {
         if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, true>, grid, block, plan.smem, st, p);
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, true>, grid, block, plan.smem, st, p);

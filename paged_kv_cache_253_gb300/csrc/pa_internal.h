@@ -28,9 +28,11 @@ struct pa_pool {
     // (boxes 16 tokens x 128 d, 32-byte swizzle), made on first use
     CUtensorMap kmap;
     CUtensorMap vmap;
-    // V^T again as 128-byte lines (4 d rows of 16 tokens; boxes of D/4 lines, 128-byte swizzle)
-    CUtensorMap vmap_lines;
     bool tmaps_ready = false;
+    // kernel-choice options (pa_pool_set_option)
+    int opt_partition_cap = -1;     // decode partition cap, tokens; -1 automatic, 0 none
+    int opt_shared_kernel = 0;      // 0 tcgen05 where eligible, 1 mma.sync
+    int opt_prefill_kernel = 0;     // 0 tcgen05 where eligible, 1 mma.sync
     // shared-prefix descriptor last uploaded by pa_decode_shared (host copy + device copy)
     std::vector<int> desc_host;
     int* desc_dev = nullptr;
@@ -49,7 +51,6 @@ struct DecodeParams {
     float* part_ml;             // [max_items][G][2]  (running max, sum) in log2 units
     int* ticket;                // [2] work ticket and retired-CTA count, zero between launches
     int* sched;                 // [S + 3] PT, item count, first item of each sequence
-    int* unit_cnt;              // [S * Hkv] pieces of each unit finished (stream-K), zero between launches
     int* err;
     float scale_log2;           // scale * log2(e) (* k_scale for an fp8 pool)
     float v_scale;              // factor on the value sums (fp8 pool's v_scale, else 1)
@@ -84,9 +85,6 @@ struct DecodeParams {
     // waited for the work before it; the split kernel then runs alongside it and
     // waits for it only before exiting (so the merge after it sees both).
     int defer_wait;
-    // Stream-K split pass (pa_decode_stream.cu): ring stages per warp, bytes per stage.
-    int sk_stages;
-    int sk_stage_bytes;
 };
 
 // Everything one prefill launch needs (pa_prefill), passed by value.
@@ -118,12 +116,11 @@ inline void decode_scales(const pa_pool* pool, float scale, DecodeParams* p) {
 }
 
 // Decode workspace header: ticket[2], 2 spare ints, the published schedule
-// (S + 3 ints used of S + 4), then one arrival counter per (sequence, KV head)
-// unit; zeroed before first use (the kernels reset what they count).
-inline size_t decode_header_bytes(int S, int Hkv) {
-    return ((static_cast<size_t>(S) + 8 + static_cast<size_t>(S) * Hkv) * sizeof(int) + 255) / 256 * 256;
+// (S + 3 ints used of S + 4); zeroed before first use (the kernels reset the
+// tickets they count).
+inline size_t decode_header_bytes(int S) {
+    return ((static_cast<size_t>(S) + 8) * sizeof(int) + 255) / 256 * 256;
 }
-inline int* decode_unit_counters(int* header, int S) { return header + S + 8; }
 
 namespace pa_detail {
 
@@ -157,8 +154,6 @@ struct DecodePlan {
     bool shared = false;        // shared-prefix items present (fast path only)
     bool fuse = false;          // the decode kernel also appends each sequence's new token
     bool tc = false;            // shared items run in the tcgen05 kernel before the split pass
-    bool stream = false;        // stream-K split pass with TMA-fed per-warp rings
-    int sk_stages = 0, sk_stage_bytes = 0;
     pa_pool* pool = nullptr;
     bool fast;                  // tensor-core path (bf16 pool, or fp8 codes widened to f16)
     bool bf16;                  // pool element type is bf16
@@ -170,15 +165,13 @@ struct DecodePlan {
     size_t min_items;           // fewest partial slots the kernel can work with (fast path)
 };
 int plan_decode(pa_pool* p, int S, int Hq, int max_blocks, DecodePlan* plan);
+// Host checks of pa_decode's arguments (shared by every decode entry point).
+int check_decode_args(const pa_pool* pool, const void* q, int S, int Hq, const int32_t* tables,
+                      int max_blocks, const int32_t* lens, const void* out, pa_dtype out_dtype);
 int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t st);
 
 // TMA descriptors of the pool's K and V^T (16-token blocks), made once per pool.
 int ensure_tensor_maps(pa_pool* pool);
-
-// Stream-K split pass (pa_decode_stream.cu): fills `plan` and returns true when
-// the pool and batch suit it (bf16, 16-token blocks, head_dim 64/128/256, G <= 8).
-bool plan_stream(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan);
-int launch_stream(const DecodePlan& plan, const DecodeParams& p, cudaStream_t st);
 
 // tcgen05 shared-prefix items (pa_shared_tc.cu).
 bool shared_tc_eligible(const pa_pool* pool, int G);

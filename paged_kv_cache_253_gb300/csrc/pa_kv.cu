@@ -3,7 +3,7 @@
 // append: each new token's keys and values go to its (physical block,
 // offset) slot (kgptalkie "Day 28: PagedAttention / vLLM", "Follow One Token
 // Address", "Growth Needs Only Another Free Block"; zenaique prefix-sharing
-// answer: the new token "is written there").
+// answer: the new token's data goes into its request's slot).
 // copy:   copy-on-write duplicates a whole shared block before the diverging
 // write (kgptalkie "Shared Blocks Must Not Be Changed in Place"; zenaique
 // "Most common mistake": only the divergent block is copied).

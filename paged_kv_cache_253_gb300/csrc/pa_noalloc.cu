@@ -10,11 +10,15 @@
 // same decode kernel with its scratch in a fixed array that is part of the
 // library image itself, so the call never allocates.
 //
-// The array is a file-scope __device__ object: every GPU that loads this
-// library holds its kScratchBytes until the process exits.  Host code cannot
-// use the array's name as a device address; the address is looked up once per
-// device with cudaGetSymbolAddress (on the first call made on that device) and
-// cached.
+// The array is a file-scope __device__ object.  Host code cannot use the
+// array's name as a device address; the address is looked up once per device
+// with cudaGetSymbolAddress (on the first call made on that device, with that
+// device current) and cached.  Under lazy module loading (the CUDA default)
+// that lookup is also what loads this library's device code onto the device,
+// so the array's kScratchBytes are reserved then, on the first call on each
+// device, and held until the process exits.  A cudaDeviceReset of the device
+// unloads the module: the cached address is then stale and the process must
+// not call this entry point on that device again.
 #include <cstdint>
 #include <mutex>
 
@@ -45,7 +49,8 @@ int scratch_address(int device, void** out) {
         const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
         if (e != cudaSuccess || !p) {
             cudaGetLastError();
-            return PA_ERR_CUDA;
+            // loading the module (and the array with it) needs device memory
+            return e == cudaErrorMemoryAllocation ? PA_ERR_OUT_OF_MEMORY : PA_ERR_CUDA;
         }
         g_scratch_ptr[device] = p;
     }
@@ -59,18 +64,10 @@ extern "C" int pa_decode_noalloc(pa_pool* pool, const void* q, int num_seqs, int
                                  const int32_t* block_tables, int max_blocks_per_seq,
                                  const int32_t* context_lens, float scale, void* out,
                                  pa_dtype out_dtype, void* stream) {
-    if (!pool || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0)
-        return PA_ERR_INVALID_ARG;
-    if (num_q_heads % pool->kv_heads != 0 || num_q_heads / pool->kv_heads > 16)
-        return PA_ERR_UNSUPPORTED;
-    if (out_dtype != PA_F32 && out_dtype != PA_BF16) return PA_ERR_DTYPE;
-    if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return PA_OK;
-    if (!q || !block_tables || !context_lens || !out || max_blocks_per_seq == 0)
-        return PA_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(q) % 16 != 0) return PA_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(max_blocks_per_seq) * pool->block_size > (int64_t{1} << 30))
-        return PA_ERR_UNSUPPORTED;
+    // the same argument rules as pa_decode
+    const int arc = pa_detail::check_decode_args(pool, q, num_seqs, num_q_heads, block_tables,
+                                                 max_blocks_per_seq, context_lens, out, out_dtype);
+    if (arc != PA_OK || num_seqs == 0) return arc;
 
     int prev = -1;
     if (cudaGetDevice(&prev) != cudaSuccess) return PA_ERR_CUDA;
@@ -85,7 +82,7 @@ extern "C" int pa_decode_noalloc(pa_pool* pool, const void* q, int num_seqs, int
     pa_detail::DecodePlan plan;
     int rc = pa_detail::plan_decode(pool, num_seqs, num_q_heads, max_blocks_per_seq, &plan);
     if (rc != PA_OK) return rc;
-    const size_t counters = decode_header_bytes(num_seqs, Hkv);
+    const size_t counters = decode_header_bytes(num_seqs);
     // partial slots: as many as the plan asks for, or as fit in the array (the
     // kernel lengthens its partitions to stay within what it is given)
     const size_t per_item = static_cast<size_t>(G) * (D + 2) * sizeof(float);
@@ -100,8 +97,7 @@ extern "C" int pa_decode_noalloc(pa_pool* pool, const void* q, int num_seqs, int
     rc = scratch_address(pool->device, &base);
     if (rc != PA_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // the work ticket and unit counters must start at zero; the array keeps the
-    // previous call's bytes
+    // the work tickets must start at zero; the array keeps the previous call's bytes
     if (cudaMemsetAsync(base, 0, counters, st) != cudaSuccess) return PA_ERR_CUDA;
 
     DecodeParams p{};
@@ -113,7 +109,6 @@ extern "C" int pa_decode_noalloc(pa_pool* pool, const void* q, int num_seqs, int
     p.out = out;
     p.ticket = static_cast<int*>(base);
     p.sched = p.ticket + 4;
-    p.unit_cnt = decode_unit_counters(p.ticket, num_seqs);
     p.part_acc = reinterpret_cast<float*>(static_cast<char*>(base) + counters);
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(base) + counters + acc);
     p.err = pool->err;

@@ -2,8 +2,8 @@
 // attend, through the sequence's block table, to the cached prefix and to the
 // chunk causally up to themselves (kgptalkie "Day 28: PagedAttention / vLLM",
 // "Prefix Sharing Is a Natural Extension" and the zenaique prefix-sharing
-// answer name the step through what a cache hit saves: "the prefill for that
-// span is skipped").  The chunk's keys and values are appended before the
+// answer name the step through what a cache hit saves: the cached span needs
+// no prefill).  The chunk's keys and values are appended before the
 // call (pa_append_kv), so chunk token i of a sequence with context length L
 // after the append sits at position L-n+i and sees keys 0 .. L-n+i.
 //
@@ -17,7 +17,6 @@
 // causal and length masks, online softmax per row, O += P V with P as a bf16
 // high + low pair.  Each row's normalised output is written directly.
 #include <cstdint>
-#include <cstdlib>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -331,11 +330,10 @@ extern "C" int pa_prefill(pa_pool* pool, const void* q, int num_tokens, int num_
     p.out_bf16 = out_dtype == PA_BF16;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // tcgen05 form (128 rows per CTA, TMA-staged K/V^T) where the pool's TMA
-    // views apply; PA_PREFILL_MMA_SYNC=1 in the environment selects the
-    // mma.sync form instead (for comparison)
-    const char* force_sync = std::getenv("PA_PREFILL_MMA_SYNC");
+    // views apply; the pool's PA_OPT_PREFILL_KERNEL option selects the
+    // mma.sync form instead
     if (pa_detail::prefill_tc_eligible(pool) && reinterpret_cast<uintptr_t>(out) % 16 == 0 &&
-        !(force_sync && force_sync[0] == '1')) {
+        pool->opt_prefill_kernel == 0) {
         const int rows = pa_detail::prefill_tc_rows();
         const dim3 tgrid(static_cast<unsigned>((static_cast<int64_t>(max_q_len) * G + rows - 1) / rows),
                          static_cast<unsigned>(Hkv), static_cast<unsigned>(num_seqs));

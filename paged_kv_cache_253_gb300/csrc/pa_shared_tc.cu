@@ -15,8 +15,10 @@
 //                 maximum grows by more than 2^8 (then O is rescaled in TMEM)
 //   O[128 x 128] += P[128 x 64] . V[64 x 128]    tcgen05.mma, fp32 in TMEM cols [128,256),
 //                 P entering as a bf16 high part plus a bf16 low part
-// Q, K (64 tokens x 128 d) and V^T (128 d x 64 tokens) are staged with cp.async
-// into 128-byte-swizzled K-major shared-memory tiles (two K/V stages); P goes
+// Q is staged with cp.async, K (64 tokens x 128 d) and V^T (128 d x 64 tokens)
+// by TMA, into swizzled K-major shared-memory tiles (two K/V stages); value
+// columns that get zero weight (block slots a step did not load) are zeroed
+// before the value product, so stale non-finite bits never reach it; P goes
 // from registers to TMEM (tcgen05.st) and feeds the value product from there, so
 // a CTA needs ~99 KB of shared memory and two fit on an SM; one thread
 // issues the MMAs and commits them to an mbarrier that the others wait on
@@ -82,11 +84,6 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         pa_tc::mbar_init(bar_full + 1, 1);
         pa_tc::mbar_init_fence();
     }
-    // Stages start zeroed: a step past the span's end leaves some block slots
-    // unloaded, and their (zero-probability) values must be finite.
-    for (uint32_t o = tid * 16; o < 2 * kStageBytes; o += kThreads * 16)
-        *reinterpret_cast<uint4*>(base + kStageOff + o) = make_uint4(0u, 0u, 0u, 0u);
-    pa_tc::fence_smem_to_async();
     if (warp == 0) pa_tc::tmem_alloc<kTmemCols>(tslot);
     pa_tc::fence_before_sync();
     __syncthreads();
@@ -200,6 +197,18 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                 if (st) ph_full1 ^= 1u; else ph_full0 ^= 1u;
                 if (!__syncthreads_and(w)) { ok = false; break; }
             }
+            // Block slots this step did not load (past the span's end, or a
+            // block id outside the pool) hold what an earlier step left there.
+            // Their scores are masked below, but a zero-weight value still
+            // enters P.V and 0 * Inf or 0 * NaN is NaN: zero their V^T rows
+            // (thread t clears row t of each such slot).
+            int loaded = 0;                                // bit b: block slot b holds this step's keys
+#pragma unroll
+            for (int b = 0; b < kStep / 16; ++b) {
+                const int rel = j * kStep + 16 * b;
+                if (t0 + rel < t1 && s_tbl[rel >> 4] >= 0) loaded |= 1 << b;
+                else pa_tc::zero_vt_row_tail(base + kStageOff + st * kStageBytes + 16384 + b * 4096, tid, 0);
+            }
             pa_tc::fence_smem_to_async();
             pa_tc::fence_before_sync();
             __syncthreads();
@@ -232,11 +241,10 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                     s[32 + i] = b32[i];
                 }
             }
-            const int nvalid = min(kStep, t1 - (t0 + j * kStep));
             float mx = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-                s[i] = i < nvalid ? s[i] * sl : -INFINITY;
+                s[i] = (loaded >> (i >> 4)) & 1 ? s[i] * sl : -INFINITY;
                 mx = fmaxf(mx, s[i]);
             }
             // raise the reference maximum only when it is far behind (or unset)
@@ -385,10 +393,6 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
         pa_tc::mbar_init(bar_full + 1, 1);
         pa_tc::mbar_init_fence();
     }
-    // zeroed stages: block slots a step leaves unloaded must hold finite values
-    for (uint32_t o = tid * 16; o < 2 * kStageBytes; o += kThreads * 16)
-        *reinterpret_cast<uint4*>(base + kStageOff + o) = make_uint4(0u, 0u, 0u, 0u);
-    pa_tc::fence_smem_to_async();
     if (warp == 0) pa_tc::tmem_alloc<kTmemCols>(tslot);
     pa_tc::fence_before_sync();
     __syncthreads();
@@ -464,6 +468,35 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
             if (st) ph_full1 ^= 1u; else ph_full0 ^= 1u;
             if (!__syncthreads_and(w)) { ok = false; break; }
         }
+        // Keys that no row of the tile may weigh: block slots this step did not
+        // load (past the tile's last key, or a block id outside the pool),
+        // which hold what an earlier step left there, and positions at or past
+        // the context length in the sequence's last block, which hold whatever
+        // the block held before.  Their scores are masked below, but a
+        // zero-weight value still enters P.V and 0 * Inf or 0 * NaN is NaN:
+        // zero those V^T columns (thread t clears row t of each tile).
+        const int kbase = j * kStep;
+        int skip = 0;                                      // bit b: block slot b not loaded
+#pragma unroll
+        for (int b = 0; b < kStep / 16; ++b) {
+            const int tok = kbase + 16 * b;
+            int zero_from = 16;
+            if (tok >= kv_end) {
+                skip |= 1 << b;
+                zero_from = 0;
+            } else {
+                const int x = __ldg(table + (tok >> 4));
+                if (x < 0 || x >= p.num_blocks) {
+                    skip |= 1 << b;
+                    zero_from = 0;
+                } else if (tok + 16 > L) {
+                    zero_from = L - tok;
+                }
+            }
+            if (zero_from < 16)
+                pa_tc::zero_vt_row_tail(base + kStageOff + st * kStageBytes + 16384 + b * 4096, tid,
+                                        zero_from);
+        }
         pa_tc::fence_smem_to_async();
         pa_tc::fence_before_sync();
         __syncthreads();
@@ -507,15 +540,6 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
         // causal mask: key j*64 + i is visible to this row iff it is at or
         // before the row's position (pos < kv_end, so this also ends the keys);
         // a block whose id is outside the pool was not loaded and is skipped
-        const int kbase = j * kStep;
-        int skip = 0;
-#pragma unroll
-        for (int b = 0; b < kStep / 16; ++b) {
-            if (kbase + 16 * b < kv_end) {
-                const int x = __ldg(table + (kbase >> 4) + b);
-                if (x < 0 || x >= p.num_blocks) skip |= 1 << b;
-            }
-        }
         float mx = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
@@ -646,9 +670,7 @@ bool shared_tc_eligible(const pa_pool* pool, int G) {
 
 // TMA descriptors over the pool (16-token blocks): K as
 // [num_blocks*Hkv*16 rows][D] with 64 x 16 boxes (128-byte swizzle); V^T as
-// [num_blocks*Hkv*D rows][16 tokens] with 16 x D boxes (32-byte swizzle), and
-// the same V^T as [num_blocks*Hkv*D/4 lines][64] with 64 x D/4 boxes
-// (128-byte swizzle: a tile moves as D/4 lines of 128 bytes).
+// [num_blocks*Hkv*D rows][16 tokens] with 16 x D boxes (32-byte swizzle).
 int ensure_tensor_maps(pa_pool* pool) {
     if (pool->tmaps_ready) return PA_OK;
     const int D = pool->head_dim;
@@ -675,13 +697,6 @@ int ensure_tensor_maps(pa_pool* pool) {
         return PA_ERR_CUDA;
     if (encode(&pool->vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool->v, vdim, vstr, vbox, one,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return PA_ERR_CUDA;
-    const cuuint64_t ldim[2] = {64, static_cast<cuuint64_t>(pool->num_blocks) * pool->kv_heads * D / 4};
-    const cuuint64_t lstr[1] = {128};
-    const cuuint32_t lbox[2] = {64, static_cast<cuuint32_t>(D / 4)};
-    if (encode(&pool->vmap_lines, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool->v, ldim, lstr, lbox, one,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return PA_ERR_CUDA;
     pool->tmaps_ready = true;

@@ -205,6 +205,22 @@ __device__ __forceinline__ void cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Zero tokens [t_from, 16) of row `d` of a V^T tile (rows of 16 bf16 tokens,
+// 32 bytes each) stored in the 32-byte swizzle: row d starts at d * 32 bytes
+// and its two 16-byte halves trade places when bit 2 of d is set.  The tile
+// starts on a 256-byte boundary.
+__device__ __forceinline__ void zero_vt_row_tail(unsigned char* tile, int d, int t_from) {
+    unsigned char* row = tile + d * 32;
+    const int flip = (d >> 2) & 1;
+    if (t_from <= 0) {
+        *reinterpret_cast<uint4*>(row) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(row + 16) = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    for (int t = t_from; t < 16; ++t)
+        *reinterpret_cast<uint16_t*>(row + ((((t >> 3) ^ flip)) << 4) + (t & 7) * 2) = 0;
+}
+
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled region.
 __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
     return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));

@@ -12,6 +12,7 @@ batch entry, with any copy-on-write pairs) and uploads the step's inputs.
 calls on the current stream.
 """
 from dataclasses import dataclass
+import time
 
 import numpy as np
 import torch
@@ -123,6 +124,7 @@ class DecodeStep:
     out: torch.Tensor
     groups: tuple = None           # (offsets, seqs, shared_blocks): decode with shared reads
     fused: bool = True             # append inside the decode kernel when there is no sharing
+    host_ms: float = 0.0           # host block-manager time of the step (slots, tables, groups)
 
     @property
     def num_pairs(self):
@@ -176,12 +178,14 @@ def prepare_step(wl, values, pool, bm, out_dtype=torch.float32, shared="auto", f
     reads (below that, L2 already absorbs the repeated reads and the plain
     kernel's higher occupancy wins, as measured on the mixed workload)."""
     dev = pool.device
+    t0 = time.perf_counter()
     slots, pairs = bm.append_slots(wl.batch, wl.step_tokens)
     tables, lens = bm.batch_tables(wl.batch)
     groups = bm.prefix_groups(wl.batch) if shared else None
     if shared == "auto" and groups is not None and \
             shared_fraction(groups, lens, wl.block_size) < SHARED_MIN_FRACTION:
         groups = None
+    host_ms = (time.perf_counter() - t0) * 1e3
     S = wl.num_seqs
     return DecodeStep(
         pool=pool,
@@ -194,7 +198,7 @@ def prepare_step(wl, values, pool, bm, out_dtype=torch.float32, shared="auto", f
         context_lens=torch.as_tensor(lens, device=dev),
         scale=wl.scale,
         out=torch.empty((S, wl.num_q_heads, wl.head_dim), dtype=out_dtype, device=dev),
-        groups=groups, fused=fused)
+        groups=groups, fused=fused, host_ms=host_ms)
 
 
 @dataclass
@@ -212,6 +216,7 @@ class PrefillStep:
     context_lens: torch.Tensor     # int32 [S], after the chunk's append
     scale: float
     out: torch.Tensor              # [T, Hq, D]
+    host_ms: float = 0.0           # host block-manager time of the step (slots, tables)
 
     @property
     def num_pairs(self):
@@ -240,9 +245,11 @@ def prepare_prefill(wl, values, pool, bm, out_dtype=torch.float32):
     """Reserve the slots of every chunk token (entry after entry, each entry's
     tokens in order) and upload the step's inputs."""
     dev = pool.device
+    t0 = time.perf_counter()
     reqs = np.repeat(np.asarray(wl.batch, dtype=np.int32), wl.chunk_lens)
     slots, pairs = bm.append_slots(reqs, wl.step_tokens)
     tables, lens = bm.batch_tables(wl.batch)
+    host_ms = (time.perf_counter() - t0) * 1e3
     cu = np.zeros(len(wl.chunk_lens) + 1, dtype=np.int32)
     cu[1:] = np.cumsum(wl.chunk_lens)
     T = int(cu[-1])
@@ -255,4 +262,5 @@ def prepare_prefill(wl, values, pool, bm, out_dtype=torch.float32):
         max_q_len=int(np.max(wl.chunk_lens)) if len(wl.chunk_lens) else 0,
         block_tables=torch.as_tensor(tables, device=dev),
         context_lens=torch.as_tensor(lens, device=dev), scale=wl.scale,
-        out=torch.empty((T, wl.num_q_heads, wl.head_dim), dtype=out_dtype, device=dev))
+        out=torch.empty((T, wl.num_q_heads, wl.head_dim), dtype=out_dtype, device=dev),
+        host_ms=host_ms)

@@ -57,6 +57,10 @@ def test_host_argument_checks_need_no_gpu(lib):
         lib.PA_ERR_INVALID_ARG
     assert lib.pa_pool_set_kv_scales(None, 1.0, 1.0) == lib.PA_ERR_INVALID_ARG
     assert lib.pa_pool_kv_scales(None, None, None) == lib.PA_ERR_INVALID_ARG
+    v = ctypes.c_int()
+    assert lib.pa_pool_set_option(None, lib.PA_OPT_PARTITION_CAP, 0) == lib.PA_ERR_INVALID_ARG
+    assert lib.pa_pool_get_option(None, lib.PA_OPT_PARTITION_CAP, ctypes.byref(v)) == \
+        lib.PA_ERR_INVALID_ARG
     assert lib.PA_FP8E4M3 == 2
 
 

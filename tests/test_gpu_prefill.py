@@ -23,8 +23,12 @@ pytestmark = pytest.mark.gpu
 D128 = dict(num_q_heads=32, num_kv_heads=8, head_dim=128)
 
 
+_FORM = {"prefill_kernel": 0}      # set by the `form` fixture
+
+
 def _run(wl, values, out_dtype=torch.float32):
     pool, bm, setup_pairs = runtime.replay_setup(wl, values, "cuda")
+    pool.set_option("prefill_kernel", _FORM["prefill_kernel"])
     step = runtime.prepare_prefill(wl, values, pool, bm, out_dtype=out_dtype)
     step.run()
     torch.cuda.synchronize()
@@ -65,14 +69,13 @@ SMALL = [
 
 
 @pytest.fixture(params=["default", "mma_sync"])
-def form(request, monkeypatch):
+def form(request):
     """The default dispatch (tcgen05 for bf16 pools of 16-token blocks and
-    head_dim 128, mma.sync otherwise) and the mma.sync kernel forced."""
-    if request.param == "mma_sync":
-        monkeypatch.setenv("PA_PREFILL_MMA_SYNC", "1")
-    else:
-        monkeypatch.delenv("PA_PREFILL_MMA_SYNC", raising=False)
-    return request.param
+    head_dim 128, mma.sync otherwise) and the mma.sync kernel selected through
+    the pool's PA_OPT_PREFILL_KERNEL option."""
+    _FORM["prefill_kernel"] = 1 if request.param == "mma_sync" else 0
+    yield request.param
+    _FORM["prefill_kernel"] = 0
 
 
 @pytest.mark.parametrize("kw", SMALL, ids=[f"case{i}" for i in range(len(SMALL))])

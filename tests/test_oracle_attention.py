@@ -3,7 +3,8 @@
 Each test ties the oracle to something other than itself: the pages' worked
 address example, closed forms, torch's float64 scaled-dot-product attention,
 and the verification recipe of kgptalkie "Day 28" ("A Tiny Block-Table
-Example": compare with a contiguous reference while moving physical blocks).
+Example": the paged output must equal a contiguous computation, whatever the
+physical placement of the blocks).
 """
 import json
 import math

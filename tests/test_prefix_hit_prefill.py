@@ -1,7 +1,6 @@
 """A prefix-cache hit skips the prefill of the cached span (zenaique prefix-
 sharing answer and kgptalkie "Prefix Sharing Is a Natural Extension": a hit on
-the chained block hash reuses the block and "the prefill for that span is
-skipped").
+the chained block hash reuses the block, and that span needs no prefill).
 
 Request a prefills a whole prompt and finishes; with retention on its full
 blocks stay registered.  Request b, admitted with the same leading tokens and

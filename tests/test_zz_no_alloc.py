@@ -15,13 +15,14 @@ import ctypes
 import pytest
 import torch
 
+from oracle import replay as orp
 from paged_kv_cache_253_gb300 import _lib as L
 from paged_kv_cache_253_gb300 import runtime
 from paged_kv_cache_253_gb300 import workloads as wls
 
 pytestmark = pytest.mark.gpu
 
-TOL = 5e-3      # max-abs tolerance of the bf16 parity tests
+TOL = {"bf16": 5e-3, "f32": 1e-5}   # max-abs tolerances of the parity tests
 
 
 def _p(t):
@@ -34,17 +35,21 @@ def _noalloc(pool, q, tables, lens, scale, out):
                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-def test_noalloc_matches_pa_decode_on_two_calls():
-    # lengths up to 6000 so sequences split into several partitions and the
-    # arrival counters in the fixed array are exercised
-    wl = wls.make_workload("decode", num_seqs=8, min_len=1, max_len=6000, num_q_heads=32,
-                           num_kv_heads=8, head_dim=128)
+def _two_calls(wl, sample=None):
+    """pa_decode's output, then two pa_decode_noalloc calls in a row, each
+    compared with it and with the float64 oracle (on `sample` sequences, or
+    all of them)."""
     values = wls.generate_values(wl, "cpu")
     pool, bm, _ = runtime.replay_setup(wl, values, "cuda")
     step = runtime.prepare_step(wl, values, pool, bm)
     step.run()
     torch.cuda.synchronize()
+    assert pool.get_error() == 0
     ref = step.out.clone()
+    st = orp.replay(wl, values)
+    seqs = sample if sample is not None else list(range(wl.num_seqs))
+    oracle = orp.attention(wl, values, st, seqs=seqs, threads=8)
+    tol = TOL[wl.dtype]
     for call in range(2):
         out = torch.full_like(ref, float("nan"))
         rc = _noalloc(pool, step.q, step.block_tables, step.context_lens, step.scale, out)
@@ -52,7 +57,33 @@ def test_noalloc_matches_pa_decode_on_two_calls():
         torch.cuda.synchronize()
         assert pool.get_error() == 0
         err = (out - ref).abs().max().item()
-        assert err <= TOL, f"call {call}: max-abs {err:.3g}"
+        assert err <= tol, f"call {call}: max-abs {err:.3g} against pa_decode"
+        got = out.double().cpu().numpy()[seqs]
+        err_o = abs(got - oracle).max()
+        assert err_o <= tol, f"call {call}: max-abs {err_o:.3g} against the oracle"
+
+
+def test_noalloc_matches_pa_decode_on_two_calls():
+    # lengths up to 6000 so sequences split into several partitions whose
+    # partials live in the fixed array
+    _two_calls(wls.make_workload("decode", num_seqs=8, min_len=1, max_len=6000, num_q_heads=32,
+                                 num_kv_heads=8, head_dim=128))
+
+
+def test_noalloc_batch_that_only_just_fits_the_array():
+    # 1650 sequences x 8 KV heads at G 4, head_dim 128: on a 152-SM GPU the
+    # array holds fewer partial slots than the plan would like (16,131 of
+    # 16,848) but more than it needs (15,024), so the call gives the kernel the
+    # smaller capacity and the partitions grow to fit it
+    _two_calls(wls.make_workload("decode", num_seqs=1650, min_len=1, max_len=200,
+                                 num_q_heads=32, num_kv_heads=8, head_dim=128),
+               sample=[0, 1, 777, 1648, 1649])
+
+
+def test_noalloc_fp32_pool():
+    # the fp32 CUDA-core kernel, whose partial count follows the table width
+    _two_calls(wls.make_workload("decode", num_seqs=5, min_len=1, max_len=900, dtype="f32",
+                                 num_q_heads=16, num_kv_heads=4, head_dim=64))
 
 
 def test_noalloc_refuses_a_batch_beyond_its_scratch():
