@@ -149,12 +149,14 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
         if (PTs < PT && PTs >= kGuideMinPT && bound <= p.max_items) split_at = total - total / 4;
         else PTs = PT;
     }
-    // first sequence starting at or after split_at
+    // first sequence starting at or after split_at (every thread of the CTA
+    // has the same split_at, so the branch is uniform)
+    int S_split = p.S;
     __syncthreads();                                // s_red reuse
-    int* s_split = reinterpret_cast<int*>(s_red);
-    if (tid == 0) *s_split = p.S;
-    __syncthreads();
-    {
+    if (split_at != LLONG_MAX) {
+        int* s_split = reinterpret_cast<int*>(s_red);
+        if (tid == 0) *s_split = p.S;
+        __syncthreads();
         long long c = tbase;
         for (int s = lo; s < hi; ++s) {
             if (c >= split_at) {
@@ -163,10 +165,10 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
             }
             c += priv_len(p, s, false);
         }
+        __syncthreads();
+        S_split = *s_split;
+        __syncthreads();                            // s_red reuse below
     }
-    __syncthreads();
-    const int S_split = *s_split;
-    __syncthreads();                                // s_red reuse below
     int cnt = 0;
     for (int s = lo; s < hi; ++s) {
         const int L = priv_len(p, s, false), pts = s >= S_split ? PTs : PT;
@@ -910,11 +912,12 @@ decode_fast_kernel(const DecodeParams p) {
     const Sched sc = build_schedule(p, s_start, s_red);
     publish_schedule(p, sc, s_start);
     const int n_sh = SHARED ? p.n_shared_items : 0;
-    for (int item = blockIdx.x; item < n_sh + sc.total_items; item = next_item(p, s_flag + 1)) {
+    for (int item = blockIdx.x; item < n_sh + sc.total_items;) {
         if (SHARED && item < n_sh) {
             const int k = item / p.Hkv, hh = item - k * p.Hkv;
             shared_item<D>(p, p.sh_items[4 * k], hh, p.sh_items[4 * k + 1], p.sh_items[4 * k + 2],
                            ring);
+            item = next_item(p, s_flag + 1);
             continue;
         }
         const int pitem = item - n_sh;
@@ -933,6 +936,11 @@ decode_fast_kernel(const DecodeParams p) {
             fast_item<D, FUSE, F8, 16>(p, s, h, tok0, tok1, L, sm_o, sm_m, sm_l);
         else
             fast_item<D, FUSE, F8>(p, s, h, tok0, tok1, L, sm_o, sm_m, sm_l);
+        // the next item's ticket, taken as soon as warp 0 is done with this
+        // item's blocks: its round trip overlaps the merge of the warps below
+        // (62.2 against 63.0 us on the decode batch, measured on GB300)
+        int ticket = 0;
+        if (threadIdx.x == 0) ticket = atomicAdd(p.ticket, 1);
         __syncthreads();
         // merge the warps' softmax states (in place into warp 0's buffer)
         for (int idx = threadIdx.x; idx < p.G * D; idx += kThreads) {
@@ -957,7 +965,10 @@ decode_fast_kernel(const DecodeParams p) {
         }
         __syncthreads();
         finish_item(p, pitem, s, h, nP, res_m, res_l, sm_o, OS);
+        if (threadIdx.x == 0) s_flag[1] = static_cast<int>(gridDim.x) + ticket;
         __syncthreads();
+        item = s_flag[1];
+        // s_flag[1] is written again only after the next item's first barrier
     }
     if (p.defer_wait) pa_dev::wait_prior_grid();        // the shared-prefix kernel is done too
     pa_dev::allow_next_grid();
