@@ -61,280 +61,498 @@ __device__ __forceinline__ int seq_len(const DecodeParams& p, int s) {
     return L < 0 ? 0 : min(L, p.max_blocks * p.B);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+// ------------------------------------------------- shared-prefix items ---
+//
+// Warp roles of one CTA (224 threads; one CTA per SM, so that the split pass
+// of the private suffixes runs beside it on every SM):
+//   warps 0-3  softmax: thread t owns query row t, which is TMEM lane t; they
+//              also check an item's sharing description and write each
+//              finished item's partial rows
+//   warp 4     producer: the item's Q rows by cp.async, then each 64-token
+//              step's K and V^T by TMA into a ring of kWsStages stages
+//   warp 5     Q.K^T issue (lane 0): S into one of two S buffers in TMEM
+//   warp 6     P.V issue (lane 0): O += P.V with P read from one of two P
+//              buffers in TMEM, into one of two O buffers (one per item)
+// Items go to CTAs statically (item = blockIdx.x + k * gridDim.x), so every
+// role walks the same items and steps without telling the others which; the
+// roles hand each other work through mbarriers only.  Q.K^T(j) is issued as
+// soon as the step's keys have landed and an S buffer is free, P.V(j) once the
+// softmax warps have written P(j): the tensor pipe computes the next step's
+// scores while the softmax warps work on this one, and the two kinds of MMA
+// are issued by two threads (one thread issuing both was the step's limit).
+// An item's partial rows are written while the next item's first step runs
+// (its O buffer is not touched again until the item after that).
+// Every mbarrier wait is bounded; a role that gives up raises a shared abort
+// flag that ends the others' waits at once, records PA_ERR_CUDA, and the CTA
+// drains its own copies and MMAs before it frees TMEM and exits.
+constexpr int kWsThreads = 224;
+constexpr int kWsStages = 4;
+constexpr uint32_t kWsStageOff = 32768;                  // after Q (2 x [128][128 B])
+constexpr uint32_t kWsBarOff = kWsStageOff + kWsStages * kStageBytes;
+enum WsBar {
+    kQFull, kQEmpty, kSFull0, kSFull1, kSEmpty0, kSEmpty1, kPFull0, kPFull1, kPEmpty0, kPEmpty1,
+    kOFull0, kOFull1, kMmaDone, kKvFull0, kKvEmpty0 = kKvFull0 + kWsStages,
+    kNumWsBars = kKvEmpty0 + kWsStages
+};
+constexpr uint32_t kWsMiscOff = kWsBarOff + kNumWsBars * 8;   // TMEM slot, abort flag, stage masks
+constexpr uint32_t kWsMembersOff = kWsMiscOff + 64;            // batch index of each row's member
+constexpr uint32_t kWsSmemBytes = kWsMembersOff + 4 * kRows + 1024;   // + alignment slack
+// TMEM columns: S0 [0,64), S1 [64,128), O0 [128,256), O1 [256,384), then two
+// P buffers of 64 columns at 384 and 448, P hi (bf16 pairs) in the first 32
+// and P lo in the next 32
+constexpr int kWsTmemCols = 512;
+
+// Bounded wait on an mbarrier phase that also gives up when another role has
+// raised the abort flag; a timeout raises it.
+__device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    const uint32_t a = pa_tc::smem_u32(bar);
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((i & 31) == 31 && *abort_flag) return false;
+    }
+    *abort_flag = 1;
+    return false;
+}
+
+__device__ __forceinline__ void ws_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(pa_tc::smem_u32(bar)) : "memory");
+}
+
+// What every role derives from an item index.
+struct WsItem {
+    int grp, h, chunk, m0, m1, moff, t0, t1, nsteps, nC, lbc, nbc;
+    const int32_t* table;       // the first member's table (the shared blocks)
+};
+
+__device__ __forceinline__ WsItem ws_item(const DecodeParams& p, int item) {
+    WsItem it;
+    const int k = item / p.Hkv;
+    it.h = item - k * p.Hkv;
+    it.grp = p.sh_items[4 * k];
+    const int tile = p.sh_items[4 * k + 1];
+    it.chunk = p.sh_items[4 * k + 2];
+    it.moff = p.g_members_off[it.grp];
+    const int M = p.g_members_off[it.grp + 1] - it.moff;
+    it.m0 = tile * p.members_per_tile;
+    it.m1 = min(M, it.m0 + p.members_per_tile);
+    const int shared_tok = p.g_shared_tokens[it.grp];
+    it.t0 = it.chunk * p.chunk_tokens;
+    it.t1 = min(shared_tok, it.t0 + p.chunk_tokens);
+    it.nsteps = (it.t1 - it.t0 + kStep - 1) / kStep;
+    it.nC = p.g_nchunks[it.grp];
+    it.lbc = it.t0 / p.B;
+    it.nbc = (it.t1 - it.t0) / p.B;
+    it.table = p.tables + static_cast<size_t>(p.g_members[it.moff]) * p.max_blocks;
+    return it;
+}
+
+// The sharing description must match the tables: every member covers the
+// shared span, and every member's table holds the first member's blocks on
+// this item's chunk (recorded, never trapped).  The tables do not depend on
+// the head, so the Hkv items of one (group, tile, chunk) split the checks
+// between them: the item of head h takes every Hkv-th entry, starting at h.
+// Run by the 128 softmax threads, eight table entries in flight per thread.
+__device__ __forceinline__ void ws_validate(const DecodeParams& p, const WsItem& it, int t) {
+    const int nm = it.m1 - it.m0, step = 128 * p.Hkv;
+    if (it.chunk == 0)
+        for (int mi = it.h + t * p.Hkv; mi < nm; mi += step)
+            if (seq_len(p, p.g_members[it.moff + it.m0 + mi]) < p.g_shared_tokens[it.grp])
+                pa_dev::record_error(p.err, PA_ERR_INVALID_ARG);
+    const int n = nm * it.nbc;
+    for (int e0 = it.h + t * p.Hkv; e0 < n; e0 += 8 * step) {
+        int mine[8], ref[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = e0 + u * step;
+            mine[u] = ref[u] = 0;
+            if (e < n) {
+                const int mi = e / it.nbc, bi = e - mi * it.nbc;
+                mine[u] = __ldg(p.tables + static_cast<size_t>(p.g_members[it.moff + it.m0 + mi]) * p.max_blocks +
+                                it.lbc + bi);
+                ref[u] = __ldg(it.table + it.lbc + bi);
+            }
+        }
+        bool bad = false;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) bad |= mine[u] != ref[u];
+        if (bad) pa_dev::record_error(p.err, PA_ERR_INVALID_ARG);
+    }
+}
+
+__global__ void __launch_bounds__(kWsThreads, 2)
 shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ unsigned char tc_raw[];
     const uint32_t raw_s = pa_tc::smem_u32(tc_raw);
     unsigned char* base = tc_raw + ((1024u - (raw_s & 1023u)) & 1023u);
     const uint32_t sbase = pa_tc::smem_u32(base);
-    uint64_t* bar_s = reinterpret_cast<uint64_t*>(base + kMiscOff);
-    uint64_t* bar_pv = bar_s + 1;
-    uint64_t* bar_full = bar_s + 2;                                // [2]: a stage's TMA copies landed
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kMiscOff + 32);
-    int* s_tbl = reinterpret_cast<int*>(base + kMiscOff + 64);   // kChunkBlocks block ids of a chunk
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + kWsBarOff);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kWsMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kWsMiscOff + 4);
+    volatile int* stage_mask = reinterpret_cast<volatile int*>(base + kWsMiscOff + 8);   // [kWsStages]
+    int* s_members = reinterpret_cast<int*>(base + kWsMembersOff);   // [kRows], producer only
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pa_dev::wait_prior_grid();
-    pa_dev::allow_next_grid();       // the private-span split kernel may run alongside
+    pa_dev::allow_next_grid();       // the private-span split kernel runs alongside
     if (tid == 0) {
-        pa_tc::mbar_init(bar_s, 1);
-        pa_tc::mbar_init(bar_pv, 1);
-        pa_tc::mbar_init(bar_full, 1);
-        pa_tc::mbar_init(bar_full + 1, 1);
+        pa_tc::mbar_init(&bars[kQFull], 32);                 // the producer's 32 lanes
+        pa_tc::mbar_init(&bars[kQEmpty], 1);
+        pa_tc::mbar_init(&bars[kSFull0], 1);
+        pa_tc::mbar_init(&bars[kSFull1], 1);
+        pa_tc::mbar_init(&bars[kSEmpty0], 4);                // one arrival per softmax warp
+        pa_tc::mbar_init(&bars[kSEmpty1], 4);
+        pa_tc::mbar_init(&bars[kPFull0], 4);
+        pa_tc::mbar_init(&bars[kPFull1], 4);
+        pa_tc::mbar_init(&bars[kPEmpty0], 1);
+        pa_tc::mbar_init(&bars[kPEmpty1], 1);
+        pa_tc::mbar_init(&bars[kOFull0], 1);
+        pa_tc::mbar_init(&bars[kOFull1], 1);
+        pa_tc::mbar_init(&bars[kMmaDone], 2);                // both MMA-issuing warps
+        for (int s = 0; s < kWsStages; ++s) {
+            pa_tc::mbar_init(&bars[kKvFull0 + s], 1);
+            pa_tc::mbar_init(&bars[kKvEmpty0 + s], 1);
+        }
+        *abort_flag = 0;
         pa_tc::mbar_init_fence();
     }
-    if (warp == 0) pa_tc::tmem_alloc<kTmemCols>(tslot);
+    if (warp == 0) pa_tc::tmem_alloc<kWsTmemCols>(tslot);
     pa_tc::fence_before_sync();
     __syncthreads();
     pa_tc::fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t tS = tmem, tO = tmem + 64, tPh = tmem + 192, tPl = tmem + 224;
-    const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;   // this warp's TMEM lanes
-    uint32_t ph_s = 0, ph_pv = 0, ph_full0 = 0, ph_full1 = 0;
+    const uint32_t tO = tmem + 128, tP = tmem + 384;     // O buffer b at tO + 128 b, P buffer b at tP + 64 b
+    const int G = p.G, Hkv = p.Hkv;
     bool ok = true;
 
-    const int G = p.G, B = p.B, Hkv = p.Hkv;
-    const uint16_t* qg = static_cast<const uint16_t*>(p.q);
-    const float sl = p.scale_log2;
-
-    for (int item = blockIdx.x; ok && item < p.n_shared_items; item += gridDim.x) {
-        const int k = item / Hkv, h = item - k * Hkv;
-        const int grp = p.sh_items[4 * k], tile = p.sh_items[4 * k + 1], chunk = p.sh_items[4 * k + 2];
-        const int moff = p.g_members_off[grp];
-        const int M = p.g_members_off[grp + 1] - moff;
-        const int mpt = p.members_per_tile;
-        const int m0 = tile * mpt, m1 = min(M, m0 + mpt);
-        const int shared_tok = p.g_shared_tokens[grp];
-        const int t0 = chunk * p.chunk_tokens, t1 = min(shared_tok, t0 + p.chunk_tokens);
-        const int nsteps = (t1 - t0 + kStep - 1) / kStep;
-        const int nC = p.g_nchunks[grp];
-        const int32_t* table = p.tables + static_cast<size_t>(p.g_members[moff]) * p.max_blocks;
-        const int lbc = t0 / B, nbc = (t1 - t0) / B;
-
-        // validation (recorded, never trapped): members cover the span and agree;
-        // the tables do not depend on the head, so the head-0 item checks them
-        if (h == 0 && chunk == 0)
-            for (int mi = tid; mi < m1 - m0; mi += kThreads)
-                if (seq_len(p, p.g_members[moff + m0 + mi]) < shared_tok)
-                    pa_dev::record_error(p.err, PA_ERR_INVALID_ARG);
-        for (int e = tid; h == 0 && e < (m1 - m0) * nbc; e += kThreads) {
-            const int mi = e / nbc, bi = e - mi * nbc;
-            const int32_t* mt = p.tables + static_cast<size_t>(p.g_members[moff + m0 + mi]) * p.max_blocks;
-            if (__ldg(mt + lbc + bi) != __ldg(table + lbc + bi))
-                pa_dev::record_error(p.err, PA_ERR_INVALID_ARG);
-        }
-        static_assert(kChunkBlocks <= kThreads, "one thread per block of a chunk");
-        if (tid < nbc) {
-            int b = __ldg(table + lbc + tid);
-            if (b < 0 || b >= p.num_blocks) {
-                pa_dev::record_error(p.err, PA_ERR_BAD_BLOCK_ID);
-                b = -1;
-            }
-            s_tbl[tid] = b;
-        }
-
-        // this thread's query row
-        const int row_m = m0 + tid / G, row_n = tid - (tid / G) * G;
-        const bool row_ok = tid < mpt * G && row_m < m1;
-        const int row_s = row_ok ? p.g_members[moff + row_m] : 0;
-
-        // Q tile: 128 rows x 16 chunks of 16 B, zero rows where no query
-        for (int idx = tid; idx < kRows * 16; idx += kThreads) {
-            const int r = idx >> 4, c16 = idx & 15;
-            const int rm = m0 + r / G, rn = r - (r / G) * G;
-            const bool v = r < mpt * G && rm < m1;
-            const uint16_t* src = qg + (v ? ((static_cast<size_t>(p.g_members[moff + rm]) * p.Hq +
-                                              static_cast<size_t>(h) * G + rn) * kD + c16 * 8)
-                                          : 0);
-            pa_tc::cp16(sbase + kQOff + (c16 >> 3) * 16384 + pa_tc::sw128_off(r, c16 & 7), src,
-                        v ? 16u : 0u);
-        }
-        pa_tc::cp_commit();
-        __syncthreads();                                   // s_tbl visible
-
-        // One thread stages a step: per 16-token block, its K rows as two
-        // 64-d boxes (128-byte swizzle, placed at row 16b of the two K regions)
-        // and its V^T tile as one 16-token x 128-d box (32-byte swizzle, own
-        // 4 KB region); the stage's mbarrier completes when all bytes landed.
-        auto load_step = [&](int j) {
-            if (tid != 0) return;
-            const int st = j & 1;
-            const uint32_t kst = sbase + kStageOff + st * kStageBytes;
-            uint32_t bytes = 0;
-#pragma unroll
-            for (int b = 0; b < kStep / 16; ++b) {
-                const int rel = j * kStep + 16 * b;
-                if (t0 + rel < t1 && s_tbl[rel >> 4] >= 0) bytes += 2 * 2048 + 4096;
-            }
-            pa_tc::mbar_expect_tx(bar_full + st, bytes);
-#pragma unroll
-            for (int b = 0; b < kStep / 16; ++b) {
-                const int rel = j * kStep + 16 * b;
-                if (t0 + rel >= t1) continue;
-                const int phys = s_tbl[rel >> 4];
-                if (phys < 0) continue;
-                const int yk = (phys * Hkv + h) * 16, yv = (phys * Hkv + h) * kD;
-                pa_tc::tma_load_2d(kst + b * 2048, &kmap, 0, yk, bar_full + st);
-                pa_tc::tma_load_2d(kst + 8192 + b * 2048, &kmap, 64, yk, bar_full + st);
-                pa_tc::tma_load_2d(kst + 16384 + b * 4096, &vmap, 0, yv, bar_full + st);
-            }
-        };
-
-        load_step(0);
-        float m_ref = -INFINITY, l = 0.f;
-        for (int j = 0; j < nsteps && ok; ++j) {
-            const int st = j & 1;
-            if (j > 0) {                                   // P.V of step j-1 done: its stage and P are free
-                const bool w = pa_tc::mbar_wait(bar_pv, ph_pv, kWaitLimit);
-                if (!__syncthreads_and(w)) { ok = false; break; }
-                ph_pv ^= 1u;
-            }
-            if (j + 1 < nsteps) load_step(j + 1);
-            if (j == 0) pa_tc::cp_wait<0>();               // this item's Q rows (cp.async)
-            {
-                const bool w = pa_tc::mbar_wait(bar_full + st, st ? ph_full1 : ph_full0, kWaitLimit);
-                if (st) ph_full1 ^= 1u; else ph_full0 ^= 1u;
-                if (!__syncthreads_and(w)) { ok = false; break; }
-            }
-            // Block slots this step did not load (past the span's end, or a
-            // block id outside the pool) hold what an earlier step left there.
-            // Their scores are masked below, but a zero-weight value still
-            // enters P.V and 0 * Inf or 0 * NaN is NaN: zero their V^T rows
-            // (thread t clears row t of each such slot).
-            int loaded = 0;                                // bit b: block slot b holds this step's keys
-#pragma unroll
-            for (int b = 0; b < kStep / 16; ++b) {
-                const int rel = j * kStep + 16 * b;
-                if (t0 + rel < t1 && s_tbl[rel >> 4] >= 0) loaded |= 1 << b;
-                else pa_tc::zero_vt_row_tail(base + kStageOff + st * kStageBytes + 16384 + b * 4096, tid, 0);
-            }
-            pa_tc::fence_smem_to_async();
-            pa_tc::fence_before_sync();
-            __syncthreads();
-            pa_tc::fence_after_sync();
-            const uint32_t kst = sbase + kStageOff + st * kStageBytes;
-            if (tid == 0) {
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint64_t a = pa_tc::sw128_desc(sbase + kQOff + (kk >> 2) * 16384 + (kk & 3) * 32);
-                    const uint64_t b = pa_tc::sw128_desc(kst + (kk >> 2) * 8192 + (kk & 3) * 32);
-                    pa_tc::mma_bf16(tS, a, b, kIdescQK, kk > 0);
+    if (warp == 4) {
+        // ------------------------------------------------------ producer
+        const uint16_t* qg = static_cast<const uint16_t*>(p.q);
+        uint32_t kv_it = 0, fills[kWsStages] = {};
+        int kk = 0;
+        for (int item = blockIdx.x; ok && item < p.n_shared_items; item += gridDim.x, ++kk) {
+            const WsItem it = ws_item(p, item);
+            // the chunk's block ids (at most 64): lane b holds blocks b and b + 32
+            auto block_id = [&](int bi) {
+                int b = bi < it.nbc ? __ldg(it.table + it.lbc + bi) : -1;
+                if (bi < it.nbc && (b < 0 || b >= p.num_blocks)) {
+                    pa_dev::record_error(p.err, PA_ERR_BAD_BLOCK_ID);
+                    b = -1;
                 }
-                pa_tc::commit(bar_s);
+                return b;
+            };
+            const int tb0 = block_id(lane), tb1 = block_id(lane + 32);
+            // the tile's members (batch indices), read once for the row loop below
+            for (int mi = lane; mi < it.m1 - it.m0; mi += 32) s_members[mi] = p.g_members[it.moff + it.m0 + mi];
+            __syncwarp();
+            // Q rows, once the previous item's last Q.K^T is done with the Q tile
+            if (kk > 0 && !ws_wait(&bars[kQEmpty], (kk - 1) & 1, abort_flag)) { ok = false; break; }
+            for (int idx = lane; idx < kRows * 16; idx += 32) {
+                const int r = idx >> 4, c16 = idx & 15;
+                const int rmi = r / G, rn = r - rmi * G;
+                const bool v = r < p.members_per_tile * G && it.m0 + rmi < it.m1;
+                const uint16_t* src = qg + (v ? ((static_cast<size_t>(s_members[rmi]) * p.Hq +
+                                                  static_cast<size_t>(it.h) * G + rn) * kD + c16 * 8)
+                                              : 0);
+                pa_tc::cp16(sbase + kQOff + (c16 >> 3) * 16384 + pa_tc::sw128_off(r, c16 & 7), src,
+                            v ? 16u : 0u);
             }
-            {
-                const bool w = pa_tc::mbar_wait(bar_s, ph_s, kWaitLimit);
-                if (!__syncthreads_and(w)) { ok = false; break; }
+            pa_tc::cp_commit();
+            pa_tc::cp_wait<0>();
+            pa_tc::fence_smem_to_async();                    // cp.async writes -> tensor core reads
+            ws_arrive(&bars[kQFull]);
+            for (int j = 0; j < it.nsteps; ++j, ++kv_it) {
+                const int st = kv_it % kWsStages;
+                const uint32_t use = kv_it / kWsStages;
+                if (use > 0 && !ws_wait(&bars[kKvEmpty0 + st], (use - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char* stage = base + kWsStageOff + st * kStageBytes;
+                int phys[kStep / 16], loaded = 0;
+#pragma unroll
+                for (int b = 0; b < kStep / 16; ++b) {
+                    const int rel = j * kStep + 16 * b, bi = rel >> 4;
+                    const int id = bi < 32 ? __shfl_sync(0xffffffffu, tb0, bi & 31)
+                                           : __shfl_sync(0xffffffffu, tb1, bi & 31);
+                    phys[b] = it.t0 + rel < it.t1 ? id : -1;
+                    if (phys[b] >= 0) loaded |= 1 << b;
+                }
+                // slots without keys keep what an earlier step left: their scores
+                // are masked, and zero values keep 0 * Inf out of P.V
+                if (loaded != (1 << (kStep / 16)) - 1) {
+#pragma unroll
+                    for (int b = 0; b < kStep / 16; ++b)
+                        if (!((loaded >> b) & 1))
+                            for (int o = lane * 16; o < 4096; o += 32 * 16)
+                                *reinterpret_cast<uint4*>(stage + 16384 + b * 4096 + o) = make_uint4(0u, 0u, 0u, 0u);
+                    pa_tc::fence_smem_to_async();
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    stage_mask[st] = loaded;
+                    const uint32_t kst = sbase + kWsStageOff + st * kStageBytes;
+                    pa_tc::mbar_expect_tx(&bars[kKvFull0 + st],
+                                          static_cast<uint32_t>(__popc(loaded)) * (2 * 2048 + 4096));
+#pragma unroll
+                    for (int b = 0; b < kStep / 16; ++b) {
+                        if (phys[b] < 0) continue;
+                        const int yk = (phys[b] * Hkv + it.h) * 16, yv = (phys[b] * Hkv + it.h) * kD;
+                        pa_tc::tma_load_2d(kst + b * 2048, &kmap, 0, yk, &bars[kKvFull0 + st]);
+                        pa_tc::tma_load_2d(kst + 8192 + b * 2048, &kmap, 64, yk, &bars[kKvFull0 + st]);
+                        pa_tc::tma_load_2d(kst + 16384 + b * 4096, &vmap, 0, yv, &bars[kKvFull0 + st]);
+                    }
+                }
+                __syncwarp();
+                ++fills[st];
             }
-            ph_s ^= 1u;
+        }
+        // every copy issued must have landed before the CTA's shared memory is released
+        for (int s = 0; s < kWsStages; ++s)
+            if (fills[s] > 0) pa_tc::mbar_wait(&bars[kKvFull0 + s], (fills[s] - 1) & 1, kWaitLimit);
+    } else if (warp == 5) {
+        // ----------------------------------------------- Q.K^T issue
+        uint32_t kv_it = 0, s_it = 0;
+        int kk = 0;
+        for (int item = blockIdx.x; ok && item < p.n_shared_items; item += gridDim.x, ++kk) {
+            const WsItem it = ws_item(p, item);
+            if (!ws_wait(&bars[kQFull], kk & 1, abort_flag)) { ok = false; break; }
+            for (int j = 0; j < it.nsteps; ++j, ++kv_it, ++s_it) {
+                const int st = kv_it % kWsStages, sb = s_it & 1;
+                if (!ws_wait(&bars[kKvFull0 + st], (kv_it / kWsStages) & 1, abort_flag) ||
+                    ((s_it >> 1) > 0 && !ws_wait(&bars[kSEmpty0 + sb], ((s_it >> 1) - 1) & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                pa_tc::fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t kst = sbase + kWsStageOff + st * kStageBytes;
+#pragma unroll
+                    for (int q = 0; q < kD / 16; ++q) {
+                        const uint64_t a = pa_tc::sw128_desc(sbase + kQOff + (q >> 2) * 16384 + (q & 3) * 32);
+                        const uint64_t b = pa_tc::sw128_desc(kst + (q >> 2) * 8192 + (q & 3) * 32);
+                        pa_tc::mma_bf16(tmem + sb * 64, a, b, kIdescQK, q > 0);
+                    }
+                    pa_tc::commit(&bars[kSFull0 + sb]);
+                    if (j == it.nsteps - 1) pa_tc::commit(&bars[kQEmpty]);   // Q tile free
+                }
+                __syncwarp();
+            }
+        }
+        // every MMA issued must be complete before TMEM is freed
+        if (lane == 0) pa_tc::commit(&bars[kMmaDone]);
+        __syncwarp();
+        pa_tc::mbar_wait(&bars[kMmaDone], 0, kWaitLimit);
+    } else if (warp == 6) {
+        // ------------------------------------------------- P.V issue
+        // P.V(j) needs P(j) from the softmax warps, which took S(j), which
+        // needed the step's keys: so its Q.K^T is done and its values landed
+        // (the wait on the stage below is already complete).
+        uint32_t kv_it = 0, p_it = 0;
+        int kk = 0;
+        for (int item = blockIdx.x; ok && item < p.n_shared_items; item += gridDim.x, ++kk) {
+            const WsItem it = ws_item(p, item);
+            const int ob = kk & 1;
+            for (int j = 0; j < it.nsteps; ++j, ++kv_it, ++p_it) {
+                const int st = kv_it % kWsStages, pb = p_it & 1;
+                if (!ws_wait(&bars[kPFull0 + pb], (p_it >> 1) & 1, abort_flag) ||
+                    !ws_wait(&bars[kKvFull0 + st], (kv_it / kWsStages) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                pa_tc::fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t kst = sbase + kWsStageOff + st * kStageBytes;
+                    const uint32_t ph = tP + pb * 64, pl = ph + 32, od = tO + ob * 128;
+#pragma unroll
+                    for (int q = 0; q < kStep / 16; ++q) {
+                        const uint64_t b = pa_tc::sw32_desc(kst + 16384 + q * 4096);   // block q's V^T
+                        pa_tc::mma_bf16_ta(od, ph + q * 8, b, kIdescPV, !(j == 0 && q == 0));
+                        pa_tc::mma_bf16_ta(od, pl + q * 8, b, kIdescPV, true);
+                    }
+                    pa_tc::commit(&bars[kKvEmpty0 + st]);    // the stage may be refilled
+                    pa_tc::commit(&bars[kPEmpty0 + pb]);     // P buffer free, O settled up to here
+                    if (j == it.nsteps - 1) pa_tc::commit(&bars[kOFull0 + ob]);
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0) pa_tc::commit(&bars[kMmaDone]);
+        __syncwarp();
+        pa_tc::mbar_wait(&bars[kMmaDone], 0, kWaitLimit);
+    } else {
+        // ------------------------------------------------------- softmax
+        const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;   // this warp's TMEM lanes
+        const float sl = p.scale_log2;
+        uint32_t kv_it = 0, s_it = 0, p_it = 0;
+        int kk = 0;
+        // the previous item's partial rows, written during this item's first step
+        struct Pending {
+            bool live;
+            int kk;
+            size_t slot;            // this thread's partial slot (valid when row_ok)
+            bool row_ok;
+            int row_n;
+            float m, l;
+        } pend = {false, 0, 0, false, 0, 0.f, 0.f};
+        auto write_partial = [&]() {
+            if (!ws_wait(&bars[kOFull0 + (pend.kk & 1)], (pend.kk >> 1) & 1, abort_flag)) return false;
             pa_tc::fence_after_sync();
-            float s[64];
-            {
-                float a32[32], b32[32];
-                pa_tc::tmem_ld32(tS + lane_sel, a32);
-                pa_tc::tmem_ld32(tS + lane_sel + 32, b32);
+            float* acc = p.spart_acc + (pend.slot * G + pend.row_n) * kD;
+            const uint32_t od = tO + (pend.kk & 1) * 128 + lane_sel;
+#pragma unroll 1
+            for (int cc = 0; cc < kD / 32; ++cc) {
+                float o[32];
+                pa_tc::tmem_ld32(od + cc * 32, o);
                 pa_tc::tmem_wait_ld();
+                if (pend.row_ok) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    s[i] = a32[i];
-                    s[32 + i] = b32[i];
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(acc + cc * 32 + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
                 }
             }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                s[i] = (loaded >> (i >> 4)) & 1 ? s[i] * sl : -INFINITY;
-                mx = fmaxf(mx, s[i]);
+            if (pend.row_ok) {
+                p.spart_ml[(pend.slot * G + pend.row_n) * 2] = pend.m;
+                p.spart_ml[(pend.slot * G + pend.row_n) * 2 + 1] = pend.l;
             }
-            // raise the reference maximum only when it is far behind (or unset)
-            const bool first = m_ref == -INFINITY;
-            const bool raise = !first && mx > m_ref + 8.f;
-            if (first) m_ref = mx;
-            if (__any_sync(0xffffffffu, raise)) {          // rescale this warp's rows of O
-                const float corr = raise ? exp2_approx(m_ref - mx) : 1.f;
-                if (raise) {
-                    l *= corr;
-                    m_ref = mx;
-                }
-#pragma unroll
-                for (int cc = 0; cc < kD / 32; ++cc) {
-                    float o[32];
-                    pa_tc::tmem_ld32(tO + lane_sel + cc * 32, o);
-                    pa_tc::tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= corr;
-                    pa_tc::tmem_st32(tO + lane_sel + cc * 32, o);
-                }
-                pa_tc::tmem_wait_st();
-            }
-            const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-            float sum = 0.f;
-            {
-                uint32_t hi[32], lo[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p0 = exp2_approx(s[2 * e] - ref);
-                    const float p1 = exp2_approx(s[2 * e + 1] - ref);
-                    sum += p0 + p1;
-                    hi[e] = pa_dev::pack_bf16(p0, p1);
-                    lo[e] = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(hi[e]), p1 - pa_dev::bf16_hi(hi[e]));
-                }
-                pa_tc::tmem_st32u(tPh + lane_sel, hi);         // this row of P, bf16 pairs
-                pa_tc::tmem_st32u(tPl + lane_sel, lo);
-                pa_tc::tmem_wait_st();
-            }
-            l += sum;
             pa_tc::fence_before_sync();
-            __syncthreads();
-            pa_tc::fence_after_sync();
-            if (tid == 0) {
-#pragma unroll
-                for (int kk = 0; kk < kStep / 16; ++kk) {
-                    const uint64_t b = pa_tc::sw32_desc(kst + 16384 + kk * 4096);   // block kk's V^T
-                    pa_tc::mma_bf16_ta(tO, tPh + kk * 8, b, kIdescPV, j > 0 || kk > 0);
-                    pa_tc::mma_bf16_ta(tO, tPl + kk * 8, b, kIdescPV, true);
+            pend.live = false;
+            return true;
+        };
+        for (int item = blockIdx.x; ok && item < p.n_shared_items; item += gridDim.x, ++kk) {
+            const WsItem it = ws_item(p, item);
+            ws_validate(p, it, tid);
+            const int row_m = it.m0 + tid / G, row_n = tid - (tid / G) * G;
+            const bool row_ok = tid < p.members_per_tile * G && row_m < it.m1;
+            const uint32_t od = tO + (kk & 1) * 128 + lane_sel;   // this item's O rows
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.nsteps; ++j, ++kv_it, ++s_it, ++p_it) {
+                const int st = kv_it % kWsStages, sb = s_it & 1;
+                // the stage's keys have landed (and its slot mask is written)
+                if (!ws_wait(&bars[kKvFull0 + st], (kv_it / kWsStages) & 1, abort_flag) ||
+                    !ws_wait(&bars[kSFull0 + sb], (s_it >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                pa_tc::commit(bar_pv);
-            }
-        }
-        if (!ok) break;
-        {
-            const bool w = pa_tc::mbar_wait(bar_pv, ph_pv, kWaitLimit);
-            if (!__syncthreads_and(w)) { ok = false; break; }
-        }
-        ph_pv ^= 1u;
-        pa_tc::fence_after_sync();
-        // this row's partial: O (relative to m_ref), m_ref, l
-        const size_t slot = row_ok ? (static_cast<size_t>(p.g_spart_base[grp]) +
-                                      static_cast<size_t>(row_m) * nC + chunk) * Hkv + h : 0;
-        float* acc = p.spart_acc + (slot * G + row_n) * kD;
+                const int loaded = stage_mask[st];
+                pa_tc::fence_after_sync();
+                // scores of this row in two halves of 32 keys (TMEM columns)
+                float sa[32], sb32[32];
+                pa_tc::tmem_ld32(tmem + sb * 64 + lane_sel, sa);
+                pa_tc::tmem_ld32(tmem + sb * 64 + lane_sel + 32, sb32);
+                pa_tc::tmem_wait_ld();
+                pa_tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ws_arrive(&bars[kSEmpty0 + sb]);   // S buffer free
+                // Fast path (every key slot loaded, positive scale): the maximum of
+                // the scaled scores is scale times the raw maximum, and each weight
+                // is one FFMA and one exp2.  Otherwise: scale, mask, then exp2.
+                const bool fast = loaded == (1 << (kStep / 16)) - 1 && sl > 0.f;
+                float mx = -INFINITY;
+                if (fast) {
 #pragma unroll
-        for (int cc = 0; cc < kD / 32; ++cc) {
-            float o[32];
-            pa_tc::tmem_ld32(tO + lane_sel + cc * 32, o);
-            pa_tc::tmem_wait_ld();
-            if (row_ok) {
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(sa[i], sb32[i]));
+                    mx *= sl;
+                } else {
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<float4*>(acc + cc * 32 + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+                    for (int i = 0; i < 32; ++i) {
+                        sa[i] = (loaded >> (i >> 4)) & 1 ? sa[i] * sl : -INFINITY;
+                        sb32[i] = (loaded >> (2 + (i >> 4))) & 1 ? sb32[i] * sl : -INFINITY;
+                        mx = fmaxf(mx, fmaxf(sa[i], sb32[i]));
+                    }
+                }
+                // raise the reference maximum only when it is far behind (or unset)
+                const bool first = m_ref == -INFINITY;
+                const bool raise = !first && mx > m_ref + 8.f;
+                const float old_ref = m_ref;
+                if (first || raise) m_ref = mx;
+                const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+                if (__any_sync(0xffffffffu, raise)) {
+                    // O holds the sums up to the previous step once its P.V is done;
+                    // rescale this warp's rows of O to the new reference
+                    if (p_it > 0 &&
+                        !ws_wait(&bars[kPEmpty0 + ((p_it - 1) & 1)], ((p_it - 1) >> 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    pa_tc::fence_after_sync();
+                    const float corr = raise ? exp2_approx(old_ref - m_ref) : 1.f;
+                    if (raise) l *= corr;
+#pragma unroll 1
+                    for (int cc = 0; cc < kD / 32; ++cc) {
+                        float o[32];
+                        pa_tc::tmem_ld32(od + cc * 32, o);
+                        pa_tc::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= corr;
+                        pa_tc::tmem_st32(od + cc * 32, o);
+                    }
+                }
+                // this step's P buffer was last read by the P.V two steps back
+                const int pb = p_it & 1;
+                if (p_it >= 2 && !ws_wait(&bars[kPEmpty0 + pb], ((p_it >> 1) - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                pa_tc::fence_after_sync();
+                const uint32_t ph = tP + pb * 64 + lane_sel, pl = ph + 32;
+                // weight = exp2(x * xs - ref): raw scores with xs = scale on the
+                // fast path, already scaled (and masked) scores with xs = 1 otherwise
+                const float nref = -ref, xs = fast ? sl : 1.f;
+                float sum = 0.f;
+                auto weights = [&](const float (&x)[32], uint32_t col) {
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = exp2_approx(fmaf(x[2 * e], xs, nref));
+                        const float p1 = exp2_approx(fmaf(x[2 * e + 1], xs, nref));
+                        sum += p0 + p1;
+                        hi[e] = pa_dev::pack_bf16(p0, p1);
+                        lo[e] = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(hi[e]), p1 - pa_dev::bf16_hi(hi[e]));
+                    }
+                    pa_tc::tmem_st16u(ph + col, hi);
+                    pa_tc::tmem_st16u(pl + col, lo);
+                };
+                weights(sa, 0);                                 // keys 0..31 of the step
+                weights(sb32, 16);                              // keys 32..63
+                pa_tc::tmem_wait_st();
+                l += sum;
+                pa_tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ws_arrive(&bars[kPFull0 + pb]);
+                // the previous item's rows, while this item's P.V runs
+                if (j == 0 && pend.live && !write_partial()) {
+                    ok = false;
+                    break;
+                }
             }
+            if (!ok) break;
+            pend.live = true;
+            pend.kk = kk;
+            pend.row_ok = row_ok;
+            pend.row_n = row_n;
+            pend.slot = row_ok ? (static_cast<size_t>(p.g_spart_base[it.grp]) +
+                                  static_cast<size_t>(row_m) * it.nC + it.chunk) * Hkv + it.h : 0;
+            pend.m = m_ref;
+            pend.l = l;
         }
-        if (row_ok) {
-            p.spart_ml[(slot * G + row_n) * 2] = m_ref;
-            p.spart_ml[(slot * G + row_n) * 2 + 1] = l;
-        }
-        (void)row_s;
-        pa_tc::fence_before_sync();
-        __syncthreads();                                   // TMEM and stages are reused by the next item
-        pa_tc::fence_after_sync();
+        if (ok && pend.live && !write_partial()) ok = false;
     }
-    if (!ok && tid == 0) pa_dev::record_error(p.err, PA_ERR_CUDA);
-    pa_tc::cp_wait<0>();
+    if (!ok) {
+        *abort_flag = 1;
+        if (lane == 0) pa_dev::record_error(p.err, PA_ERR_CUDA);
+    }
     pa_tc::fence_before_sync();
     __syncthreads();
     pa_tc::fence_after_sync();
-    if (warp == 0) pa_tc::tmem_free<kTmemCols>(tmem);
+    if (warp == 0) pa_tc::tmem_free<kWsTmemCols>(tmem);
 }
 
 // ------------------------------------------------------------ prefill ---
@@ -711,11 +929,12 @@ int launch_shared_tc(pa_pool* pool, const DecodeParams& p, cudaStream_t st) {
     const int rc = ensure_tensor_maps(pool);
     if (rc != PA_OK) return rc;
     if (cudaFuncSetAttribute(shared_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+                             static_cast<int>(kWsSmemBytes)) != cudaSuccess)
         return PA_ERR_CUDA;
-    const int grid = p.n_shared_items < 2 * pool->num_sms ? p.n_shared_items : 2 * pool->num_sms;
-    const cudaError_t e = launch_pdl(shared_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, p,
-                                     pool->kmap, pool->vmap);
+    // one CTA per SM: the split pass of the private suffixes fills the rest of each SM
+    const int grid = p.n_shared_items < pool->num_sms ? p.n_shared_items : pool->num_sms;
+    const cudaError_t e = launch_pdl(shared_tc_kernel, dim3(grid), dim3(kWsThreads), kWsSmemBytes,
+                                     st, p, pool->kmap, pool->vmap);
     count_launch();
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
