@@ -528,8 +528,8 @@ def main():
                     help="--impl reference: total oracle seconds over warm-up and timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.workload == "prefill" and args.kv_dtype not in (None, "bf16"):
-        ap.error("the prefill workload runs on bf16 pools only")
+    if args.workload == "prefill" and args.kv_dtype == "f32":
+        ap.error("the prefill workload runs on bf16 and fp8 pools")
     if args.impl == "reference":
         return run_reference(args)
     from paged_kv_cache_253_gb300 import build

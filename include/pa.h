@@ -220,10 +220,12 @@ int pa_decode(pa_pool *pool, const void *q, int num_seqs, int num_q_heads,
  * pa_decode.  Each slot must be the slot of position context_lens[s] - 1 of
  * sequence s (the token the decode of s reads last); otherwise nothing is
  * written for it and PA_ERR_INVALID_ARG is recorded on the device.  On the
- * bf16 tensor-core path the write is done inside the decode kernel by the warp
- * that reads that block (one launch fewer per step); other shapes, and fp8
- * pools, run pa_append_kv and pa_decode back to back.  Copy-on-write copies, if any,
- * must be issued before (pa_copy_blocks). */
+ * tensor-core path (bf16 pools, and fp8 pools whose codes the kernel widens)
+ * the write is done inside the decode kernel by the warp that reads that block
+ * (one launch fewer per step; an fp8 pool's codes are quantized there exactly
+ * as pa_append_kv quantizes them); other shapes run pa_append_kv and pa_decode
+ * back to back.  Copy-on-write copies, if any, must be issued before
+ * (pa_copy_blocks). */
 int pa_append_decode(pa_pool *pool, const void *k, const void *v, const int64_t *slot_mapping,
                      const void *q, int num_seqs, int num_q_heads, const int32_t *block_tables,
                      int max_blocks_per_seq, const int32_t *context_lens, float scale,
@@ -314,8 +316,11 @@ int pa_decode_noalloc(pa_pool *pool, const void *q, int num_seqs, int num_q_head
  *   block_tables  device int32 [S][max_blocks_per_seq]
  *   context_lens  device int32 [S]: L after the chunk's append, L >= n
  *   out           device [T][num_q_heads][head_dim] of out_dtype (8-byte aligned)
- * Requires a bf16 pool (else PA_ERR_DTYPE), block_size % 16 == 0 and
- * head_dim 64/128/256 (else PA_ERR_UNSUPPORTED).  One kernel launch: one CTA per
+ * Requires a bf16 or fp8 pool (else PA_ERR_DTYPE), block_size % 16 == 0
+ * and head_dim 64/128/256 (else PA_ERR_UNSUPPORTED).  An fp8 pool's codes are
+ * widened exactly to f16 and the bf16 queries re-rounded to f16 (exact for
+ * magnitudes 2^-17 .. 65504); products are summed in fp32, k_scale is applied
+ * to the scores and v_scale to the outputs (mma.sync kernel).  One kernel launch: one CTA per
  * (query rows, KV head, sequence) streams the keys up to its last row's
  * position through shared memory once for all its rows: 128 rows on the
  * tcgen05 tensor cores (TMA-staged keys/values, TMEM accumulators) for 16-token

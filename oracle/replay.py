@@ -143,6 +143,21 @@ def replay(wl, values, *, run_step=True):
     return st
 
 
+def _pools_for(wl, st, bt):
+    """The pools the attention reads and the tables into them: the stored bits
+    as they are, or for an fp8 pool the values its codes stand for (code value
+    times the K or V scale), of the blocks these tables reach only (renumbered
+    so that only those are widened to float64)."""
+    kp, vp = st.k_pool, st.v_pool
+    if wl.dtype != "fp8":
+        return kp, vp, bt
+    used = np.unique(bt[bt >= 0])
+    renum = np.full(kp.shape[0], -1, dtype=np.int32)
+    renum[used] = np.arange(len(used), dtype=np.int32)
+    bt = np.where(bt >= 0, renum[np.maximum(bt, 0)], -1).astype(np.int32)
+    return fp8.dequantize(kp[used], wl.kv_scales[0]), fp8.dequantize(vp[used], wl.kv_scales[1]), bt
+
+
 def attention(wl, values, st, seqs=None, threads=1):
     """float64 decode attention for all batch entries (or the listed ones)."""
     q = values_to_numpy(values["q"])
@@ -152,16 +167,7 @@ def attention(wl, values, st, seqs=None, threads=1):
     if seqs is not None:
         seqs = np.asarray(seqs, dtype=np.int64)
         q, bt, lens = q[seqs], bt[seqs], lens[seqs]
-    kp, vp = st.k_pool, st.v_pool
-    if wl.dtype == "fp8":
-        # the values the codes stand for, of the blocks these tables reach
-        # (renumbered so that only those are widened to float64)
-        used = np.unique(bt[bt >= 0])
-        renum = np.full(kp.shape[0], -1, dtype=np.int32)
-        renum[used] = np.arange(len(used), dtype=np.int32)
-        bt = np.where(bt >= 0, renum[np.maximum(bt, 0)], -1).astype(np.int32)
-        kp = fp8.dequantize(kp[used], wl.kv_scales[0])
-        vp = fp8.dequantize(vp[used], wl.kv_scales[1])
+    kp, vp, bt = _pools_for(wl, st, bt)
     return paged_decode(q, kp, vp, bt, lens, wl.scale, wl.num_kv_heads, threads=threads)
 
 
@@ -179,5 +185,5 @@ def prefill_attention(wl, values, st, seqs=None, threads=1):
         n = cu[seqs + 1] - cu[seqs]
         q, bt, lens = q[rows], bt[seqs], lens[seqs]
         cu = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
-    return paged_prefill(q, st.k_pool, st.v_pool, bt, cu, lens, wl.scale, wl.num_kv_heads,
-                         threads=threads)
+    kp, vp, bt = _pools_for(wl, st, bt)
+    return paged_prefill(q, kp, vp, bt, cu, lens, wl.scale, wl.num_kv_heads, threads=threads)

@@ -431,7 +431,7 @@ int pa_decode_shared(pa_pool* pool, const void* q, int num_seqs, int num_q_heads
                                                !group_shared_blocks)))
         return PA_ERR_INVALID_ARG;
     const int Hkv = pool->kv_heads, G = num_q_heads / Hkv, B = pool->block_size;
-    const bool tensor_path = pool->dtype == PA_BF16 && B % 16 == 0 && G <= 8 &&
+    const bool tensor_path = (pool->dtype == PA_BF16 || pool->dtype == PA_FP8E4M3) && B % 16 == 0 && G <= 8 &&
                              (pool->head_dim == 64 || pool->head_dim == 128 || pool->head_dim == 256);
     // validate and keep groups of at least two members with a shared span
     std::vector<char> seen(num_seqs, 0);

@@ -433,7 +433,6 @@ template <int D, bool FUSE, bool F8 = false, int BS = 0>
 __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, int tok0,
                                           int tok1, int L, float* sm_o, float* sm_m,
                                           float* sm_l) {
-    static_assert(!(F8 && FUSE), "an fp8 pool appends in its own (quantizing) kernel");
     constexpr int NJ = D / 32, NT = D / 16;
     constexpr int ES = F8 ? 1 : 2;        // bytes per pool element
     constexpr int OS = D + 4;             // padded row stride of the merge buffer
@@ -555,7 +554,40 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
     // tile ahead of the tile being widened and computed, so that every warp
     // keeps two tiles' loads in flight (at one byte per element a tile is half
     // the bytes of a bf16 tile, and one tile in flight per warp left HBM idle).
-    auto walk_f8 = [&]() {
+    //
+    // Fused append into an fp8 pool: the warp that owns the block holding
+    // position L-1 quantizes the new token's bf16 key row and value column
+    // (code = e4m3(fl32(x / scale)), the arithmetic of the quantizing append)
+    // and writes the codes before its first load; its tiles are then loaded
+    // through L2 (ld.global.cg), so it reads its own writes.
+    auto append_f8 = [&]() {
+        const int phys = __ldg(table + lb_last);
+        const int64_t new_slot = __ldg(p.new_slots + s);
+        const int off = (L - 1) - lb_last * B;
+        if (phys < 0 || phys >= p.num_blocks || new_slot < 0) return;   // the walk records a bad id
+        if (new_slot != static_cast<int64_t>(phys) * B + off) {
+            if (lane == 0) record_error(p.err, PA_ERR_INVALID_ARG);     // not this sequence's slot
+            return;
+        }
+        const size_t tile = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems;
+        unsigned char* kw = const_cast<unsigned char*>(static_cast<const unsigned char*>(p.k)) + tile +
+                            static_cast<size_t>(off) * D;
+        unsigned char* vw = const_cast<unsigned char*>(static_cast<const unsigned char*>(p.v)) + tile + off;
+        const uint16_t* ks = static_cast<const uint16_t*>(p.new_k) + new_row;
+        const uint16_t* vs = static_cast<const uint16_t*>(p.new_v) + new_row;
+        auto bf = [](uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); };
+        for (int i = lane; i < D / 2; i += 32) {
+            const uint32_t kc = pa_dev::e4m3x2_from_f32(__fdiv_rn(bf(__ldg(ks + 2 * i)), p.k_scale),
+                                                        __fdiv_rn(bf(__ldg(ks + 2 * i + 1)), p.k_scale));
+            reinterpret_cast<uint16_t*>(kw)[i] = static_cast<uint16_t>(kc);
+            const uint32_t vc = pa_dev::e4m3x2_from_f32(__fdiv_rn(bf(__ldg(vs + 2 * i)), p.v_scale),
+                                                        __fdiv_rn(bf(__ldg(vs + 2 * i + 1)), p.v_scale));
+            vw[static_cast<size_t>(2 * i) * B] = static_cast<unsigned char>(vc);
+            vw[static_cast<size_t>(2 * i + 1) * B] = static_cast<unsigned char>(vc >> 8);
+        }
+    };
+    auto walk_f8 = [&](auto cg_tag) {
+        constexpr bool CG = decltype(cg_tag)::value;
         const unsigned char* kb = static_cast<const unsigned char*>(p.k);
         const unsigned char* vb = static_cast<const unsigned char*>(p.v);
         const int nunits = nblk * nsub;
@@ -591,13 +623,17 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
             const unsigned char* vt = vb + tile + sub * 16 + 4 * c;
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
-                rk0[j] = pa_dev::ld_stream8(kt + r0 * D + (4 * j + c) * 8);
-                rk1[j] = pa_dev::ld_stream8(kt + r1 * D + (4 * j + c) * 8);
+                rk0[j] = CG ? pa_dev::ld_cg8(kt + r0 * D + (4 * j + c) * 8)
+                            : pa_dev::ld_stream8(kt + r0 * D + (4 * j + c) * 8);
+                rk1[j] = CG ? pa_dev::ld_cg8(kt + r1 * D + (4 * j + c) * 8)
+                            : pa_dev::ld_stream8(kt + r1 * D + (4 * j + c) * 8);
             }
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                rv0[t] = pa_dev::ld_stream4(vt + static_cast<size_t>(16 * t + g) * B);
-                rv1[t] = pa_dev::ld_stream4(vt + static_cast<size_t>(16 * t + g + 8) * B);
+                rv0[t] = CG ? pa_dev::ld_cg4(vt + static_cast<size_t>(16 * t + g) * B)
+                            : pa_dev::ld_stream4(vt + static_cast<size_t>(16 * t + g) * B);
+                rv1[t] = CG ? pa_dev::ld_cg4(vt + static_cast<size_t>(16 * t + g + 8) * B)
+                            : pa_dev::ld_stream4(vt + static_cast<size_t>(16 * t + g + 8) * B);
             }
             r_valid = nv;
         };
@@ -626,7 +662,13 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
         }
     };
     if constexpr (F8) {
-        walk_f8();
+        // with a fused append every warp of the kernel loads through L2 (one
+        // walk compiled instead of two: the fp8 walk has no registers to spare)
+        if (own_new) {
+            append_f8();
+            __syncwarp();                         // the codes are written before any lane loads them
+        }
+        walk_f8(std::integral_constant<bool, FUSE>{});
     } else {
         // only the warp that writes the new token needs loads that see it
         if (own_new) walk(std::true_type{});
@@ -667,11 +709,20 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
 // with the same token permutation and d-chunk split as the private path, so
 // K and V^T fragments are read with 16-byte / 8-byte loads.  The item's
 // (acc, max, sum) per (member, head) go to the shared-partial slots.
-template <int D>
+//
+// F8 (fp8 pool): the staged tiles hold e4m3 codes (half the bytes; key rows
+// with 16-byte chunk c of row r at c ^ (r & 7)), widened to f16 pairs as each
+// fragment is read; the queries are re-rounded to f16, the products are f16
+// mma.sync, P enters as an f16 pair, and v_scale multiplies the partial sums.
+template <int D, bool F8 = false>
 __device__ void shared_item(const DecodeParams& p, int grp, int h, int tile, int chunk,
                             unsigned char* stage_mem) {
     constexpr int NJ = D / 32, NT = D / 16, ND = D / 8;
-    constexpr int UNIT = 64 * D;                    // bytes per staged tile pair
+    constexpr int ES = F8 ? 1 : 2;                  // bytes per pool element
+    constexpr int UNIT = 32 * ES * D;               // bytes per staged tile pair
+    constexpr int KB = 16 * ES * D;                 // K part of a pair
+    constexpr int NCH = ES * D / 16;                // 16-byte chunks per key row (fp8)
+    constexpr int SWZ = NCH < 8 ? NCH - 1 : 7;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gi = lane >> 2, c = lane & 3;
     const int G = p.G, B = p.B;
@@ -703,6 +754,10 @@ __device__ void shared_item(const DecodeParams& p, int grp, int h, int tile, int
         for (int j = 0; j < NJ; ++j) {
             qa[j] = okA ? __ldg(reinterpret_cast<const uint4*>(rowA + (4 * j + c) * 8)) : make_uint4(0u, 0u, 0u, 0u);
             qb[j] = okB ? __ldg(reinterpret_cast<const uint4*>(rowB + (4 * j + c) * 8)) : make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (F8) {
+                qa[j] = bf16x8_to_f16x8(qa[j]);
+                qb[j] = bf16x8_to_f16x8(qb[j]);
+            }
         }
     }
     float o[ND][4];
@@ -713,9 +768,9 @@ __device__ void shared_item(const DecodeParams& p, int grp, int h, int tile, int
     const int r0 = 4 * (gi >> 1) + (gi & 1), r1 = r0 + 2;
 
     const int32_t* table = p.tables + static_cast<size_t>(p.g_members[moff]) * p.max_blocks;
-    const uint16_t* kpool = static_cast<const uint16_t*>(p.k);
-    const uint16_t* vpool = static_cast<const uint16_t*>(p.v);
-    const size_t tile_elems = static_cast<size_t>(B) * D;
+    const char* kpool = static_cast<const char*>(p.k);
+    const char* vpool = static_cast<const char*>(p.v);
+    const size_t tile_bytes = static_cast<size_t>(B) * D * ES;
     const uint32_t stage_s = static_cast<uint32_t>(__cvta_generic_to_shared(stage_mem));
     constexpr int NS = kSharedStages, CH = kSharedUnitsPerSync;
     unsigned valid = 0;
@@ -731,17 +786,26 @@ __device__ void shared_item(const DecodeParams& p, int grp, int h, int tile, int
         if (phys < 0 || phys >= p.num_blocks) {
             if (tid == 0) record_error(p.err, PA_ERR_BAD_BLOCK_ID);
         } else {
-            const size_t tl = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems;
-            const uint16_t* kg = kpool + tl + static_cast<size_t>(sub) * 16 * D;
-            const uint16_t* vg = vpool + tl + sub * 16;
-            const uint32_t ks = stage_s + st * UNIT, vs = ks + 32 * D;
-            for (int q = tid; q < 2 * D; q += kThreads) {
-                const int r = q / (D / 8), ch = q - r * (D / 8);
-                cp_async16(ks + r * (2 * D) + ((ch ^ ((r & 1) << 2)) << 4), kg + r * D + ch * 8);
-            }
-            for (int q = tid; q < 2 * D; q += kThreads) {
-                const int d = q >> 1, half = q & 1;
-                cp_async16(vs + d * 32 + half * 16, vg + static_cast<size_t>(d) * B + half * 8);
+            const size_t tl = (static_cast<size_t>(phys) * p.Hkv + h) * tile_bytes;
+            const char* kg = kpool + tl + static_cast<size_t>(sub) * 16 * D * ES;
+            const char* vg = vpool + tl + sub * 16 * ES;
+            const uint32_t ks = stage_s + st * UNIT, vs = ks + KB;
+            if constexpr (F8) {
+                for (int q = tid; q < 16 * NCH; q += kThreads) {     // K: 16 rows x D/16 chunks
+                    const int r = q / NCH, ch = q - r * NCH;
+                    cp_async16(ks + r * D + ((ch ^ (r & SWZ)) << 4), kg + r * D + ch * 16);
+                }
+                for (int d = tid; d < D; d += kThreads)              // V^T: D rows of 16 codes
+                    cp_async16(vs + d * 16, vg + static_cast<size_t>(d) * B);
+            } else {
+                for (int q = tid; q < 2 * D; q += kThreads) {
+                    const int r = q / (D / 8), ch = q - r * (D / 8);
+                    cp_async16(ks + r * (2 * D) + ((ch ^ ((r & 1) << 2)) << 4), kg + r * D * 2 + ch * 16);
+                }
+                for (int q = tid; q < 2 * D; q += kThreads) {
+                    const int d = q >> 1, half = q & 1;
+                    cp_async16(vs + d * 32 + half * 16, vg + static_cast<size_t>(d) * B * 2 + half * 16);
+                }
             }
             valid |= 1u << st;
         }
@@ -784,12 +848,23 @@ __device__ void shared_item(const DecodeParams& p, int grp, int h, int tile, int
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
                 const int ch = 4 * j + c;
-                const uint4 ka = *reinterpret_cast<const uint4*>(ks + r0 * (2 * D) + ((ch ^ ((r0 & 1) << 2)) << 4));
-                const uint4 kb = *reinterpret_cast<const uint4*>(ks + r1 * (2 * D) + ((ch ^ ((r1 & 1) << 2)) << 4));
-                pa_dev::mma_bf16_16816(sA[2 * w], qa[j].x, qb[j].x, qa[j].y, qb[j].y, ka.x, ka.y);
-                pa_dev::mma_bf16_16816(sB[2 * w], qa[j].z, qb[j].z, qa[j].w, qb[j].w, ka.z, ka.w);
-                pa_dev::mma_bf16_16816(sA[2 * w + 1], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kb.x, kb.y);
-                pa_dev::mma_bf16_16816(sB[2 * w + 1], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kb.z, kb.w);
+                if constexpr (F8) {
+                    const uint4 ka = widen8(*reinterpret_cast<const uint2*>(
+                        ks + r0 * D + (((ch >> 1) ^ (r0 & SWZ)) << 4) + (ch & 1) * 8));
+                    const uint4 kb = widen8(*reinterpret_cast<const uint2*>(
+                        ks + r1 * D + (((ch >> 1) ^ (r1 & SWZ)) << 4) + (ch & 1) * 8));
+                    pa_dev::mma_f16_16816(sA[2 * w], qa[j].x, qb[j].x, qa[j].y, qb[j].y, ka.x, ka.y);
+                    pa_dev::mma_f16_16816(sB[2 * w], qa[j].z, qb[j].z, qa[j].w, qb[j].w, ka.z, ka.w);
+                    pa_dev::mma_f16_16816(sA[2 * w + 1], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kb.x, kb.y);
+                    pa_dev::mma_f16_16816(sB[2 * w + 1], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kb.z, kb.w);
+                } else {
+                    const uint4 ka = *reinterpret_cast<const uint4*>(ks + r0 * (2 * D) + ((ch ^ ((r0 & 1) << 2)) << 4));
+                    const uint4 kb = *reinterpret_cast<const uint4*>(ks + r1 * (2 * D) + ((ch ^ ((r1 & 1) << 2)) << 4));
+                    pa_dev::mma_bf16_16816(sA[2 * w], qa[j].x, qb[j].x, qa[j].y, qb[j].y, ka.x, ka.y);
+                    pa_dev::mma_bf16_16816(sB[2 * w], qa[j].z, qb[j].z, qa[j].w, qb[j].w, ka.z, ka.w);
+                    pa_dev::mma_bf16_16816(sA[2 * w + 1], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kb.x, kb.y);
+                    pa_dev::mma_bf16_16816(sB[2 * w + 1], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kb.z, kb.w);
+                }
             }
         }
         // rows gi ([0], [1]) and gi + 8 ([2], [3]) of each n-tile
@@ -828,19 +903,23 @@ __device__ void shared_item(const DecodeParams& p, int grp, int h, int tile, int
         lb_ = lb_ * crb + sumb;
         ma = na;
         mb = nb;
-        // A fragments of P for the two 16-token k-steps (bf16 high and low parts)
+        // A fragments of P for the two 16-token k-steps (high and low parts:
+        // bf16, or f16 for the f16 products of an fp8 pool)
         uint32_t ah[2][4], al[2][4];
+        auto pk = [](float x, float y) { return F8 ? pa_dev::pack_f16(x, y) : pa_dev::pack_bf16(x, y); };
+        auto lo16 = [](uint32_t v) { return F8 ? pa_dev::f16_lo(v) : pa_dev::bf16_lo(v); };
+        auto hi16 = [](uint32_t v) { return F8 ? pa_dev::f16_hi(v) : pa_dev::bf16_hi(v); };
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
             const int n0 = 2 * w, n1 = 2 * w + 1;
-            ah[w][0] = pa_dev::pack_bf16(pa[2 * n0], pa[2 * n0 + 1]);
-            ah[w][1] = pa_dev::pack_bf16(pb[2 * n0], pb[2 * n0 + 1]);
-            ah[w][2] = pa_dev::pack_bf16(pa[2 * n1], pa[2 * n1 + 1]);
-            ah[w][3] = pa_dev::pack_bf16(pb[2 * n1], pb[2 * n1 + 1]);
-            al[w][0] = pa_dev::pack_bf16(pa[2 * n0] - pa_dev::bf16_lo(ah[w][0]), pa[2 * n0 + 1] - pa_dev::bf16_hi(ah[w][0]));
-            al[w][1] = pa_dev::pack_bf16(pb[2 * n0] - pa_dev::bf16_lo(ah[w][1]), pb[2 * n0 + 1] - pa_dev::bf16_hi(ah[w][1]));
-            al[w][2] = pa_dev::pack_bf16(pa[2 * n1] - pa_dev::bf16_lo(ah[w][2]), pa[2 * n1 + 1] - pa_dev::bf16_hi(ah[w][2]));
-            al[w][3] = pa_dev::pack_bf16(pb[2 * n1] - pa_dev::bf16_lo(ah[w][3]), pb[2 * n1 + 1] - pa_dev::bf16_hi(ah[w][3]));
+            ah[w][0] = pk(pa[2 * n0], pa[2 * n0 + 1]);
+            ah[w][1] = pk(pb[2 * n0], pb[2 * n0 + 1]);
+            ah[w][2] = pk(pa[2 * n1], pa[2 * n1 + 1]);
+            ah[w][3] = pk(pb[2 * n1], pb[2 * n1 + 1]);
+            al[w][0] = pk(pa[2 * n0] - lo16(ah[w][0]), pa[2 * n0 + 1] - hi16(ah[w][0]));
+            al[w][1] = pk(pb[2 * n0] - lo16(ah[w][1]), pb[2 * n0 + 1] - hi16(ah[w][1]));
+            al[w][2] = pk(pa[2 * n1] - lo16(ah[w][2]), pa[2 * n1 + 1] - hi16(ah[w][2]));
+            al[w][3] = pk(pb[2 * n1] - lo16(ah[w][3]), pb[2 * n1 + 1] - hi16(ah[w][3]));
         }
 #pragma unroll
         for (int t = 0; t < ND; ++t) {
@@ -849,12 +928,18 @@ __device__ void shared_item(const DecodeParams& p, int grp, int h, int tile, int
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
             if (!(w == 0 ? v0ok : v1ok)) continue;
-            const unsigned char* vs = stage_mem + ((u + w) % NS) * UNIT + 32 * D;
+            const unsigned char* vs = stage_mem + ((u + w) % NS) * UNIT + KB;
 #pragma unroll
             for (int t = 0; t < ND; ++t) {
-                const uint2 v = *reinterpret_cast<const uint2*>(vs + (8 * t + gi) * 32 + 8 * c);
-                pa_dev::mma_bf16_16816(o[t], ah[w][0], ah[w][1], ah[w][2], ah[w][3], v.x, v.y);
-                pa_dev::mma_bf16_16816(o[t], al[w][0], al[w][1], al[w][2], al[w][3], v.x, v.y);
+                if constexpr (F8) {
+                    const uint2 v = widen4(*reinterpret_cast<const uint32_t*>(vs + (8 * t + gi) * 16 + 4 * c));
+                    pa_dev::mma_f16_16816(o[t], ah[w][0], ah[w][1], ah[w][2], ah[w][3], v.x, v.y);
+                    pa_dev::mma_f16_16816(o[t], al[w][0], al[w][1], al[w][2], al[w][3], v.x, v.y);
+                } else {
+                    const uint2 v = *reinterpret_cast<const uint2*>(vs + (8 * t + gi) * 32 + 8 * c);
+                    pa_dev::mma_bf16_16816(o[t], ah[w][0], ah[w][1], ah[w][2], ah[w][3], v.x, v.y);
+                    pa_dev::mma_bf16_16816(o[t], al[w][0], al[w][1], al[w][2], al[w][3], v.x, v.y);
+                }
             }
         }
       }
@@ -872,7 +957,8 @@ __device__ void shared_item(const DecodeParams& p, int grp, int h, int tile, int
         float* acc = p.spart_acc + slot * GD + static_cast<size_t>(n) * D;
 #pragma unroll
         for (int t = 0; t < ND; ++t)
-            *reinterpret_cast<float2*>(acc + 8 * t + 2 * c) = make_float2(o[t][which], o[t][which + 1]);
+            *reinterpret_cast<float2*>(acc + 8 * t + 2 * c) =
+                make_float2(o[t][which] * p.v_scale, o[t][which + 1] * p.v_scale);
         if (c == 0) {
             p.spart_ml[(slot * G + n) * 2] = m;
             p.spart_ml[(slot * G + n) * 2 + 1] = l;
@@ -915,8 +1001,8 @@ decode_fast_kernel(const DecodeParams p) {
     for (int item = blockIdx.x; item < n_sh + sc.total_items;) {
         if (SHARED && item < n_sh) {
             const int k = item / p.Hkv, hh = item - k * p.Hkv;
-            shared_item<D>(p, p.sh_items[4 * k], hh, p.sh_items[4 * k + 1], p.sh_items[4 * k + 2],
-                           ring);
+            shared_item<D, F8>(p, p.sh_items[4 * k], hh, p.sh_items[4 * k + 1], p.sh_items[4 * k + 2],
+                               ring);
             item = next_item(p, s_flag + 1);
             continue;
         }
@@ -1191,10 +1277,7 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
     const bool fp8 = pool->dtype == PA_FP8E4M3;
     const bool tc_shape = (D == 64 || D == 128 || D == 256) && B % 16 == 0 && G <= 8;
     const bool fast = tc_shape && (pool->dtype == PA_BF16 || fp8);
-    if (fp8) {                  // appends quantize in their own kernel; no shared-prefix items
-        plan->fuse = false;
-        plan->shared = plan->tc = false;
-    }
+    if (fp8) plan->tc = false;      // an fp8 pool's shared items run on the mma.sync form
     plan->fast = fast;
     plan->pool = pool;
     plan->bf16 = pool->dtype == PA_BF16;
@@ -1213,10 +1296,18 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
         const int pt_max = pool->opt_partition_cap >= 0 ? pool->opt_partition_cap
                                                          : (S > pool->num_sms ? kPtMax : 0);
         plan->pt_max = pt_max > 0 ? std::max(plan->pt_min, pt_max / B * B) : 0;
-        if (plan->shared && !plan->tc) {
+        if (plan->shared && !plan->tc && fp8) {
+            if (D == 64) occ = occupancy(decode_fast_kernel<64, true, false, true>, plan->smem);
+            else if (D == 128) occ = occupancy(decode_fast_kernel<128, true, false, true>, plan->smem);
+            else occ = occupancy(decode_fast_kernel<256, true, false, true>, plan->smem);
+        } else if (plan->shared && !plan->tc) {
             if (D == 64) occ = occupancy(decode_fast_kernel<64, true, false>, plan->smem);
             else if (D == 128) occ = occupancy(decode_fast_kernel<128, true, false>, plan->smem);
             else occ = occupancy(decode_fast_kernel<256, true, false>, plan->smem);
+        } else if (fp8 && plan->fuse) {
+            if (D == 64) occ = occupancy(decode_fast_kernel<64, false, true, true>, plan->smem);
+            else if (D == 128) occ = occupancy(decode_fast_kernel<128, false, true, true>, plan->smem);
+            else occ = occupancy(decode_fast_kernel<256, false, true, true>, plan->smem);
         } else if (fp8) {
             if (D == 64) occ = occupancy(decode_fast_kernel<64, false, false, true>, plan->smem);
             else if (D == 128) occ = occupancy(decode_fast_kernel<128, false, false, true>, plan->smem);
@@ -1279,10 +1370,18 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
         if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, false>, grid, block, plan.smem, st, q);
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, false>, grid, block, plan.smem, st, q);
         else e = launch_pdl(decode_fast_kernel<256, false, false>, grid, block, plan.smem, st, q);
+    } else if (plan.fast && plan.shared && plan.fp8) {
+        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, true, false, true>, grid, block, plan.smem, st, p);
+        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, true, false, true>, grid, block, plan.smem, st, p);
+        else e = launch_pdl(decode_fast_kernel<256, true, false, true>, grid, block, plan.smem, st, p);
     } else if (plan.fast && plan.shared) {
         if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, true, false>, grid, block, plan.smem, st, p);
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, true, false>, grid, block, plan.smem, st, p);
         else e = launch_pdl(decode_fast_kernel<256, true, false>, grid, block, plan.smem, st, p);
+    } else if (plan.fast && plan.fp8 && plan.fuse) {
+        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, true, true>, grid, block, plan.smem, st, p);
+        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, true, true>, grid, block, plan.smem, st, p);
+        else e = launch_pdl(decode_fast_kernel<256, false, true, true>, grid, block, plan.smem, st, p);
     } else if (plan.fast && plan.fp8) {
         if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, false, true>, grid, block, plan.smem, st, p);
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, false, true>, grid, block, plan.smem, st, p);

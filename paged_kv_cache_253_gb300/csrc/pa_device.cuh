@@ -76,6 +76,12 @@ __device__ __forceinline__ uint4 ld_cg16(const void* p) {
                  : "l"(p) : "memory");
     return r;
 }
+__device__ __forceinline__ uint32_t ld_cg4(const void* p) {
+    uint32_t r;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
+    return r;
+}
+
 __device__ __forceinline__ uint2 ld_cg8(const void* p) {
     uint2 r;
     asm volatile("ld.global.cg.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p) : "memory");

@@ -54,6 +54,7 @@ struct DecodeParams {
     int* err;
     float scale_log2;           // scale * log2(e) (* k_scale for an fp8 pool)
     float v_scale;              // factor on the value sums (fp8 pool's v_scale, else 1)
+    float k_scale;              // fp8 pool's k_scale (quantizing a fused append), else 1
     int S, Hq, Hkv, G, D, B, num_blocks, max_blocks;
     int out_bf16;
     int items_target;           // wanted number of work items (fast path)
@@ -90,14 +91,15 @@ struct DecodeParams {
 // Everything one prefill launch needs (pa_prefill), passed by value.
 struct PrefillParams {
     const uint16_t* q;          // [T][Hq][D] bf16
-    const uint16_t* k;          // pool K
-    const uint16_t* v;          // pool V^T tiles
+    const void* k;              // pool K (bf16 values or e4m3 codes)
+    const void* v;              // pool V^T tiles
     const int32_t* cu_q;        // [S + 1] first query row of each sequence
     const int32_t* tables;      // [S][max_blocks]
     const int32_t* lens;        // [S] context length after the chunk's append
     void* out;                  // [T][Hq][D]
     int* err;
-    float scale_log2;
+    float scale_log2;           // scale * log2(e) (* k_scale for an fp8 pool)
+    float v_scale;              // factor on the outputs (fp8 pool's v_scale, else 1)
     int T, S, Hq, Hkv, G, B, num_blocks, max_blocks;
     int max_q;                  // longest chunk the launch was sized for
     int out_bf16;
@@ -113,6 +115,7 @@ inline void decode_scales(const pa_pool* pool, float scale, DecodeParams* p) {
     p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 *
                                        (f8 ? static_cast<double>(pool->k_scale) : 1.0));
     p->v_scale = f8 ? pool->v_scale : 1.f;
+    p->k_scale = f8 ? pool->k_scale : 1.f;
 }
 
 // Decode workspace header: ticket[2], 2 spare ints, the published schedule

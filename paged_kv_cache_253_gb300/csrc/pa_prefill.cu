@@ -16,6 +16,14 @@
 // 16-byte d chunks): S = Q K^T by mma.sync m16n8k16 (bf16, fp32 accumulate),
 // causal and length masks, online softmax per row, O += P V with P as a bf16
 // high + low pair.  Each row's normalised output is written directly.
+//
+// fp8 (e4m3) pools (F8): the units hold codes (one byte per element, half the
+// bytes), staged the same way; each thread widens its fragments to f16 pairs
+// in registers (exact: every e4m3 value is an f16 value), the queries are
+// re-rounded to f16 once (exact for bf16 magnitudes 2^-17 .. 65504), the
+// products run as f16 mma.sync with fp32 accumulation and P enters as an f16
+// high + low pair; k_scale is folded into the score factor and v_scale
+// multiplies the outputs.
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -34,10 +42,27 @@ constexpr int kStagesP = 8;               // staged 16-token units
 constexpr int kPerSyncP = 4;              // units consumed per barrier (even: 32-token steps)
 static_assert(kStagesP > kPerSyncP && kPerSyncP % 2 == 0, "prefill pipeline shape");
 
-template <int D>
+// Eight e4m3 codes widened to four f16 pairs, four to two, and eight bf16
+// values re-rounded to f16.
+__device__ __forceinline__ uint4 f8_widen8(uint2 c) {
+    return make_uint4(pa_dev::e4m3x2_to_f16x2(c.x), pa_dev::e4m3x2_to_f16x2(c.x >> 16),
+                      pa_dev::e4m3x2_to_f16x2(c.y), pa_dev::e4m3x2_to_f16x2(c.y >> 16));
+}
+__device__ __forceinline__ uint2 f8_widen4(uint32_t c) {
+    return make_uint2(pa_dev::e4m3x2_to_f16x2(c), pa_dev::e4m3x2_to_f16x2(c >> 16));
+}
+__device__ __forceinline__ uint32_t bf16x2_f16x2(uint32_t x) {
+    return pa_dev::pack_f16(pa_dev::bf16_lo(x), pa_dev::bf16_hi(x));
+}
+
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreadsP, 2) prefill_kernel(const PrefillParams p) {
     constexpr int NJ = D / 32, ND = D / 8;
-    constexpr int UNIT = 64 * D;                      // K 16 x D + V^T D x 16, bf16
+    constexpr int ES = F8 ? 1 : 2;                    // bytes per pool element
+    constexpr int UNIT = 32 * ES * D;                 // K 16 x D + V^T D x 16
+    constexpr int KB = 16 * ES * D;                   // K part of a unit
+    constexpr int NCH = ES * D / 16;                  // 16-byte chunks per key row
+    constexpr int SWZ = NCH < 8 ? NCH - 1 : 7;        // fp8 key rows: chunk c of row r at c ^ (r & SWZ)
     extern __shared__ __align__(128) unsigned char stage_mem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gi = lane >> 2, c = lane & 3;
@@ -85,6 +110,12 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_kernel(const PrefillPara
         for (int j = 0; j < NJ; ++j) {
             qa[j] = okA ? __ldg(reinterpret_cast<const uint4*>(rowA + (4 * j + c) * 8)) : make_uint4(0u, 0u, 0u, 0u);
             qb[j] = okB ? __ldg(reinterpret_cast<const uint4*>(rowB + (4 * j + c) * 8)) : make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (F8) {
+                qa[j] = make_uint4(bf16x2_f16x2(qa[j].x), bf16x2_f16x2(qa[j].y), bf16x2_f16x2(qa[j].z),
+                                   bf16x2_f16x2(qa[j].w));
+                qb[j] = make_uint4(bf16x2_f16x2(qb[j].x), bf16x2_f16x2(qb[j].y), bf16x2_f16x2(qb[j].z),
+                                   bf16x2_f16x2(qb[j].w));
+            }
         }
     }
     float o[ND][4];
@@ -107,17 +138,26 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_kernel(const PrefillPara
         if (phys < 0 || phys >= p.num_blocks) {
             if (tid == 0) pa_dev::record_error(p.err, PA_ERR_BAD_BLOCK_ID);
         } else {
-            const size_t tl = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems;
-            const uint16_t* kg = p.k + tl + static_cast<size_t>(sub) * 16 * D;
-            const uint16_t* vg = p.v + tl + sub * 16;
-            const uint32_t ks = stage_s + st * UNIT, vs = ks + 32 * D;
-            for (int q = tid; q < 2 * D; q += kThreadsP) {       // K: 16 rows x D/8 chunks
-                const int r = q / (D / 8), ch = q - r * (D / 8);
-                pa_dev::cp_async16(ks + r * (2 * D) + ((ch ^ ((r & 1) << 2)) << 4), kg + r * D + ch * 8);
-            }
-            for (int q = tid; q < 2 * D; q += kThreadsP) {       // V^T: D rows x 2 halves
-                const int d = q >> 1, half = q & 1;
-                pa_dev::cp_async16(vs + d * 32 + half * 16, vg + static_cast<size_t>(d) * B + half * 8);
+            const size_t tl = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems * ES;
+            const char* kg = static_cast<const char*>(p.k) + tl + static_cast<size_t>(sub) * 16 * D * ES;
+            const char* vg = static_cast<const char*>(p.v) + tl + sub * 16 * ES;
+            const uint32_t ks = stage_s + st * UNIT, vs = ks + KB;
+            if constexpr (F8) {
+                for (int q = tid; q < 16 * NCH; q += kThreadsP) {    // K: 16 rows x D/16 chunks
+                    const int r = q / NCH, ch = q - r * NCH;
+                    pa_dev::cp_async16(ks + r * D + ((ch ^ (r & SWZ)) << 4), kg + r * D + ch * 16);
+                }
+                for (int d = tid; d < D; d += kThreadsP)             // V^T: D rows of 16 codes
+                    pa_dev::cp_async16(vs + d * 16, vg + static_cast<size_t>(d) * B);
+            } else {
+                for (int q = tid; q < 2 * D; q += kThreadsP) {       // K: 16 rows x D/8 chunks
+                    const int r = q / (D / 8), ch = q - r * (D / 8);
+                    pa_dev::cp_async16(ks + r * (2 * D) + ((ch ^ ((r & 1) << 2)) << 4), kg + r * D * 2 + ch * 16);
+                }
+                for (int q = tid; q < 2 * D; q += kThreadsP) {       // V^T: D rows x 2 halves
+                    const int d = q >> 1, half = q & 1;
+                    pa_dev::cp_async16(vs + d * 32 + half * 16, vg + static_cast<size_t>(d) * B * 2 + half * 16);
+                }
             }
             valid |= 1u << st;
         }
@@ -151,12 +191,24 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_kernel(const PrefillPara
 #pragma unroll
                 for (int j = 0; j < NJ; ++j) {
                     const int ch = 4 * j + c;
-                    const uint4 ka = *reinterpret_cast<const uint4*>(ks + r0 * (2 * D) + ((ch ^ ((r0 & 1) << 2)) << 4));
-                    const uint4 kb = *reinterpret_cast<const uint4*>(ks + r1 * (2 * D) + ((ch ^ ((r1 & 1) << 2)) << 4));
-                    pa_dev::mma_bf16_16816(sA[2 * w], qa[j].x, qb[j].x, qa[j].y, qb[j].y, ka.x, ka.y);
-                    pa_dev::mma_bf16_16816(sB[2 * w], qa[j].z, qb[j].z, qa[j].w, qb[j].w, ka.z, ka.w);
-                    pa_dev::mma_bf16_16816(sA[2 * w + 1], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kb.x, kb.y);
-                    pa_dev::mma_bf16_16816(sB[2 * w + 1], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kb.z, kb.w);
+                    if constexpr (F8) {
+                        // 8 codes: half (ch & 1) of 16-byte chunk ch >> 1 of the row
+                        const uint4 ka = f8_widen8(*reinterpret_cast<const uint2*>(
+                            ks + r0 * D + (((ch >> 1) ^ (r0 & SWZ)) << 4) + (ch & 1) * 8));
+                        const uint4 kb = f8_widen8(*reinterpret_cast<const uint2*>(
+                            ks + r1 * D + (((ch >> 1) ^ (r1 & SWZ)) << 4) + (ch & 1) * 8));
+                        pa_dev::mma_f16_16816(sA[2 * w], qa[j].x, qb[j].x, qa[j].y, qb[j].y, ka.x, ka.y);
+                        pa_dev::mma_f16_16816(sB[2 * w], qa[j].z, qb[j].z, qa[j].w, qb[j].w, ka.z, ka.w);
+                        pa_dev::mma_f16_16816(sA[2 * w + 1], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kb.x, kb.y);
+                        pa_dev::mma_f16_16816(sB[2 * w + 1], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kb.z, kb.w);
+                    } else {
+                        const uint4 ka = *reinterpret_cast<const uint4*>(ks + r0 * (2 * D) + ((ch ^ ((r0 & 1) << 2)) << 4));
+                        const uint4 kb = *reinterpret_cast<const uint4*>(ks + r1 * (2 * D) + ((ch ^ ((r1 & 1) << 2)) << 4));
+                        pa_dev::mma_bf16_16816(sA[2 * w], qa[j].x, qb[j].x, qa[j].y, qb[j].y, ka.x, ka.y);
+                        pa_dev::mma_bf16_16816(sB[2 * w], qa[j].z, qb[j].z, qa[j].w, qb[j].w, ka.z, ka.w);
+                        pa_dev::mma_bf16_16816(sA[2 * w + 1], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kb.x, kb.y);
+                        pa_dev::mma_bf16_16816(sB[2 * w + 1], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kb.z, kb.w);
+                    }
                 }
             }
             // score (row, n-tile nt, column e) is the key at position
@@ -197,8 +249,23 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_kernel(const PrefillPara
             lb = lb * crb + sumb;
             ma = na;
             mb = nb;
-            // A fragments of P for the two 16-token k-steps (bf16 high and low parts)
+            // A fragments of P for the two 16-token k-steps (high and low parts:
+            // bf16, or f16 for an fp8 pool's f16 products)
             uint32_t ah[2][4], al[2][4];
+            if constexpr (F8) {
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int n0 = 2 * w, n1 = 2 * w + 1;
+                    ah[w][0] = pa_dev::pack_f16(pa[2 * n0], pa[2 * n0 + 1]);
+                    ah[w][1] = pa_dev::pack_f16(pb[2 * n0], pb[2 * n0 + 1]);
+                    ah[w][2] = pa_dev::pack_f16(pa[2 * n1], pa[2 * n1 + 1]);
+                    ah[w][3] = pa_dev::pack_f16(pb[2 * n1], pb[2 * n1 + 1]);
+                    al[w][0] = pa_dev::pack_f16(pa[2 * n0] - pa_dev::f16_lo(ah[w][0]), pa[2 * n0 + 1] - pa_dev::f16_hi(ah[w][0]));
+                    al[w][1] = pa_dev::pack_f16(pb[2 * n0] - pa_dev::f16_lo(ah[w][1]), pb[2 * n0 + 1] - pa_dev::f16_hi(ah[w][1]));
+                    al[w][2] = pa_dev::pack_f16(pa[2 * n1] - pa_dev::f16_lo(ah[w][2]), pa[2 * n1 + 1] - pa_dev::f16_hi(ah[w][2]));
+                    al[w][3] = pa_dev::pack_f16(pb[2 * n1] - pa_dev::f16_lo(ah[w][3]), pb[2 * n1 + 1] - pa_dev::f16_hi(ah[w][3]));
+                }
+            } else {
 #pragma unroll
             for (int w = 0; w < 2; ++w) {
                 const int n0 = 2 * w, n1 = 2 * w + 1;
@@ -211,6 +278,7 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_kernel(const PrefillPara
                 al[w][2] = pa_dev::pack_bf16(pa[2 * n1] - pa_dev::bf16_lo(ah[w][2]), pa[2 * n1 + 1] - pa_dev::bf16_hi(ah[w][2]));
                 al[w][3] = pa_dev::pack_bf16(pb[2 * n1] - pa_dev::bf16_lo(ah[w][3]), pb[2 * n1 + 1] - pa_dev::bf16_hi(ah[w][3]));
             }
+            }
 #pragma unroll
             for (int t = 0; t < ND; ++t) {
                 o[t][0] *= cra; o[t][1] *= cra; o[t][2] *= crb; o[t][3] *= crb;
@@ -218,7 +286,7 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_kernel(const PrefillPara
 #pragma unroll
             for (int w = 0; w < 2; ++w) {
                 if (!(w == 0 ? v0ok : v1ok)) continue;
-                const unsigned char* vs = stage_mem + ((u + w) % kStagesP) * UNIT + 32 * D;
+                const unsigned char* vs = stage_mem + ((u + w) % kStagesP) * UNIT + KB;
                 // value columns at or past the context length hold whatever the
                 // block held before: zero them so that 0 * (garbage) stays 0
                 const int tb = 16 * (u + w) + 4 * c;
@@ -227,13 +295,22 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_kernel(const PrefillPara
                 const uint32_t mhi = (tb + 2 < L ? 0x0000ffffu : 0u) | (tb + 3 < L ? 0xffff0000u : 0u);
 #pragma unroll
                 for (int t = 0; t < ND; ++t) {
-                    uint2 v = *reinterpret_cast<const uint2*>(vs + (8 * t + gi) * 32 + 8 * c);
+                    uint2 v;
+                    if constexpr (F8)                          // 4 codes: tokens 4c .. 4c+3 of row d
+                        v = f8_widen4(*reinterpret_cast<const uint32_t*>(vs + (8 * t + gi) * 16 + 4 * c));
+                    else
+                        v = *reinterpret_cast<const uint2*>(vs + (8 * t + gi) * 32 + 8 * c);
                     if (tail) {
                         v.x &= mlo;
                         v.y &= mhi;
                     }
-                    pa_dev::mma_bf16_16816(o[t], ah[w][0], ah[w][1], ah[w][2], ah[w][3], v.x, v.y);
-                    pa_dev::mma_bf16_16816(o[t], al[w][0], al[w][1], al[w][2], al[w][3], v.x, v.y);
+                    if constexpr (F8) {
+                        pa_dev::mma_f16_16816(o[t], ah[w][0], ah[w][1], ah[w][2], ah[w][3], v.x, v.y);
+                        pa_dev::mma_f16_16816(o[t], al[w][0], al[w][1], al[w][2], al[w][3], v.x, v.y);
+                    } else {
+                        pa_dev::mma_bf16_16816(o[t], ah[w][0], ah[w][1], ah[w][2], ah[w][3], v.x, v.y);
+                        pa_dev::mma_bf16_16816(o[t], al[w][0], al[w][1], al[w][2], al[w][3], v.x, v.y);
+                    }
                 }
             }
         }
@@ -247,7 +324,7 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_kernel(const PrefillPara
     }
     auto write_row = [&](int qi, int hq, int which, float l) {
         const size_t row = (static_cast<size_t>(q0 + qi) * p.Hq + hq) * D;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? p.v_scale / l : 0.f;
 #pragma unroll
         for (int t = 0; t < ND; ++t) {
             const int d = 8 * t + 2 * c;
@@ -262,14 +339,14 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_kernel(const PrefillPara
     if (okB) write_row(qiB, h * G + rB % G, 2, lb);
 }
 
-template <int D>
+template <int D, bool F8>
 int launch_prefill_d(const PrefillParams& prm, dim3 grid, cudaStream_t st) {
-    const size_t smem = static_cast<size_t>(kStagesP) * 64 * D;
+    const size_t smem = static_cast<size_t>(kStagesP) * (F8 ? 32 : 64) * D;
     if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(prefill_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return PA_ERR_CUDA;
-    const cudaError_t e = pa_detail::launch_pdl(prefill_kernel<D>, grid, dim3(kThreadsP), smem, st, prm);
+    const cudaError_t e = pa_detail::launch_pdl(prefill_kernel<D, F8>, grid, dim3(kThreadsP), smem, st, prm);
     pa_detail::count_launch();
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -284,7 +361,7 @@ extern "C" int pa_prefill(pa_pool* pool, const void* q, int num_tokens, int num_
     if (!pool || num_tokens < 0 || num_seqs < 0 || max_q_len < 0 || num_q_heads <= 0 ||
         max_blocks_per_seq < 0)
         return PA_ERR_INVALID_ARG;
-    if (pool->dtype != PA_BF16) return PA_ERR_DTYPE;
+    if (pool->dtype != PA_BF16 && pool->dtype != PA_FP8E4M3) return PA_ERR_DTYPE;
     if (out_dtype != PA_F32 && out_dtype != PA_BF16) return PA_ERR_DTYPE;
     const int D = pool->head_dim, B = pool->block_size, Hkv = pool->kv_heads;
     if (num_q_heads % Hkv != 0 || B % 16 != 0 || (D != 64 && D != 128 && D != 256) ||
@@ -310,14 +387,17 @@ extern "C" int pa_prefill(pa_pool* pool, const void* q, int num_tokens, int num_
 
     PrefillParams p{};
     p.q = static_cast<const uint16_t*>(q);
-    p.k = static_cast<const uint16_t*>(pool->k);
-    p.v = static_cast<const uint16_t*>(pool->v);
+    p.k = pool->k;
+    p.v = pool->v;
     p.cu_q = cu_seqlens_q;
     p.tables = block_tables;
     p.lens = context_lens;
     p.out = out;
     p.err = pool->err;
-    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    const bool f8 = pool->dtype == PA_FP8E4M3;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 *
+                                      (f8 ? static_cast<double>(pool->k_scale) : 1.0));
+    p.v_scale = f8 ? pool->v_scale : 1.f;
     p.T = num_tokens;
     p.S = num_seqs;
     p.Hq = num_q_heads;
@@ -341,7 +421,12 @@ extern "C" int pa_prefill(pa_pool* pool, const void* q, int num_tokens, int num_
     }
     const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(Hkv),
                     static_cast<unsigned>(num_seqs));
-    if (D == 64) return launch_prefill_d<64>(p, grid, st);
-    if (D == 128) return launch_prefill_d<128>(p, grid, st);
-    return launch_prefill_d<256>(p, grid, st);
+    if (f8) {
+        if (D == 64) return launch_prefill_d<64, true>(p, grid, st);
+        if (D == 128) return launch_prefill_d<128, true>(p, grid, st);
+        return launch_prefill_d<256, true>(p, grid, st);
+    }
+    if (D == 64) return launch_prefill_d<64, false>(p, grid, st);
+    if (D == 128) return launch_prefill_d<128, false>(p, grid, st);
+    return launch_prefill_d<256, false>(p, grid, st);
 }

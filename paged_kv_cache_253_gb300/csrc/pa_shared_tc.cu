@@ -604,6 +604,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
     uint64_t* bar_pv = bar_s + 1;
     uint64_t* bar_full = bar_s + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kMiscOff + 32);
+    volatile int* s_skip = reinterpret_cast<volatile int*>(base + kMiscOff + 48);   // [2] per stage
     if (tid == 0) {
         pa_tc::mbar_init(bar_s, 1);
         pa_tc::mbar_init(bar_pv, 1);
@@ -643,12 +644,13 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
     pa_tc::cp_commit();
 
     // One thread stages step j: its (up to) four 16-token blocks, K as two
-    // 64-d boxes and V^T as one box each, on the stage's mbarrier.
+    // 64-d boxes and V^T as one box each, on the stage's mbarrier; the block
+    // slots it leaves unloaded go to s_skip[stage] (read after the wait).
     auto load_step = [&](int j) {
         if (tid != 0) return;
         const int st = j & 1;
         const uint32_t kst = sbase + kStageOff + st * kStageBytes;
-        int phys[kStep / 16];
+        int phys[kStep / 16], skip = 0;
         uint32_t bytes = 0;
 #pragma unroll
         for (int b = 0; b < kStep / 16; ++b) {
@@ -660,7 +662,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
                 else phys[b] = x;
             }
             if (phys[b] >= 0) bytes += 2 * 2048 + 4096;
+            else skip |= 1 << b;
         }
+        s_skip[st] = skip;
         pa_tc::mbar_expect_tx(bar_full + st, bytes);
 #pragma unroll
         for (int b = 0; b < kStep / 16; ++b) {
@@ -694,23 +698,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
         // zero-weight value still enters P.V and 0 * Inf or 0 * NaN is NaN:
         // zero those V^T columns (thread t clears row t of each tile).
         const int kbase = j * kStep;
-        int skip = 0;                                      // bit b: block slot b not loaded
+        const int skip = s_skip[st];                       // bit b: block slot b not loaded
 #pragma unroll
         for (int b = 0; b < kStep / 16; ++b) {
             const int tok = kbase + 16 * b;
-            int zero_from = 16;
-            if (tok >= kv_end) {
-                skip |= 1 << b;
-                zero_from = 0;
-            } else {
-                const int x = __ldg(table + (tok >> 4));
-                if (x < 0 || x >= p.num_blocks) {
-                    skip |= 1 << b;
-                    zero_from = 0;
-                } else if (tok + 16 > L) {
-                    zero_from = L - tok;
-                }
-            }
+            const int zero_from = (skip >> b) & 1 ? 0 : tok + 16 > L ? L - tok : 16;
             if (zero_from < 16)
                 pa_tc::zero_vt_row_tail(base + kStageOff + st * kStageBytes + 16384 + b * 4096, tid,
                                         zero_from);

@@ -152,9 +152,10 @@ class DecodeStep:
         return self.out
 
     def launches(self):
-        """Kernels per step: [copy] + [append] + decode split + merge (an fp8
-        pool's append is always its own launch)."""
-        fused = self.fused and not self.sharing() and not self.pool.fp8
+        """Kernels per step: [copy] + [append] + decode split + merge (the append
+        runs inside the split kernel when fused, as it is on the tensor-core
+        shapes, bf16 and fp8 pools alike)."""
+        fused = self.fused and not self.sharing()
         return (1 if self.num_pairs else 0) + (0 if fused else 1) + 2
 
 

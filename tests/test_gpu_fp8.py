@@ -15,7 +15,7 @@ import torch
 from oracle import attention as oatt
 from oracle import fp8
 from oracle import replay as orp
-from paged_kv_cache_253_gb300 import workloads as wls
+from paged_kv_cache_253_gb300 import runtime, workloads as wls
 from paged_kv_cache_253_gb300._lib import PagedAttnError
 from paged_kv_cache_253_gb300.api import KVPool
 
@@ -142,16 +142,85 @@ def test_small_parity(name, kw):
     print(f"{wl.name} {kw}: max-abs {err:.3g}")
 
 
-def test_append_decode_equals_separate_calls():
-    """An fp8 pool's append_decode is the quantizing append then the decode."""
-    wl = wls.make_workload("decode", num_seqs=6, min_len=1, max_len=300, **D128)
+@pytest.mark.parametrize("kw", [dict(num_seqs=6, min_len=1, max_len=300, **D128),
+                                dict(lengths=[1, 16, 17, 33], num_q_heads=16, num_kv_heads=4,
+                                     head_dim=64, dtype="fp8"),
+                                dict(num_seqs=3, min_len=1, max_len=200, num_q_heads=8,
+                                     num_kv_heads=2, head_dim=256, dtype="fp8"),
+                                dict(num_seqs=4, min_len=1, max_len=200, block_size=32, **D128)])
+def test_append_decode_equals_separate_calls(kw):
+    """An fp8 pool's append_decode (the quantizing append fused into the decode
+    kernel on the tensor-core shapes) equals the quantizing append then the
+    decode: the same codes in the pool, bit for bit, and the same outputs."""
+    wl = wls.make_workload("decode", **kw)
     values = wls.generate_values(wl, "cuda")
-    outs = []
+    outs, pools = [], []
     for fused in (True, False):
         pool, _, _, step = run_library(wl, values, fused=fused)
         assert pool.get_error() == 0
         outs.append(step.out.cpu())
+        k, v = pool.export()
+        torch.cuda.synchronize()
+        pools.append((k.cpu(), v.cpu()))
+    assert torch.equal(pools[0][0], pools[1][0]) and torch.equal(pools[0][1], pools[1][1])
     assert torch.equal(outs[0], outs[1])
+
+
+PREFILL = [
+    dict(lengths=[0, 3, 40, 16], chunks=[1, 15, 16, 17], **D128),
+    dict(lengths=[5, 0, 100], chunks=[33, 64, 47], **D128),
+    dict(lengths=[0, 21], chunks=[130, 9], num_q_heads=64, num_kv_heads=8, head_dim=128,
+         dtype="fp8"),                                                      # G = 8
+    dict(lengths=[19, 2], chunks=[40, 23], num_q_heads=10, num_kv_heads=2, head_dim=128,
+         dtype="fp8"),                                                      # G = 5
+    dict(lengths=[33, 0], chunks=[50, 17], num_q_heads=16, num_kv_heads=4, head_dim=64,
+         dtype="fp8"),
+    dict(lengths=[12, 30], chunks=[29, 8], num_q_heads=8, num_kv_heads=2, head_dim=256,
+         dtype="fp8"),
+    dict(lengths=[45, 0, 3], chunks=[20, 33, 1], block_size=32, **D128),
+]
+
+
+def _check_prefill(wl, values, seqs=None, threads=1):
+    pool, bm, setup_pairs = runtime.replay_setup(wl, values, "cuda")
+    step = runtime.prepare_prefill(wl, values, pool, bm)
+    step.run()
+    torch.cuda.synchronize()
+    assert pool.get_error() == 0
+    st = orp.replay(wl, values)
+    assert setup_pairs == st.setup_pairs
+    assert step.slots.cpu().numpy().tolist() == st.step_slots.tolist()
+    assert np.array_equal(step.block_tables.cpu().numpy(), st.block_tables)
+    assert_pools_equal(pool, st)
+    ref = orp.prefill_attention(wl, values, st, seqs=seqs, threads=threads)
+    got = step.out.double().cpu().numpy()
+    if seqs is not None:
+        cu = st.cu_seqlens_q
+        got = got[np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs])]
+    err = np.abs(got - ref).max() if ref.size else 0.0
+    assert err <= FP8_TOL, f"max-abs {err:.3g} > {FP8_TOL}"
+    return err
+
+
+@pytest.mark.parametrize("kw", PREFILL, ids=[f"case{i}" for i in range(len(PREFILL))])
+def test_prefill_parity(kw):
+    """Chunked prefill over an fp8 pool: the chunk's codes (quantizing append)
+    bit-exact, every query row within FP8_TOL of float64 attention over the
+    codes' values."""
+    wl = wls.make_workload("prefill", **kw)
+    values = wls.generate_values(wl, "cuda")
+    err = _check_prefill(wl, values)
+    print(f"prefill fp8 {kw}: max-abs {err:.3g}")
+
+
+def test_prefill_full_size_parity():
+    """The prefill workload (16 sequences, cached prefixes up to 4096, chunks of
+    128..512) on an fp8 pool: codes bit-exact, attention on sampled sequences."""
+    wl = wls.make_workload("prefill", dtype="fp8")
+    values = wls.generate_values(wl, "cuda")
+    seqs = [0, 7, wl.num_seqs - 1]
+    err = _check_prefill(wl, values, seqs=seqs, threads=16)
+    print(f"prefill fp8 full size: max-abs over sequences {seqs}: {err:.3g}")
 
 
 def test_full_size_parity():
@@ -163,3 +232,23 @@ def test_full_size_parity():
     seqs = sorted(set(rng.choice(wl.num_seqs, size=12, replace=False).tolist()) | {0, wl.num_seqs - 1})
     err = _check(wl, values, seqs=seqs, threads=8)
     print(f"decode fp8 full size: max-abs over {len(seqs)} sequences {err:.3g} (tol {FP8_TOL})")
+
+
+def test_prefix_full_size_shared_parity():
+    """The prefix workload (256 forks of a 4104-token prompt) on an fp8 pool
+    through pa_decode_shared: the shared span read once per tile of members on
+    the mma.sync form (codes widened to f16), codes bit-exact, attention on
+    sampled sequences."""
+    wl = wls.make_workload("prefix", dtype="fp8")
+    values = wls.generate_values(wl, "cuda")
+    pool, bm, setup_pairs, step = run_library(wl, values, shared=True)
+    assert step.sharing()
+    assert pool.get_error() == 0
+    st = orp.replay(wl, values)
+    assert setup_pairs == st.setup_pairs
+    assert_pools_equal(pool, st)
+    seqs = [0, 1, 100, wl.num_seqs - 1]
+    ref = orp.attention(wl, values, st, seqs=seqs, threads=8)
+    got = step.out.double().cpu().numpy()[np.asarray(seqs)]
+    err = np.abs(got - ref).max()
+    assert err <= FP8_TOL, f"max-abs {err:.3g} > {FP8_TOL}"

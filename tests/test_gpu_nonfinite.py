@@ -91,6 +91,8 @@ DECODE = [
     ("decode", dict(lengths=[3, 31, 70], dtype="f32", **D128)),
     ("decode", dict(lengths=[5, 19, 41], block_size=32, **D128)),
     ("long", dict(num_seqs=2, min_len=3001, max_len=5003, **D128)),
+    ("mixed", dict(num_seqs=24, median=60, min_len=1, max_len=400, prefix_min=20, prefix_max=90,
+                   num_q_heads=64, num_kv_heads=8, head_dim=128, dtype="fp8")),
 ]
 
 
@@ -100,12 +102,13 @@ def test_decode_ignores_stale_nonfinite(name, kw):
 
 
 @pytest.mark.parametrize("prefix_len", [41, 16 * 21 + 3, 16 * 64 + 5])
-@pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync"])
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync", "fp8"])
 def test_shared_prefix_ignores_stale_nonfinite(prefix_len, kernel):
     """pa_decode_shared: shared spans of 2, 21 and 64 full blocks (steps of 64
-    tokens that leave 2, 3 and 0 block slots unloaded at the span's end)."""
+    tokens that leave 2, 3 and 0 block slots unloaded at the span's end), on
+    both bf16 forms and on an fp8 pool (its NaN codes planted)."""
     wl = wls.make_workload("prefix", num_seqs=6, prefix_len=prefix_len, suffix_min=1,
-                           suffix_max=40, **D128)
+                           suffix_max=40, **D128, **({"dtype": "fp8"} if kernel == "fp8" else {}))
     values = wls.generate_values(wl, "cuda")
     pool, bm, _ = runtime.replay_setup(wl, values, "cuda")
     pool.set_option("shared_kernel", 1 if kernel == "mma_sync" else 0)
@@ -133,6 +136,8 @@ PREFILL = [
     dict(lengths=[0, 250], chunks=[129, 3], **D128),
     dict(lengths=[17, 40], chunks=[1, 31], num_q_heads=64, num_kv_heads=8, head_dim=128),
     dict(lengths=[9, 0], chunks=[23, 40], num_q_heads=16, num_kv_heads=4, head_dim=64),
+    dict(lengths=[7, 30], chunks=[25, 3], num_q_heads=32, num_kv_heads=8, head_dim=128,
+         dtype="fp8"),
 ]
 
 

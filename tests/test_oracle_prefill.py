@@ -204,3 +204,48 @@ def test_prefill_after_a_fork_copies_the_shared_partial_block():
             attn_mask=torch.from_numpy(mask), scale=0.35)
         np.testing.assert_allclose(out[cu[s]:cu[s + 1]], ref.permute(1, 0, 2).numpy(),
                                    rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_prefill_replay_equals_contiguous_causal_over_quantized_rows():
+    """An fp8 pool stores every appended row (history and chunk) as codes under
+    its own K or V scale; the prefill oracle reads the values the codes stand
+    for: each chunk query equals causal attention over its request's rows,
+    each quantized on its own (K and V scales differ, so a swap shows)."""
+    torch = pytest.importorskip("torch")
+    from oracle import fp8
+    from oracle import replay as orp
+    from paged_kv_cache_253_gb300 import workloads as wls
+    wl = wls.make_workload("prefill", num_seqs=3, lengths=[0, 5, 17], chunks=[6, 1, 9],
+                           num_q_heads=4, num_kv_heads=2, head_dim=16, block_size=4, dtype="fp8")
+    assert wl.kv_scales[0] != wl.kv_scales[1]
+    values = wls.generate_values(wl, "cpu")
+    st = orp.replay(wl, values)
+    assert st.k_pool.dtype == np.uint8
+    out = orp.prefill_attention(wl, values, st)
+
+    def rows(name, which):
+        x = oatt.bf16_bits_to_f32(orp.values_to_numpy(values[name]))
+        return fp8.dequantize(fp8.quantize(x, wl.kv_scales[which]), wl.kv_scales[which])
+    hk, hv, nk, nv = rows("hist_k", 0), rows("hist_v", 1), rows("new_k", 0), rows("new_v", 1)
+    q = oatt.bf16_bits_to_f32(orp.values_to_numpy(values["q"]))
+    hist = [0, 0, 5]
+    for s, (P, n) in enumerate(zip([0, 5, 17], [6, 1, 9])):
+        c0, c1 = st.cu_seqlens_q[s], st.cu_seqlens_q[s + 1]
+        ks = np.concatenate([hk[hist[s]:hist[s] + P], nk[c0:c1]])
+        vs = np.concatenate([hv[hist[s]:hist[s] + P], nv[c0:c1]])
+        L = P + n
+        mask = np.tril(np.ones((L, L), dtype=bool))[P:]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[c0:c1].astype(np.float64)).permute(1, 0, 2),
+            torch.from_numpy(ks.astype(np.float64)).permute(1, 0, 2).repeat_interleave(2, 0),
+            torch.from_numpy(vs.astype(np.float64)).permute(1, 0, 2).repeat_interleave(2, 0),
+            attn_mask=torch.from_numpy(mask), scale=wl.scale)
+        np.testing.assert_allclose(out[c0:c1], ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-12)
+    # the bf16 workload's prefill differs from it by quantization error only
+    # (e4m3 keeps 3 mantissa bits: a few-key row can move by several percent
+    # of a value)
+    wl16 = wls.make_workload("prefill", num_seqs=3, lengths=[0, 5, 17], chunks=[6, 1, 9],
+                             num_q_heads=4, num_kv_heads=2, head_dim=16, block_size=4)
+    ref16 = orp.prefill_attention(wl16, values, orp.replay(wl16, values))
+    err = np.abs(out - ref16).max()
+    assert 1e-4 < err < 0.5, err
