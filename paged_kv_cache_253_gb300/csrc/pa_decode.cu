@@ -343,17 +343,24 @@ __device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D /
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
-    const float mn0 = fmaxf(a.m0, mx0), mn1 = fmaxf(a.m1, mx1);
+    // Each head keeps a reference, not the running maximum: it is raised only
+    // when a score passes it by more than 2^8 (log2 units), so the weights
+    // 2^(x - ref) stay below 2^8 and the sums are rescaled only then (a lane
+    // rescales 2 NT + 2 values).  A partial carries its reference in place of
+    // its maximum; the log-sum-exp merges are exact for any reference.  With
+    // the running maximum itself the sums were rescaled on most tiles, since
+    // a warp sees only a few tiles of each item.
+    const bool up0 = mx0 > a.m0 + 8.f, up1 = mx1 > a.m1 + 8.f;   // also: reference still unset
+    const float mn0 = up0 ? mx0 : a.m0, mn1 = up1 ? mx1 : a.m1;
     const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
     const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
     const float p0 = pa_dev::ex2(x0 - ms0), p1 = pa_dev::ex2(x1 - ms1);
     const float p2 = pa_dev::ex2(x2 - ms0), p3 = pa_dev::ex2(x3 - ms1);
-    // Rescale the running sums only when some head's maximum moved: otherwise
-    // the factor is exactly 1 (an unchanged -inf maximum leaves sums that are
-    // still 0), so skipping it changes no bit; past the first tiles of an item
-    // the maximum rarely moves.
-    if (__any_sync(0xffffffffu, mn0 != a.m0 || mn1 != a.m1)) {
-        const float cr0 = pa_dev::ex2(a.m0 - ms0), cr1 = pa_dev::ex2(a.m1 - ms1);
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+        // factor 1 for a head that kept its reference; 0 for one that had none
+        // (its sums are still 0)
+        const float cr0 = up0 ? pa_dev::ex2(a.m0 - ms0) : 1.f;
+        const float cr1 = up1 ? pa_dev::ex2(a.m1 - ms1) : 1.f;
         a.l0 *= cr0;
         a.l1 *= cr1;
 #pragma unroll
