@@ -128,6 +128,7 @@ TRAFFIC_PROFILES = {
     ("long", "bf16"): "decode_kernel_long_context.md",
     ("mixed", "bf16"): "decode_kernel_mixed.md",
     ("prefix", "bf16"): "decode_call_prefix.md",
+    ("prefill", "bf16"): "prefill_tc_prefill_batch.md",
 }
 
 
@@ -260,6 +261,27 @@ def _oracle_sample(wl, values, target_s=12.0, threads=None, st=None):
     desc = (f"{done_seq} sequence {kind} ({done_tok} cached tokens) drawn from the same "
             f"{wl.num_seqs}-sequence batch, float64 oracle, {threads} threads, {spent:.1f} s")
     return gbs, done_q / spent, threads, desc
+
+
+def _parity_sample(wl, values, st, out, n=3):
+    """Max-abs difference between the bench's last output and the float64
+    oracle on a few sequences of the batch (the same seeded pick as the CPU
+    baseline's sample), against the parity tests' tolerance."""
+    import numpy as np
+    from oracle import replay as orp
+    from oracle.attention import default_threads
+    pick = np.sort(np.random.default_rng(wl.seed).permutation(wl.num_seqs)[:n])
+    got = out.double().cpu().numpy()
+    if wl.chunk_lens is not None:
+        cu = np.concatenate([[0], np.cumsum(wl.chunk_lens)])
+        got = got[np.concatenate([np.arange(cu[s], cu[s + 1]) for s in pick])]
+        ref = orp.prefill_attention(wl, values, st, seqs=pick, threads=default_threads())
+    else:
+        got = got[pick]
+        ref = orp.attention(wl, values, st, seqs=pick, threads=default_threads())
+    tol = {"f32": 1e-5, "bf16": 5e-3, "fp8": 5e-5}[wl.dtype]
+    err = float(np.abs(got - ref).max()) if ref.size else 0.0
+    return {"seqs": [int(s) for s in pick], "max_abs_err": err, "tol": tol, "ok": err <= tol}
 
 
 def _dtype_kw(args):
@@ -454,7 +476,7 @@ def run_ours(args):
         tflops = flops / (dms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak,
                     "peak_kind": tpeak_kind + " bf16 dense burst", "unit": "TFLOP/s",
-                    "frac": round(tflops / tpeak, 4), "traffic": None,
+                    "frac": round(tflops / tpeak, 4), "traffic": _traffic_from_profile(wl),
                     "kernel": "prefill (pa_prefill)", "algorithmic_flops_per_launch": flops}
     else:
         roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
@@ -497,6 +519,7 @@ def run_ours(args):
         gbs, tps, threads, desc = _oracle_sample(wl, cvals, target_s=args.cpu_seconds, st=st)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
                                 "kind": "oracle", "sample": desc}
+        line["parity_sample"] = _parity_sample(wl, cvals, st, step.out)
         if wl.name in ("tiny", "decode"):
             # the same oracle on one host thread
             gbs1, _, _, desc1 = _oracle_sample(wl, cvals, target_s=args.cpu_seconds / 2,
