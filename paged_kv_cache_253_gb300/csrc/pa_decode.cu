@@ -1152,14 +1152,23 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
     }
     if (occ <= 0) return PA_ERR_UNSUPPORTED;
     plan->grid = pool->num_sms * occ;
+    plan->tcd = false;
     if (fast) {
         plan->items_target = plan->grid * kItemsPerCta;
+        // the tcgen05 split pass where the pool's PA_OPT_DECODE_KERNEL option asks
+        // for it and the shape allows it (automatic: the mma.sync kernels, which
+        // measure faster on every workload so far)
+        if (!plan->shared && !plan->no_tcd && pool->opt_decode_kernel == 2 && decode_tc_eligible(pool, G)) {
+            const int stages = decode_tc_stages(pool, S);
+            if (stages > 0) plan_decode_tc(pool, S, stages, plan);
+        }
         // items <= Hkv * (total / PT + S); PT >= total * Hkv / items_target keeps
         // that below min_items.  The extra items_target of room lets the
         // partition cap and the guided tail take effect; the kernel never
         // exceeds max_items.
         plan->min_items = static_cast<size_t>(plan->items_target) + static_cast<size_t>(Hkv) * S;
-        plan->max_items = plan->min_items + static_cast<size_t>(plan->items_target);
+        plan->max_items = plan->min_items + (plan->tcd ? decode_tc_extra_items(*plan)
+                                                       : static_cast<size_t>(plan->items_target));
     } else {
         plan->items_target = 0;
         const size_t per_seq = (static_cast<size_t>(max_blocks) * B + plan->pt_fixed - 1) / plan->pt_fixed;
@@ -1179,8 +1188,11 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
     p.max_items = static_cast<int>(std::min<size_t>(plan.max_items, 1u << 30));
     p.pt_fixed = plan.pt_fixed;
     const dim3 grid(plan.grid), block(plan.threads);
-    cudaError_t e;
-    if (plan.fast && plan.shared && plan.tc) {
+    cudaError_t e = cudaSuccess;
+    if (plan.tcd) {
+        const int rc = launch_decode_tc(plan.pool, plan, p, st);
+        if (rc != PA_OK) return rc;
+    } else if (plan.fast && plan.shared && plan.tc) {
         // shared items on tcgen05 first, then the private spans on the plain split kernel
         const int rc = launch_shared_tc(plan.pool, p, st);
         if (rc != PA_OK) return rc;
@@ -1221,7 +1233,7 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
     } else {
         e = launch_pdl(decode_simple_kernel<float, float>, grid, block, plan.smem, st, p);
     }
-    count_launch();
+    if (!plan.tcd) count_launch();
     if (e != cudaSuccess) return PA_ERR_CUDA;
     e = launch_pdl(decode_merge_kernel, dim3(static_cast<unsigned>(p.S) * static_cast<unsigned>(p.Hkv)),
                    dim3(kThreads), 0, st, p);

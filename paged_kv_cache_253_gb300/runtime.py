@@ -151,13 +151,6 @@ class DecodeStep:
         self.decode()
         return self.out
 
-    def launches(self):
-        """Kernels per step: [copy] + [append] + decode split + merge (the append
-        runs inside the split kernel when fused, as it is on the tensor-core
-        shapes, bf16 and fp8 pools alike)."""
-        fused = self.fused and not self.sharing()
-        return (1 if self.num_pairs else 0) + (0 if fused else 1) + 2
-
 
 SHARED_MIN_FRACTION = 0.5
 
@@ -236,10 +229,6 @@ class PrefillStep:
         self.pool.append_kv(self.new_k, self.new_v, self.slots)
         self.attend()
         return self.out
-
-    def launches(self):
-        """Kernels per step: [copy] + append + prefill."""
-        return (1 if self.num_pairs else 0) + 2
 
 
 def prepare_prefill(wl, values, pool, bm, out_dtype=torch.float32):
