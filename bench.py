@@ -339,8 +339,6 @@ def run_ours(args):
     wl = wls.make_workload(args.workload, **_dtype_kw(args))
     values = wls.generate_values(wl, f"cuda:{local}", seed=wl.seed + 1000 * rank)
     pool, bm, _ = runtime.replay_setup(wl, values, f"cuda:{local}")
-    if args.decode_kernel is not None:
-        pool.set_option("decode_kernel", {"mma_sync": 1, "tcgen05": 2}[args.decode_kernel])
     prefill = wl.chunk_lens is not None
     step = runtime.prepare_prefill(wl, values, pool, bm) if prefill else \
         runtime.prepare_step(wl, values, pool, bm)
@@ -548,9 +546,6 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="shrink the workload to this many sequences (reduced cases for "
                          "profiler captures; the bench lines use the full workloads)")
-    ap.add_argument("--decode-kernel", default=None, choices=["tcgen05", "mma_sync"],
-                    help="split kernel of the decode call (default: the library's automatic "
-                         "choice)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=40.0,
                     help="--impl reference: total oracle seconds over warm-up and timed steps")

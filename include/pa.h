@@ -133,19 +133,12 @@ int pa_pool_kv_scales(const pa_pool *pool, float *k_scale, float *v_scale);
  *                          allows it, 1 = the mma.sync form.
  *   PA_OPT_PREFILL_KERNEL  pa_prefill: 0 (default) = the tcgen05 kernel where
  *                          the shape allows it, 1 = the mma.sync form.
- *   PA_OPT_DECODE_KERNEL   split pass of pa_decode and pa_append_decode: 0
- *                          (default) = automatic (the kernels measured
- *                          fastest: the mma.sync ones), 1 = the mma.sync
- *                          kernels, 2 = the tcgen05 kernel where the shape
- *                          allows it (bf16 or fp8 pools, head_dim 128,
- *                          16-token blocks, G <= 8), else the mma.sync ones.
  * An unknown option or a value out of range returns PA_ERR_INVALID_ARG and
  * changes nothing. */
 typedef enum {
     PA_OPT_PARTITION_CAP = 0,
     PA_OPT_SHARED_KERNEL = 1,
-    PA_OPT_PREFILL_KERNEL = 2,
-    PA_OPT_DECODE_KERNEL = 3
+    PA_OPT_PREFILL_KERNEL = 2
 } pa_option;
 int pa_pool_set_option(pa_pool *pool, pa_option option, int value);
 int pa_pool_get_option(const pa_pool *pool, pa_option option, int *value);

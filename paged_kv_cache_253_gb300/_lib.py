@@ -25,7 +25,7 @@ c_u8p = ctypes.POINTER(ctypes.c_uint8)
 c_intp = ctypes.POINTER(c_int)
 
 PA_F32, PA_BF16, PA_FP8E4M3 = 0, 1, 2
-PA_OPT_PARTITION_CAP, PA_OPT_SHARED_KERNEL, PA_OPT_PREFILL_KERNEL, PA_OPT_DECODE_KERNEL = 0, 1, 2, 3
+PA_OPT_PARTITION_CAP, PA_OPT_SHARED_KERNEL, PA_OPT_PREFILL_KERNEL = 0, 1, 2
 
 ERRORS = {
     0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_DTYPE", -3: "PA_ERR_CUDA",

@@ -76,13 +76,12 @@ class KVPool:
         return k.value, v.value
 
     OPTIONS = {"partition_cap": L.PA_OPT_PARTITION_CAP, "shared_kernel": L.PA_OPT_SHARED_KERNEL,
-               "prefill_kernel": L.PA_OPT_PREFILL_KERNEL, "decode_kernel": L.PA_OPT_DECODE_KERNEL}
+               "prefill_kernel": L.PA_OPT_PREFILL_KERNEL}
 
     def set_option(self, name, value):
         """Kernel-choice option of this pool (pa_pool_set_option): partition_cap
         (tokens; 0 none, -1 automatic), shared_kernel / prefill_kernel (0
-        tcgen05 where eligible, 1 mma.sync), decode_kernel (0 automatic, 1
-        mma.sync, 2 tcgen05 where eligible)."""
+        tcgen05 where eligible, 1 mma.sync)."""
         L.check(L.pa_pool_set_option(self.handle, self.OPTIONS[name], int(value)),
                 "pa_pool_set_option")
 

@@ -210,10 +210,6 @@ int pa_pool_set_option(pa_pool* pool, pa_option option, int value) {
             if (value != 0 && value != 1) return PA_ERR_INVALID_ARG;
             pool->opt_prefill_kernel = value;
             return PA_OK;
-        case PA_OPT_DECODE_KERNEL:
-            if (value < 0 || value > 2) return PA_ERR_INVALID_ARG;
-            pool->opt_decode_kernel = value;
-            return PA_OK;
         default:
             return PA_ERR_INVALID_ARG;
     }
@@ -225,7 +221,6 @@ int pa_pool_get_option(const pa_pool* pool, pa_option option, int* value) {
         case PA_OPT_PARTITION_CAP: *value = pool->opt_partition_cap; return PA_OK;
         case PA_OPT_SHARED_KERNEL: *value = pool->opt_shared_kernel; return PA_OK;
         case PA_OPT_PREFILL_KERNEL: *value = pool->opt_prefill_kernel; return PA_OK;
-        case PA_OPT_DECODE_KERNEL: *value = pool->opt_decode_kernel; return PA_OK;
         default: return PA_ERR_INVALID_ARG;
     }
 }
@@ -279,18 +274,12 @@ int pa_decode_reserve(pa_pool* pool, int max_seqs, int max_q_heads) {
         return PA_ERR_INVALID_ARG;
     DeviceGuard g(pool->device);
     if (!g.ok) return PA_ERR_CUDA;
-    // the fp32 path's partial count grows with the table width; reserve for the
-    // fast path, whichever split kernel (tcgen05 or mma.sync) a call picks
-    size_t bytes = 0;
-    for (int k = 0; k < 2; ++k) {
-        pa_detail::DecodePlan plan;
-        plan.no_tcd = k == 1;
-        const int rc = pa_detail::plan_decode(pool, max_seqs, max_q_heads, 1, &plan);
-        if (rc != PA_OK) return rc;
-        bytes = std::max(bytes, workspace_bytes(plan, max_seqs, max_q_heads / pool->kv_heads,
-                                                pool->head_dim, nullptr));
-    }
-    return ensure_workspace(pool, bytes);
+    pa_detail::DecodePlan plan;
+    // the fp32 path's partial count grows with the table width; reserve for the fast path
+    int rc = pa_detail::plan_decode(pool, max_seqs, max_q_heads, 1, &plan);
+    if (rc != PA_OK) return rc;
+    return ensure_workspace(pool, workspace_bytes(plan, max_seqs, max_q_heads / pool->kv_heads,
+                                                  pool->head_dim, nullptr));
 }
 
 // Host plan of the shared-prefix items (see pa_decode_shared).

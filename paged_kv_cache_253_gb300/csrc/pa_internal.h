@@ -29,16 +29,10 @@ struct pa_pool {
     CUtensorMap kmap;
     CUtensorMap vmap;
     bool tmaps_ready = false;
-    // fp8 pools: K codes (boxes 128 d x 16 tokens, 128-byte swizzle) and V^T
-    // codes (boxes 16 tokens x 128 d), made on first use
-    CUtensorMap kmap8;
-    CUtensorMap vmap8;
-    bool tmaps8_ready = false;
     // kernel-choice options (pa_pool_set_option)
     int opt_partition_cap = -1;     // decode partition cap, tokens; -1 automatic, 0 none
     int opt_shared_kernel = 0;      // 0 tcgen05 where eligible, 1 mma.sync
     int opt_prefill_kernel = 0;     // 0 tcgen05 where eligible, 1 mma.sync
-    int opt_decode_kernel = 0;      // 0 automatic, 1 mma.sync, 2 tcgen05 where eligible
     // shared-prefix descriptor last uploaded by pa_decode_shared (host copy + device copy)
     std::vector<int> desc_host;
     int* desc_dev = nullptr;
@@ -92,7 +86,6 @@ struct DecodeParams {
     // waited for the work before it; the split kernel then runs alongside it and
     // waits for it only before exiting (so the merge after it sees both).
     int defer_wait;
-    int tc_stages;              // tcgen05 decode kernel: shared-memory stages of its TMA ring
 };
 
 // Everything one prefill launch needs (pa_prefill), passed by value.
@@ -164,9 +157,6 @@ struct DecodePlan {
     bool shared = false;        // shared-prefix items present (fast path only)
     bool fuse = false;          // the decode kernel also appends each sequence's new token
     bool tc = false;            // shared items run in the tcgen05 kernel before the split pass
-    bool tcd = false;           // the split pass runs on the tcgen05 decode kernel
-    bool no_tcd = false;        // caller: plan for the mma.sync split kernels only
-    int tc_stages = 0;
     pa_pool* pool = nullptr;
     bool fast;                  // tensor-core path (bf16 pool, or fp8 codes widened to f16)
     bool bf16;                  // pool element type is bf16
@@ -182,14 +172,6 @@ int plan_decode(pa_pool* p, int S, int Hq, int max_blocks, DecodePlan* plan);
 int check_decode_args(const pa_pool* pool, const void* q, int S, int Hq, const int32_t* tables,
                       int max_blocks, const int32_t* lens, const void* out, pa_dtype out_dtype);
 int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t st);
-
-// tcgen05 decode kernel (pa_decode_tc.cu): tokens as the MMA's M dimension;
-// bf16 and fp8 pools of 16-token blocks, head_dim 128, G <= 8.
-bool decode_tc_eligible(const pa_pool* pool, int G);
-int decode_tc_stages(const pa_pool* pool, int S);     // 0: the schedule of S sequences leaves no room
-void plan_decode_tc(const pa_pool* pool, int S, int stages, DecodePlan* plan);
-size_t decode_tc_extra_items(const DecodePlan& plan);   // partial slots beyond min_items
-int launch_decode_tc(pa_pool* pool, const DecodePlan& plan, const DecodeParams& p, cudaStream_t st);
 
 // TMA descriptors of the pool's K and V^T (16-token blocks), made once per pool.
 int ensure_tensor_maps(pa_pool* pool);

@@ -70,11 +70,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Instruction descriptor of kind::f16: f16 A and B (both K-major), fp32 D, M x N.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
-    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
-}
-
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, bool accumulate) {
@@ -125,31 +120,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
         if (done) return true;
     }
     return false;
-}
-
-// Bounded wait that also gives up when another role of the CTA has raised
-// *abort_flag (checked every 32 polls); a timeout raises the flag itself.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              uint32_t limit) {
-    const uint32_t a = smem_u32(bar);
-    for (uint32_t i = 0; i < limit; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((i & 31) == 31 && *abort_flag) return false;
-    }
-    *abort_flag = 1;
-    return false;
-}
-
-// One arrival on the mbarrier's current phase.
-__device__ __forceinline__ void arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Arrive on the mbarrier and raise the byte count its current phase waits for.
@@ -226,59 +196,6 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[1
         "r"(v[15])
         : "memory");
 }
-// N consecutive columns (N = 4, 8 or 16) of this warp's 32 lanes.
-template <int N>
-__device__ __forceinline__ void tmem_ldn(uint32_t taddr, float (&v)[N]) {
-    uint32_t r[N];
-    if constexpr (N == 4) {
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                     : "r"(taddr)
-                     : "memory");
-    } else if constexpr (N == 8) {
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                       "=r"(r[6]), "=r"(r[7])
-                     : "r"(taddr)
-                     : "memory");
-    } else {
-        static_assert(N == 16, "4, 8 or 16 columns");
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-              "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-              "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-            : "r"(taddr)
-            : "memory");
-    }
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
-}
-template <int N>
-__device__ __forceinline__ void tmem_stn(uint32_t taddr, const float (&v)[N]) {
-    if constexpr (N == 4) {
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
-                     "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
-                     "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3]))
-                     : "memory");
-    } else if constexpr (N == 8) {
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
-                         taddr),
-                     "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
-                     "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
-                     "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-                     "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
-                     : "memory");
-    } else {
-        static_assert(N == 16, "4, 8 or 16 columns");
-        uint32_t u[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[i]);
-        tmem_st16u(taddr, u);
-    }
-}
-
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

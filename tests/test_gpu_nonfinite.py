@@ -174,15 +174,11 @@ def test_pool_options_round_trip_and_reject_bad_values():
     assert pool.get_option("partition_cap") == -1
     assert pool.get_option("shared_kernel") == 0
     assert pool.get_option("prefill_kernel") == 0
-    assert pool.get_option("decode_kernel") == 0
     pool.set_option("partition_cap", 512)
     pool.set_option("prefill_kernel", 1)
-    pool.set_option("decode_kernel", 2)
     assert pool.get_option("partition_cap") == 512
     assert pool.get_option("prefill_kernel") == 1
-    assert pool.get_option("decode_kernel") == 2
-    for name, bad in (("partition_cap", -2), ("shared_kernel", 2), ("prefill_kernel", -1),
-                      ("decode_kernel", 3)):
+    for name, bad in (("partition_cap", -2), ("shared_kernel", 2), ("prefill_kernel", -1)):
         with pytest.raises(PagedAttnError):
             pool.set_option(name, bad)
     assert pool.get_option("partition_cap") == 512
