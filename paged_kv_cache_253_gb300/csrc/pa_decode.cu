@@ -45,9 +45,10 @@
 // Tuning constants (the measured best on GB300).
 namespace {
 
-constexpr int kItemsPerCta = 4;         // target work items per resident CTA
+constexpr int kItemsPerSm = 12;         // target work items per SM (12 beat 9 and 15 on GB300)
 constexpr int kWarps = 4;               // warps per CTA sharing one item
-constexpr int kMinCtas = 3;             // resident CTAs per SM the register budget aims at
+constexpr int kMinCtas = 3;             // resident CTAs per SM the register budget aims at (bf16)
+constexpr int kMinCtasF8 = 4;           // the same for the fp8 walk (one tile in flight per warp)
 constexpr int kPtMax = 2048;            // partition cap in tokens for batches of many sequences
 constexpr int kBlockPrefetch = 1;       // L2 prefetch of the block a warp reads this many blocks ahead
 constexpr int kGuideMinPT = 256;        // shortest partition of the guided tail, tokens
@@ -302,40 +303,19 @@ struct WarpAcc {
     float m0, m1, l0, l1;                 // running max / sum (log2 units), heads 2c, 2c+1
 };
 
-// One 16-token tile: scores, online-softmax update, value product.  F8: the
-// fragments hold f16 pairs (widened e4m3 codes, f16 queries) instead of bf16.
-template <int D, bool F8 = false>
-__device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D / 32],
-                                            const uint4 (&k1)[D / 32], uint2 (&v0)[D / 16],
-                                            uint2 (&v1)[D / 16], int nvalid, float sl, int r0,
-                                            int r1, int c) {
-    constexpr int NJ = D / 32, NT = D / 16;
-    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};   // two chains
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        if constexpr (F8) {
-            pa_dev::mma_f16_16816(sc, k0[j].x, k1[j].x, k0[j].y, k1[j].y, a.qf[j].x, a.qf[j].y);
-            pa_dev::mma_f16_16816(sd, k0[j].z, k1[j].z, k0[j].w, k1[j].w, a.qf[j].z, a.qf[j].w);
-        } else {
-            pa_dev::mma_bf16_16816(sc, k0[j].x, k1[j].x, k0[j].y, k1[j].y, a.qf[j].x, a.qf[j].y);
-            pa_dev::mma_bf16_16816(sd, k0[j].z, k1[j].z, k0[j].w, k1[j].w, a.qf[j].z, a.qf[j].w);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sc[i] += sd[i];
+// Online-softmax update of one 16-token tile.  sc holds this thread's four
+// scores (token rows r0 / r1 x heads 2c / 2c+1); rows at or past nvalid are
+// masked.  Returns the tile's probabilities as the value product's B
+// fragments: the rounded pair (bh) and the remainder (be), bf16 or (F8) f16.
+template <int D, bool F8>
+__device__ __forceinline__ void softmax_tile(WarpAcc<D>& a, const float (&sc)[4], int nvalid, float sl,
+                                             int r0, int r1, uint32_t& bh0, uint32_t& bh1, uint32_t& be0,
+                                             uint32_t& be1) {
+    constexpr int NT = D / 16;
     float x0 = sc[0] * sl, x1 = sc[1] * sl, x2 = sc[2] * sl, x3 = sc[3] * sl;
     if (nvalid < 16) {                        // partly filled last tile
         if (r0 >= nvalid) x0 = x1 = -INFINITY;
         if (r1 >= nvalid) x2 = x3 = -INFINITY;
-        const uint32_t mlo = (4 * c < nvalid ? 0x0000ffffu : 0u) |
-                             (4 * c + 1 < nvalid ? 0xffff0000u : 0u);
-        const uint32_t mhi = (4 * c + 2 < nvalid ? 0x0000ffffu : 0u) |
-                             (4 * c + 3 < nvalid ? 0xffff0000u : 0u);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            v0[t].x &= mlo; v0[t].y &= mhi;
-            v1[t].x &= mlo; v1[t].y &= mhi;
-        }
     }
     float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
@@ -385,17 +365,44 @@ __device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D /
         e01 = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(h01), p1 - pa_dev::bf16_hi(h01));
         e23 = pa_dev::pack_bf16(p2 - pa_dev::bf16_lo(h23), p3 - pa_dev::bf16_hi(h23));
     }
-    const uint32_t bh0 = pa_dev::movmatrix_trans(h01), bh1 = pa_dev::movmatrix_trans(h23);
-    const uint32_t be0 = pa_dev::movmatrix_trans(e01), be1 = pa_dev::movmatrix_trans(e23);
+    bh0 = pa_dev::movmatrix_trans(h01);
+    bh1 = pa_dev::movmatrix_trans(h23);
+    be0 = pa_dev::movmatrix_trans(e01);
+    be1 = pa_dev::movmatrix_trans(e23);
+}
+
+// One bf16 16-token tile: scores, online-softmax update, value product.
+template <int D>
+__device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D / 32],
+                                            const uint4 (&k1)[D / 32], uint2 (&v0)[D / 16],
+                                            uint2 (&v1)[D / 16], int nvalid, float sl, int r0,
+                                            int r1, int c) {
+    constexpr int NJ = D / 32, NT = D / 16;
+    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};   // two chains
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        pa_dev::mma_bf16_16816(sc, k0[j].x, k1[j].x, k0[j].y, k1[j].y, a.qf[j].x, a.qf[j].y);
+        pa_dev::mma_bf16_16816(sd, k0[j].z, k1[j].z, k0[j].w, k1[j].w, a.qf[j].z, a.qf[j].w);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[i] += sd[i];
+    if (nvalid < 16) {                        // 0 * Inf is NaN: clear the values past the tile's end
+        const uint32_t mlo = (4 * c < nvalid ? 0x0000ffffu : 0u) |
+                             (4 * c + 1 < nvalid ? 0xffff0000u : 0u);
+        const uint32_t mhi = (4 * c + 2 < nvalid ? 0x0000ffffu : 0u) |
+                             (4 * c + 3 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            v0[t].x &= mlo; v0[t].y &= mhi;
+            v1[t].x &= mlo; v1[t].y &= mhi;
+        }
+    }
+    uint32_t bh0, bh1, be0, be1;
+    softmax_tile<D, false>(a, sc, nvalid, sl, r0, r1, bh0, bh1, be0, be1);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        if constexpr (F8) {
-            pa_dev::mma_f16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, bh0, bh1);
-            pa_dev::mma_f16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, be0, be1);
-        } else {
-            pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, bh0, bh1);
-            pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, be0, be1);
-        }
+        pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, bh0, bh1);
+        pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, be0, be1);
     }
 }
 
@@ -406,6 +413,46 @@ __device__ __forceinline__ uint4 widen8(uint2 c) {
 }
 __device__ __forceinline__ uint2 widen4(uint32_t c) {
     return make_uint2(pa_dev::e4m3x2_to_f16x2(c), pa_dev::e4m3x2_to_f16x2(c >> 16));
+}
+
+// One 16-token tile of an fp8 pool from its raw codes: K as 8-byte pieces
+// (token rows r0 / r1, 16-byte chunk j of the bf16 layout), V^T as 4-byte
+// pieces (value rows 16t+g / 16t+g+8, tokens 4c..4c+3).  Each piece is
+// widened to f16 pairs just before the MMA that reads it, so only a few
+// widened fragments are live at once; the codes of tokens past the tile's end
+// are cleared before widening (code 0 is +0).
+template <int D>
+__device__ __forceinline__ void tile_update_f8(WarpAcc<D>& a, const uint2 (&k0)[D / 32],
+                                               const uint2 (&k1)[D / 32], uint32_t (&v0)[D / 16],
+                                               uint32_t (&v1)[D / 16], int nvalid, float sl,
+                                               int r0, int r1, int c) {
+    constexpr int NJ = D / 32, NT = D / 16;
+    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};   // two chains
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        const uint4 a0 = widen8(k0[j]), a1 = widen8(k1[j]);
+        pa_dev::mma_f16_16816(sc, a0.x, a1.x, a0.y, a1.y, a.qf[j].x, a.qf[j].y);
+        pa_dev::mma_f16_16816(sd, a0.z, a1.z, a0.w, a1.w, a.qf[j].z, a.qf[j].w);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[i] += sd[i];
+    if (nvalid < 16) {                        // partly filled last tile
+        const int nv4 = min(max(nvalid - 4 * c, 0), 4);  // this thread's valid tokens of 4
+        const uint32_t vm = nv4 >= 4 ? 0xffffffffu : (1u << (8 * nv4)) - 1u;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            v0[t] &= vm;
+            v1[t] &= vm;
+        }
+    }
+    uint32_t bh0, bh1, be0, be1;
+    softmax_tile<D, true>(a, sc, nvalid, sl, r0, r1, bh0, bh1, be0, be1);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const uint2 a0 = widen4(v0[t]), a1 = widen4(v1[t]);
+        pa_dev::mma_f16_16816(a.o[t], a0.x, a1.x, a0.y, a1.y, bh0, bh1);
+        pa_dev::mma_f16_16816(a.o[t], a0.x, a1.x, a0.y, a1.y, be0, be1);
+    }
 }
 // Eight bf16 values re-rounded to f16 (exact for magnitudes 2^-17 .. 65504).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
@@ -436,7 +483,9 @@ __device__ __forceinline__ void cp_async_wait() {
 // f16 pairs in registers; the queries are re-rounded to f16 once per item.
 // BS > 0: the pool's block size is known to be BS at compile time (16-token
 // blocks: one 16-token tile per block, constant value-row strides).
-template <int D, bool FUSE, bool F8 = false, int BS = 0>
+// AHEAD (fp8): load each tile's codes one tile ahead of the tile being
+// computed, for kernels whose register budget holds a second tile's codes.
+template <int D, bool FUSE, bool F8 = false, int BS = 0, bool AHEAD = false>
 __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, int tok0,
                                           int tok1, int L, float* sm_o, float* sm_m,
                                           float* sm_l) {
@@ -557,10 +606,14 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
         }
     };
     // fp8 pool: the warp's 16-token tiles one after another, each tile's raw
-    // codes (K: 8-byte pieces, V^T: 4-byte pieces, 32 registers) loaded one
-    // tile ahead of the tile being widened and computed, so that every warp
-    // keeps two tiles' loads in flight (at one byte per element a tile is half
-    // the bytes of a bf16 tile, and one tile in flight per warp left HBM idle).
+    // codes (K: 8-byte pieces, V^T: 4-byte pieces, 32 registers) loaded, then
+    // widened piece by piece just before the MMAs that read them (walk_f8
+    // below).  Holding one tile's codes instead of two lets the walk fit 128
+    // registers, four CTAs (16 warps) per SM: more loads in flight per SM than
+    // three CTAs with a one-tile lookahead (on GB300, with the merge below,
+    // 48-50 against 52 us on the decode batch, 246-250 against 251 us on long
+    // context).  The shared-prefix kernel runs two CTAs per SM, whose register
+    // budget holds a second tile: it loads one tile ahead (AHEAD).
     //
     // Fused append into an fp8 pool: the warp that owns the block holding
     // position L-1 quantizes the new token's bf16 key row and value column
@@ -599,10 +652,10 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
         const unsigned char* vb = static_cast<const unsigned char*>(p.v);
         const int nunits = nblk * nsub;
         int my_phys = -1;
-        uint2 rk0[NJ], rk1[NJ];
-        uint32_t rv0[NT], rv1[NT];
-        int r_valid = 0;                          // tokens of the loaded tile (0: none)
-        auto load = [&](int u) {
+        // unit u's raw codes into (rk0, rk1, rv0, rv1); returns its valid
+        // tokens (0: nothing to compute)
+        auto load = [&](int u, uint2 (&rk0)[NJ], uint2 (&rk1)[NJ], uint32_t (&rv0)[NT],
+                        uint32_t (&rv1)[NT]) -> int {
             const int i = u / nsub, sub = u - i * nsub;
             if (sub == 0 && (i & 31) == 0) {
                 const int mine = lb0 + warp + kWarps * (i + lane);
@@ -619,12 +672,11 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
             }
             const int lb = lb0 + warp + kWarps * i;
             const int nv = min(16, L - (lb * B + sub * 16));
-            r_valid = 0;
             if (phys < 0 || phys >= p.num_blocks) {
                 if (lane == 0 && sub == 0) record_error(p.err, PA_ERR_BAD_BLOCK_ID);
-                return;
+                return 0;
             }
-            if (nv <= 0) return;
+            if (nv <= 0) return 0;
             const size_t tile = (static_cast<size_t>(phys) * p.Hkv + h) * tile_elems;
             const unsigned char* kt = kb + tile + static_cast<size_t>(sub) * 16 * D;
             const unsigned char* vt = vb + tile + sub * 16 + 4 * c;
@@ -642,29 +694,28 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
                 rv1[t] = CG ? pa_dev::ld_cg4(vt + static_cast<size_t>(16 * t + g + 8) * B)
                             : pa_dev::ld_stream4(vt + static_cast<size_t>(16 * t + g + 8) * B);
             }
-            r_valid = nv;
+            return nv;
         };
-        // head_dim 256 has no registers to spare for a second tile: no lookahead
-        constexpr bool kAhead = D <= 128;
-        if (kAhead && nunits > 0) load(0);
-        for (int u = 0; u < nunits; ++u) {
-            if constexpr (!kAhead) load(u);
-            uint2 ck0[NJ], ck1[NJ];
-            uint32_t cv0[NT], cv1[NT];
+        uint2 ak0[NJ], ak1[NJ];
+        uint32_t av0[NT], av1[NT];
+        if constexpr (AHEAD) {
+            // the next tile's codes load while the current tile is computed
+            int na = nunits > 0 ? load(0, ak0, ak1, av0, av1) : 0;
+            for (int u = 0; u < nunits; ++u) {
+                uint2 bk0[NJ], bk1[NJ];
+                uint32_t bv0[NT], bv1[NT];
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) { ck0[j] = rk0[j]; ck1[j] = rk1[j]; }
+                for (int j = 0; j < NJ; ++j) { bk0[j] = ak0[j]; bk1[j] = ak1[j]; }
 #pragma unroll
-            for (int t = 0; t < NT; ++t) { cv0[t] = rv0[t]; cv1[t] = rv1[t]; }
-            const int nvalid = r_valid;
-            if (kAhead && u + 1 < nunits) load(u + 1);
-            if (nvalid > 0) {
-                uint4 k0[NJ], k1[NJ];
-                uint2 v0[NT], v1[NT];
-#pragma unroll
-                for (int j = 0; j < NJ; ++j) { k0[j] = widen8(ck0[j]); k1[j] = widen8(ck1[j]); }
-#pragma unroll
-                for (int t = 0; t < NT; ++t) { v0[t] = widen4(cv0[t]); v1[t] = widen4(cv1[t]); }
-                tile_update<D, true>(a, k0, k1, v0, v1, nvalid, sl, r0, r1, c);
+                for (int t = 0; t < NT; ++t) { bv0[t] = av0[t]; bv1[t] = av1[t]; }
+                const int nb = na;
+                na = u + 1 < nunits ? load(u + 1, ak0, ak1, av0, av1) : 0;
+                if (nb > 0) tile_update_f8<D>(a, bk0, bk1, bv0, bv1, nb, sl, r0, r1, c);
+            }
+        } else {
+            for (int u = 0; u < nunits; ++u) {   // one tile's codes at a time (see above)
+                const int na = load(u, ak0, ak1, av0, av1);
+                if (na > 0) tile_update_f8<D>(a, ak0, ak1, av0, av1, na, sl, r0, r1, c);
             }
         }
     };
@@ -986,7 +1037,7 @@ __host__ __device__ constexpr size_t fast_front_bytes(int D, bool shared) {
 
 
 template <int D, bool SHARED, bool FUSE, bool F8 = false>
-__global__ void __launch_bounds__(kThreads, SHARED ? 2 : kMinCtas)
+__global__ void __launch_bounds__(kThreads, SHARED || (F8 && D > 128) ? 2 : (F8 ? kMinCtasF8 : kMinCtas))
 decode_fast_kernel(const DecodeParams p) {
     constexpr int OS = D + 4;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -1026,7 +1077,7 @@ decode_fast_kernel(const DecodeParams p) {
         // instructions, 5 % faster); the bf16 walk, bound by load latency, ran
         // 1.5 us slower with it on the decode batch (measured on GB300)
         if (F8 && p.B == 16)
-            fast_item<D, FUSE, F8, 16>(p, s, h, tok0, tok1, L, sm_o, sm_m, sm_l);
+            fast_item<D, FUSE, F8, 16, SHARED && D <= 128>(p, s, h, tok0, tok1, L, sm_o, sm_m, sm_l);
         else
             fast_item<D, FUSE, F8>(p, s, h, tok0, tok1, L, sm_o, sm_m, sm_l);
         // the next item's ticket, taken as soon as warp 0 is done with this
@@ -1035,29 +1086,46 @@ decode_fast_kernel(const DecodeParams p) {
         int ticket = 0;
         if (threadIdx.x == 0) ticket = atomicAdd(p.ticket, 1);
         __syncthreads();
-        // merge the warps' softmax states (in place into warp 0's buffer)
-        for (int idx = threadIdx.x; idx < p.G * D; idx += kThreads) {
-            const int n = idx / D, d = idx - n * D;
+        // merge the warps' softmax states: first, per head n, the weight of
+        // each warp's sums (2^(m_w - M), written over sm_m) and the combined
+        // (M, l); then every thread combines its (head, column) elements and
+        // writes them out: the normalised output row when the sequence has one
+        // partition, else the item's partial for the merge kernel
+        if (threadIdx.x < p.G) {
+            const int n = threadIdx.x;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 8 + n]);
-            float acc = 0.f, l = 0.f;
-            if (M != -INFINITY) {
+            float l = 0.f;
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float f = pa_dev::ex2(sm_m[w * 8 + n] - M);
-                    acc += f * sm_o[(w * 8 + n) * OS + d];
-                    l += f * sm_l[w * 8 + n];
-                }
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = M != -INFINITY ? pa_dev::ex2(sm_m[w * 8 + n] - M) : 0.f;
+                l += f * sm_l[w * 8 + n];
+                sm_m[w * 8 + n] = f;
             }
-            sm_o[n * OS + d] = acc;
-            if (d == 0) {
-                res_m[n] = M;
-                res_l[n] = l;
-            }
+            res_m[n] = M;
+            res_l[n] = l;
         }
         __syncthreads();
-        finish_item(p, pitem, s, h, nP, res_m, res_l, sm_o, OS);
+        const bool single = nP == 1 && !in_group(p, s);
+        const size_t dst0 = single ? (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G) * D
+                                   : static_cast<size_t>(pitem) * p.G * D;
+        for (int idx = threadIdx.x; idx < p.G * D; idx += kThreads) {
+            const int n = idx / D, d = idx - n * D;
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) acc += sm_m[w * 8 + n] * sm_o[(w * 8 + n) * OS + d];
+            if (single) {
+                const float l = res_l[n];
+                store_out(p, dst0 + idx, l > 0.f ? acc * p.v_scale / l : 0.f);
+            } else {
+                p.part_acc[dst0 + idx] = acc * p.v_scale;
+            }
+        }
+        if (!single && threadIdx.x < p.G) {
+            p.part_ml[(static_cast<size_t>(pitem) * p.G + threadIdx.x) * 2 + 0] = res_m[threadIdx.x];
+            p.part_ml[(static_cast<size_t>(pitem) * p.G + threadIdx.x) * 2 + 1] = res_l[threadIdx.x];
+        }
         if (threadIdx.x == 0) s_flag[1] = static_cast<int>(gridDim.x) + ticket;
         __syncthreads();
         item = s_flag[1];
@@ -1340,7 +1408,9 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
     if (occ <= 0) return PA_ERR_UNSUPPORTED;
     plan->grid = pool->num_sms * occ;
     if (fast) {
-        plan->items_target = plan->grid * kItemsPerCta;
+        // the mma.sync shared-prefix kernel (two CTAs per SM) keeps four items per
+        // CTA (faster on the fp8 prefix batch than twelve per SM, measured on GB300)
+        plan->items_target = plan->shared && !plan->tc ? plan->grid * 4 : pool->num_sms * kItemsPerSm;
         // items <= Hkv * (total / PT + S); PT >= total * Hkv / items_target keeps
         // that below min_items.  The extra items_target of room lets the
         // partition cap and the guided tail take effect; the kernel never
