@@ -407,12 +407,16 @@ __device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D /
 }
 
 // Eight e4m3 codes (8 bytes) widened to four f16 pairs, and four to two.
-__device__ __forceinline__ uint4 widen8(uint2 c) {
-    return make_uint4(pa_dev::e4m3x2_to_f16x2(c.x), pa_dev::e4m3x2_to_f16x2(c.x >> 16),
-                      pa_dev::e4m3x2_to_f16x2(c.y), pa_dev::e4m3x2_to_f16x2(c.y >> 16));
-}
 __device__ __forceinline__ uint2 widen4(uint32_t c) {
-    return make_uint2(pa_dev::e4m3x2_to_f16x2(c), pa_dev::e4m3x2_to_f16x2(c >> 16));
+    uint2 y;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(y.x), "=r"(y.y) : "r"(c));
+    return y;
+}
+__device__ __forceinline__ uint4 widen8(uint2 c) {
+    const uint2 a = widen4(c.x), b = widen4(c.y);
+    return make_uint4(a.x, a.y, b.x, b.y);
 }
 
 // One 16-token tile of an fp8 pool from its raw codes: K as 8-byte pieces
