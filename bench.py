@@ -126,6 +126,7 @@ TRAFFIC_PROFILES = {
     ("decode", "bf16"): "decode_kernel_decode_batch.md",
     ("decode", "fp8"): "decode_kernel_decode_batch_fp8.md",
     ("long", "bf16"): "decode_kernel_long_context.md",
+    ("long", "fp8"): "decode_kernel_long_context_fp8.md",
     ("mixed", "bf16"): "decode_kernel_mixed.md",
     ("prefix", "bf16"): "decode_call_prefix.md",
     ("prefill", "bf16"): "prefill_tc_prefill_batch.md",
