@@ -371,12 +371,46 @@ __device__ __forceinline__ void softmax_tile(WarpAcc<D>& a, const float (&sc)[4]
     be1 = pa_dev::movmatrix_trans(e23);
 }
 
+// O^T += V^T . P^T for one tile.  pack (G <= 4): the score columns 4..7
+// repeat heads 0..3, so those columns carry the probabilities' remainders
+// and one MMA per m-tile takes both parts (the two halves of the sums are
+// added once per item); otherwise the rounded pair and the remainder go
+// through two MMAs into the same accumulators.
+// afrag(t, x) fills the A fragment of m-tile t (value rows 16t..16t+15).
+template <int D, bool F16, typename AFrag>
+__device__ __forceinline__ void value_product(WarpAcc<D>& a, AFrag&& afrag, bool pack, uint32_t bh0,
+                                              uint32_t bh1, uint32_t be0, uint32_t be1) {
+    constexpr int NT = D / 16;
+    auto mma = [](float (&d)[4], const uint32_t (&x)[4], uint32_t b0, uint32_t b1) {
+        if constexpr (F16) pa_dev::mma_f16_16816(d, x[0], x[1], x[2], x[3], b0, b1);
+        else pa_dev::mma_bf16_16816(d, x[0], x[1], x[2], x[3], b0, b1);
+    };
+    if (pack) {
+        const bool upper = (threadIdx.x & 31) >= 16;          // columns 4..7
+        const uint32_t b0 = upper ? be0 : bh0, b1 = upper ? be1 : bh1;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            uint32_t x[4];
+            afrag(t, x);
+            mma(a.o[t], x, b0, b1);
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            uint32_t x[4];
+            afrag(t, x);
+            mma(a.o[t], x, bh0, bh1);
+            mma(a.o[t], x, be0, be1);
+        }
+    }
+}
+
 // One bf16 16-token tile: scores, online-softmax update, value product.
 template <int D>
 __device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D / 32],
                                             const uint4 (&k1)[D / 32], uint2 (&v0)[D / 16],
                                             uint2 (&v1)[D / 16], int nvalid, float sl, int r0,
-                                            int r1, int c) {
+                                            int r1, int c, bool pack) {
     constexpr int NJ = D / 32, NT = D / 16;
     float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};   // two chains
 #pragma unroll
@@ -399,11 +433,12 @@ __device__ __forceinline__ void tile_update(WarpAcc<D>& a, const uint4 (&k0)[D /
     }
     uint32_t bh0, bh1, be0, be1;
     softmax_tile<D, false>(a, sc, nvalid, sl, r0, r1, bh0, bh1, be0, be1);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, bh0, bh1);
-        pa_dev::mma_bf16_16816(a.o[t], v0[t].x, v1[t].x, v0[t].y, v1[t].y, be0, be1);
-    }
+    value_product<D, false>(
+        a,
+        [&](int t, uint32_t (&x)[4]) {
+            x[0] = v0[t].x; x[1] = v1[t].x; x[2] = v0[t].y; x[3] = v1[t].y;
+        },
+        pack, bh0, bh1, be0, be1);
 }
 
 // Eight e4m3 codes (8 bytes) widened to four f16 pairs, and four to two.
@@ -429,7 +464,7 @@ template <int D>
 __device__ __forceinline__ void tile_update_f8(WarpAcc<D>& a, const uint2 (&k0)[D / 32],
                                                const uint2 (&k1)[D / 32], uint32_t (&v0)[D / 16],
                                                uint32_t (&v1)[D / 16], int nvalid, float sl,
-                                               int r0, int r1, int c) {
+                                               int r0, int r1, int c, bool pack) {
     constexpr int NJ = D / 32, NT = D / 16;
     float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};   // two chains
 #pragma unroll
@@ -451,12 +486,13 @@ __device__ __forceinline__ void tile_update_f8(WarpAcc<D>& a, const uint2 (&k0)[
     }
     uint32_t bh0, bh1, be0, be1;
     softmax_tile<D, true>(a, sc, nvalid, sl, r0, r1, bh0, bh1, be0, be1);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        const uint2 a0 = widen4(v0[t]), a1 = widen4(v1[t]);
-        pa_dev::mma_f16_16816(a.o[t], a0.x, a1.x, a0.y, a1.y, bh0, bh1);
-        pa_dev::mma_f16_16816(a.o[t], a0.x, a1.x, a0.y, a1.y, be0, be1);
-    }
+    value_product<D, true>(
+        a,
+        [&](int t, uint32_t (&x)[4]) {
+            const uint2 a0 = widen4(v0[t]), a1 = widen4(v1[t]);
+            x[0] = a0.x; x[1] = a1.x; x[2] = a0.y; x[3] = a1.y;
+        },
+        pack, bh0, bh1, be0, be1);
 }
 // Eight bf16 values re-rounded to f16 (exact for magnitudes 2^-17 .. 65504).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
@@ -500,14 +536,22 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
     const int g = lane >> 2, c = lane & 3;
     const int B = BS > 0 ? BS : p.B, nsub = B / 16;
 
+    // fp8 pool, G <= 4: the score columns 4..7 repeat heads 0..3 (their
+    // queries loaded twice), which lets the value product carry the
+    // probabilities' remainders there (value_product): 8 instead of 16 value
+    // MMAs per tile for the instruction-bound fp8 walk (long context 248 ->
+    // 236 us on GB300); the bf16 walk, bound by load latency, ran 1.3 us
+    // slower with it on the decode batch
+    const bool pack = F8 && p.G <= 4;
+    const int hq = pack ? (g & 3) : g;    // the query head of score column g
     WarpAcc<D> a;
     {
         const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
-                               (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G + g) * D;
+                               (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G + hq) * D;
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
-            a.qf[j] = g < p.G ? __ldg(reinterpret_cast<const uint4*>(qrow + (4 * j + c) * 8))
-                              : make_uint4(0u, 0u, 0u, 0u);
+            a.qf[j] = hq < p.G ? __ldg(reinterpret_cast<const uint4*>(qrow + (4 * j + c) * 8))
+                               : make_uint4(0u, 0u, 0u, 0u);
             if constexpr (F8) a.qf[j] = bf16x8_to_f16x8(a.qf[j]);
         }
     }
@@ -605,7 +649,7 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
                     v1[t] = CG ? pa_dev::ld_cg8(vt + static_cast<size_t>(16 * t + g + 8) * B)
                                  : pa_dev::ld_stream8(vt + static_cast<size_t>(16 * t + g + 8) * B);
                 }
-                tile_update<D>(a, k0, k1, v0, v1, nvalid, sl, r0, r1, c);
+                tile_update<D>(a, k0, k1, v0, v1, nvalid, sl, r0, r1, c, pack);
             }
         }
     };
@@ -714,12 +758,12 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
                 for (int t = 0; t < NT; ++t) { bv0[t] = av0[t]; bv1[t] = av1[t]; }
                 const int nb = na;
                 na = u + 1 < nunits ? load(u + 1, ak0, ak1, av0, av1) : 0;
-                if (nb > 0) tile_update_f8<D>(a, bk0, bk1, bv0, bv1, nb, sl, r0, r1, c);
+                if (nb > 0) tile_update_f8<D>(a, bk0, bk1, bv0, bv1, nb, sl, r0, r1, c, pack);
             }
         } else {
             for (int u = 0; u < nunits; ++u) {   // one tile's codes at a time (see above)
                 const int na = load(u, ak0, ak1, av0, av1);
-                if (na > 0) tile_update_f8<D>(a, ak0, ak1, av0, av1, na, sl, r0, r1, c);
+                if (na > 0) tile_update_f8<D>(a, ak0, ak1, av0, av1, na, sl, r0, r1, c, pack);
             }
         }
     };
@@ -741,6 +785,14 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
     for (int off = 4; off < 32; off <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    if (pack) {
+        // the sums of the remainders (columns 4..7, lanes c + 2) join those of
+        // the rounded pairs (columns 0..3)
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a.o[t][i] += __shfl_down_sync(0xffffffffu, a.o[t][i], 2);
     }
     float* mo = sm_o + warp * 8 * OS;
 #pragma unroll

@@ -106,6 +106,15 @@ SMALL = [
                     head_dim=64, dtype="fp8")),
     ("decode", dict(num_seqs=3, min_len=1, max_len=200, num_q_heads=8, num_kv_heads=2,
                     head_dim=256, dtype="fp8")),
+    # G = 1, 2, 3 (score columns 4..7 repeat the group's heads and carry the
+    # probabilities' remainders into the value product) and G = 5 (no repeat)
+    ("decode", dict(num_seqs=4, min_len=1, max_len=300, num_q_heads=8, num_kv_heads=8,
+                    head_dim=128, dtype="fp8")),
+    ("decode", dict(lengths=[1, 17, 250], num_q_heads=16, num_kv_heads=8, head_dim=128, dtype="fp8")),
+    ("decode", dict(num_seqs=4, min_len=1, max_len=300, num_q_heads=12, num_kv_heads=4,
+                    head_dim=128, dtype="fp8")),
+    ("decode", dict(num_seqs=4, min_len=1, max_len=300, num_q_heads=20, num_kv_heads=4,
+                    head_dim=128, dtype="fp8")),
     ("decode", dict(num_seqs=4, min_len=1, max_len=200, block_size=32, **D128)),
     ("decode", dict(num_seqs=4, min_len=1, max_len=100, block_size=8, **D128)),   # fp32 kernel
     ("decode", dict(num_seqs=3, min_len=1, max_len=100, num_q_heads=32, num_kv_heads=2,
