@@ -57,6 +57,7 @@ constexpr int kSharedUnitsPerSync = 2;  // tiles consumed per barrier by shared-
 static_assert(kSharedStages > kSharedUnitsPerSync, "shared pipeline needs copies in flight");
 static_assert(kSharedUnitsPerSync % 2 == 0, "shared items consume 32-token tiles");
 constexpr int kThreads = kWarps * 32;
+constexpr int kMergeThreads = 512;      // merge kernel: four groups of 128 threads share a (sequence, KV head)
 
 using pa_dev::record_error;
 
@@ -1310,7 +1311,9 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(const DecodePar
 //   M = max_q m_q,  L = sum_q l_q 2^(m_q - M),  out = sum_q acc_q 2^(m_q - M) / L.
 // Launched as a programmatic dependent of the split kernel: it may start while
 // the split kernel drains and waits (griddepcontrol.wait) for it to finish.
-__global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodeParams p) {
+template <bool WIDE>
+__global__ void __launch_bounds__(WIDE ? kMergeThreads : kThreads, WIDE ? 2 : 1)
+decode_merge_kernel(const DecodeParams p) {
     pa_dev::wait_prior_grid();
     pa_dev::allow_next_grid();
     const int s = blockIdx.x / p.Hkv, h = blockIdx.x - s * p.Hkv;
@@ -1331,49 +1334,90 @@ __global__ void __launch_bounds__(kThreads) decode_merge_kernel(const DecodePara
         return q < nP ? static_cast<size_t>(item0) + static_cast<size_t>(q) * p.Hkv
                       : slot0 + static_cast<size_t>(q - nP) * p.Hkv;
     };
-    // Each thread owns 4 consecutive elements of one head (D % 4 == 0) and
-    // folds the partials in by an online log-sum-exp, loading a batch of
-    // kBatch partials (their (max, sum) and its 4 values) at once so that a
-    // batch costs one memory latency.
-    constexpr int kBatch = 8;
+    // Each thread owns 4 consecutive elements of one head (D % 4 == 0).  The
+    // CTA's threads form R groups of nqt threads; group r folds partials r,
+    // r + R, ... by an online log-sum-exp, loading a batch of kBatch partials
+    // (their (max, sum) and its 4 values) at once so that a batch costs one
+    // memory latency; the groups' states then combine through shared memory.
+    // WIDE (many partials per (sequence, head); long contexts: ~30):
+    // kMergeThreads threads, whose groups shorten each thread's chain of
+    // batches R-fold; otherwise kThreads threads, one group.
+    constexpr int kBatch = WIDE ? 4 : 8;
+    constexpr int kT = WIDE ? kMergeThreads : kThreads;
+    __shared__ float4 red_acc[WIDE ? kMergeThreads : 1];
+    __shared__ float2 red_ml[WIDE ? kMergeThreads : 1];
+    const int nq = GD / 4;                                  // element quads of the (sequence, head)
+    const int nqt = min(nq, kT);                            // threads per group
+    const int R = WIDE ? kT / nqt : 1;                      // groups (the narrow form: one)
+    const int r = static_cast<int>(threadIdx.x) / nqt, qd = static_cast<int>(threadIdx.x) - r * nqt;
     const size_t out0 = (static_cast<size_t>(s) * p.Hq + static_cast<size_t>(h) * p.G) * p.D;
-    for (int e = threadIdx.x * 4; e < GD; e += kThreads * 4) {
-        const int n = e / p.D;
+    for (int quad0 = 0; quad0 < nq; quad0 += nqt) {
+        const int quad = quad0 + qd;
+        const bool mine = r < R && quad < nq;
         float M = -INFINITY, L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q0 = 0; q0 < nAll; q0 += kBatch) {
-            float2 ml[kBatch];
-            float4 x[kBatch];
+        if (mine) {
+            const int e = quad * 4, n = e / p.D;
+            for (int q0 = r; q0 < nAll; q0 += kBatch * R) {
+                float2 ml[kBatch];
+                float4 x[kBatch];
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                ml[k] = make_float2(-INFINITY, 0.f);
-                x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (q0 + k < nAll) {
-                    const size_t it = part(q0 + k);
-                    const bool pr = q0 + k < nP;
-                    ml[k] = __ldcg(reinterpret_cast<const float2*>((pr ? p.part_ml : p.spart_ml) + (it * p.G + n) * 2));
-                    x[k] = __ldcg(reinterpret_cast<const float4*>((pr ? p.part_acc : p.spart_acc) + it * GD + e));
+                for (int k = 0; k < kBatch; ++k) {
+                    const int q = q0 + k * R;
+                    ml[k] = make_float2(-INFINITY, 0.f);
+                    x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (q < nAll) {
+                        const size_t it = part(q);
+                        const bool pr = q < nP;
+                        ml[k] = __ldcg(reinterpret_cast<const float2*>((pr ? p.part_ml : p.spart_ml) + (it * p.G + n) * 2));
+                        x[k] = __ldcg(reinterpret_cast<const float4*>((pr ? p.part_acc : p.spart_acc) + it * GD + e));
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    if (ml[k].x == -INFINITY) continue;     // absent, or a partial that saw nothing
+                    const float nm = fmaxf(M, ml[k].x);
+                    const float fo = M == -INFINITY ? 0.f : pa_dev::ex2(M - nm);
+                    const float fn = pa_dev::ex2(ml[k].x - nm);
+                    L = L * fo + ml[k].y * fn;
+                    acc.x = acc.x * fo + x[k].x * fn;
+                    acc.y = acc.y * fo + x[k].y * fn;
+                    acc.z = acc.z * fo + x[k].z * fn;
+                    acc.w = acc.w * fo + x[k].w * fn;
+                    M = nm;
                 }
             }
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                if (ml[k].x == -INFINITY) continue;         // absent, or a partial that saw nothing
-                const float nm = fmaxf(M, ml[k].x);
-                const float fo = M == -INFINITY ? 0.f : pa_dev::ex2(M - nm);
-                const float fn = pa_dev::ex2(ml[k].x - nm);
-                L = L * fo + ml[k].y * fn;
-                acc.x = acc.x * fo + x[k].x * fn;
-                acc.y = acc.y * fo + x[k].y * fn;
-                acc.z = acc.z * fo + x[k].z * fn;
-                acc.w = acc.w * fo + x[k].w * fn;
-                M = nm;
-            }
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        store_out(p, out0 + e + 0, acc.x * inv);
-        store_out(p, out0 + e + 1, acc.y * inv);
-        store_out(p, out0 + e + 2, acc.z * inv);
-        store_out(p, out0 + e + 3, acc.w * inv);
+        if (WIDE && R > 1) {
+            red_acc[threadIdx.x] = acc;
+            red_ml[threadIdx.x] = make_float2(M, L);
+            __syncthreads();
+            if (r == 0 && mine) {
+                for (int g2 = 1; g2 < R; ++g2) {
+                    const float2 o = red_ml[g2 * nqt + qd];
+                    if (o.x == -INFINITY) continue;
+                    const float4 y = red_acc[g2 * nqt + qd];
+                    const float nm = fmaxf(M, o.x);
+                    const float fo = M == -INFINITY ? 0.f : pa_dev::ex2(M - nm);
+                    const float fn = pa_dev::ex2(o.x - nm);
+                    L = L * fo + o.y * fn;
+                    acc.x = acc.x * fo + y.x * fn;
+                    acc.y = acc.y * fo + y.y * fn;
+                    acc.z = acc.z * fo + y.z * fn;
+                    acc.w = acc.w * fo + y.w * fn;
+                    M = nm;
+                }
+            }
+            __syncthreads();                                // red_* reuse by the next quads
+        }
+        if (r == 0 && mine) {
+            const int e = quad * 4;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            store_out(p, out0 + e + 0, acc.x * inv);
+            store_out(p, out0 + e + 1, acc.y * inv);
+            store_out(p, out0 + e + 2, acc.z * inv);
+            store_out(p, out0 + e + 3, acc.w * inv);
+        }
     }
 }
 
@@ -1536,8 +1580,14 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
     }
     count_launch();
     if (e != cudaSuccess) return PA_ERR_CUDA;
-    e = launch_pdl(decode_merge_kernel, dim3(static_cast<unsigned>(p.S) * static_cast<unsigned>(p.Hkv)),
-                   dim3(kThreads), 0, st, p);
+    // many partials per (sequence, KV head): split each one's partials over
+    // four thread groups (long context 424 -> 416 us, on an fp8 pool 238 ->
+    // 229 us, on GB300)
+    const dim3 mgrid(static_cast<unsigned>(p.S) * static_cast<unsigned>(p.Hkv));
+    if (plan.fast && plan.items_target >= 8 * p.S * p.Hkv)
+        e = launch_pdl(decode_merge_kernel<true>, mgrid, dim3(kMergeThreads), 0, st, p);
+    else
+        e = launch_pdl(decode_merge_kernel<false>, mgrid, dim3(kThreads), 0, st, p);
     count_launch();
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
