@@ -1452,7 +1452,6 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
     const bool fp8 = pool->dtype == PA_FP8E4M3;
     const bool tc_shape = (D == 64 || D == 128 || D == 256) && B % 16 == 0 && G <= 8;
     const bool fast = tc_shape && (pool->dtype == PA_BF16 || fp8);
-    if (fp8) plan->tc = false;      // an fp8 pool's shared items run on the mma.sync form
     plan->fast = fast;
     plan->pool = pool;
     plan->bf16 = pool->dtype == PA_BF16;
@@ -1544,9 +1543,15 @@ int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t 
         DecodeParams q = p;
         q.n_shared_items = 0;
         q.defer_wait = 1;
-        if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, false>, grid, block, plan.smem, st, q);
-        else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, false>, grid, block, plan.smem, st, q);
-        else e = launch_pdl(decode_fast_kernel<256, false, false>, grid, block, plan.smem, st, q);
+        if (plan.fp8) {
+            if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, false, true>, grid, block, plan.smem, st, q);
+            else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, false, true>, grid, block, plan.smem, st, q);
+            else e = launch_pdl(decode_fast_kernel<256, false, false, true>, grid, block, plan.smem, st, q);
+        } else {
+            if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, false, false>, grid, block, plan.smem, st, q);
+            else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, false, false>, grid, block, plan.smem, st, q);
+            else e = launch_pdl(decode_fast_kernel<256, false, false>, grid, block, plan.smem, st, q);
+        }
     } else if (plan.fast && plan.shared && plan.fp8) {
         if (p.D == 64) e = launch_pdl(decode_fast_kernel<64, true, false, true>, grid, block, plan.smem, st, p);
         else if (p.D == 128) e = launch_pdl(decode_fast_kernel<128, true, false, true>, grid, block, plan.smem, st, p);

@@ -86,17 +86,43 @@ __device__ __forceinline__ int seq_len(const DecodeParams& p, int s) {
 // flag that ends the others' waits at once, records PA_ERR_CUDA, and the CTA
 // drains its own copies and MMAs before it frees TMEM and exits.
 constexpr int kWsThreads = 224;
+constexpr int kWsThreadsF8 = 352;                        // fp8 pools: + 4 converter warps (7-10)
 constexpr int kWsStages = 4;
 constexpr uint32_t kWsStageOff = 32768;                  // after Q (2 x [128][128 B])
-constexpr uint32_t kWsBarOff = kWsStageOff + kWsStages * kStageBytes;
+constexpr uint32_t kWsCodeOff = kWsStageOff + kWsStages * kStageBytes;   // fp8: each stage's raw codes
+constexpr uint32_t kWsCodeBytes = 16384;                  // 4 blocks x (K 2 KB, then V^T 2 KB) of e4m3 codes
 enum WsBar {
     kQFull, kQEmpty, kSFull0, kSFull1, kSEmpty0, kSEmpty1, kPFull0, kPFull1, kPEmpty0, kPEmpty1,
     kOFull0, kOFull1, kMmaDone, kKvFull0, kKvEmpty0 = kKvFull0 + kWsStages,
-    kNumWsBars = kKvEmpty0 + kWsStages
+    kKvConv0 = kKvEmpty0 + kWsStages,        // fp8: the stage's codes are widened (4 converter warps)
+    kQConv = kKvConv0 + kWsStages,           // fp8: the Q tile is in f16
+    kNumWsBars
 };
-constexpr uint32_t kWsMiscOff = kWsBarOff + kNumWsBars * 8;   // TMEM slot, abort flag, stage masks
-constexpr uint32_t kWsMembersOff = kWsMiscOff + 64;            // batch index of each row's member
-constexpr uint32_t kWsSmemBytes = kWsMembersOff + 4 * kRows + 1024;   // + alignment slack
+// after the stages (and, for fp8 pools, the code staging): mbarriers, then TMEM
+// slot, abort flag and stage masks, then the batch index of each row's member
+__host__ __device__ constexpr uint32_t ws_bar_off(bool f8) {
+    return kWsCodeOff + (f8 ? kWsStages * kWsCodeBytes : 0);
+}
+__host__ __device__ constexpr uint32_t ws_misc_off(bool f8) { return ws_bar_off(f8) + kNumWsBars * 8; }
+__host__ __device__ constexpr uint32_t ws_members_off(bool f8) { return ws_misc_off(f8) + 64; }
+__host__ __device__ constexpr uint32_t ws_smem_bytes(bool f8) {
+    return ws_members_off(f8) + 4 * kRows + 1024;             // + alignment slack
+}
+static_assert(ws_smem_bytes(true) <= 232448, "fp8 shared-prefix CTA beyond the opt-in shared memory");
+constexpr uint32_t kIdescQK16 = pa_tc::idesc_f16_f32(kRows, kStep);
+constexpr uint32_t kIdescPV16 = pa_tc::idesc_f16_f32(kRows, kD);
+
+// Eight bf16 values (16 bytes) re-rounded to f16 in place (exact for
+// magnitudes 2^-17 .. 65504: every such bf16 value is an f16 value).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x) {
+    auto cv = [](uint32_t w) { return pa_dev::pack_f16(pa_dev::bf16_lo(w), pa_dev::bf16_hi(w)); };
+    return make_uint4(cv(x.x), cv(x.y), cv(x.z), cv(x.w));
+}
+// Eight e4m3 codes (8 bytes, first element in the low byte) widened to f16 (exact).
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 c) {
+    return make_uint4(pa_dev::e4m3x2_to_f16x2(c.x), pa_dev::e4m3x2_to_f16x2(c.x >> 16),
+                      pa_dev::e4m3x2_to_f16x2(c.y), pa_dev::e4m3x2_to_f16x2(c.y >> 16));
+}
 // TMEM columns: S0 [0,64), S1 [64,128), O0 [128,256), O1 [256,384), then two
 // P buffers of 64 columns at 384 and 448, P hi (bf16 pairs) in the first 32
 // and P lo in the next 32
@@ -186,18 +212,26 @@ __device__ __forceinline__ void ws_validate(const DecodeParams& p, const WsItem&
     }
 }
 
-__global__ void __launch_bounds__(kWsThreads, 2)
+// F8 (fp8 pool): the producer copies each block's raw e4m3 codes (K and V^T,
+// 2 KB each per KV head) into the stage's code area; four converter warps
+// widen them to f16 (exact) in the layouts the MMAs read (K: 128-byte swizzle;
+// V^T: 32-byte swizzle; blocks without keys get zero values), re-round each
+// item's Q tile to f16 in place, and release the stage to the MMA issuers; the
+// MMAs are f16, P is an f16 pair, k_scale sits in the score factor and v_scale
+// is applied to the partial sums.  kmap / vmap are unused then.
+template <bool F8>
+__global__ void __launch_bounds__(F8 ? kWsThreadsF8 : kWsThreads, F8 ? 1 : 2)
 shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ unsigned char tc_raw[];
     const uint32_t raw_s = pa_tc::smem_u32(tc_raw);
     unsigned char* base = tc_raw + ((1024u - (raw_s & 1023u)) & 1023u);
     const uint32_t sbase = pa_tc::smem_u32(base);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + kWsBarOff);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kWsMiscOff);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kWsMiscOff + 4);
-    volatile int* stage_mask = reinterpret_cast<volatile int*>(base + kWsMiscOff + 8);   // [kWsStages]
-    int* s_members = reinterpret_cast<int*>(base + kWsMembersOff);   // [kRows], producer only
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + ws_bar_off(F8));
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(base + ws_misc_off(F8));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + ws_misc_off(F8) + 4);
+    volatile int* stage_mask = reinterpret_cast<volatile int*>(base + ws_misc_off(F8) + 8);   // [kWsStages]
+    int* s_members = reinterpret_cast<int*>(base + ws_members_off(F8));   // [kRows], producer only
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pa_dev::wait_prior_grid();
@@ -219,7 +253,9 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         for (int s = 0; s < kWsStages; ++s) {
             pa_tc::mbar_init(&bars[kKvFull0 + s], 1);
             pa_tc::mbar_init(&bars[kKvEmpty0 + s], 1);
+            pa_tc::mbar_init(&bars[kKvConv0 + s], 4);        // one arrival per converter warp
         }
+        pa_tc::mbar_init(&bars[kQConv], 4);
         *abort_flag = 0;
         pa_tc::mbar_init_fence();
     }
@@ -286,8 +322,9 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                     if (phys[b] >= 0) loaded |= 1 << b;
                 }
                 // slots without keys keep what an earlier step left: their scores
-                // are masked, and zero values keep 0 * Inf out of P.V
-                if (loaded != (1 << (kStep / 16)) - 1) {
+                // are masked, and zero values keep 0 * Inf out of P.V (fp8: the
+                // converter warps write those zeros)
+                if (!F8 && loaded != (1 << (kStep / 16)) - 1) {
 #pragma unroll
                     for (int b = 0; b < kStep / 16; ++b)
                         if (!((loaded >> b) & 1))
@@ -300,14 +337,24 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                     stage_mask[st] = loaded;
                     const uint32_t kst = sbase + kWsStageOff + st * kStageBytes;
                     pa_tc::mbar_expect_tx(&bars[kKvFull0 + st],
-                                          static_cast<uint32_t>(__popc(loaded)) * (2 * 2048 + 4096));
+                                          static_cast<uint32_t>(__popc(loaded)) * (F8 ? 2 * 2048 : 2 * 2048 + 4096));
 #pragma unroll
                     for (int b = 0; b < kStep / 16; ++b) {
                         if (phys[b] < 0) continue;
-                        const int yk = (phys[b] * Hkv + it.h) * 16, yv = (phys[b] * Hkv + it.h) * kD;
-                        pa_tc::tma_load_2d(kst + b * 2048, &kmap, 0, yk, &bars[kKvFull0 + st]);
-                        pa_tc::tma_load_2d(kst + 8192 + b * 2048, &kmap, 64, yk, &bars[kKvFull0 + st]);
-                        pa_tc::tma_load_2d(kst + 16384 + b * 4096, &vmap, 0, yv, &bars[kKvFull0 + st]);
+                        if constexpr (F8) {
+                            // one block's codes for this KV head: K [16][128] then V^T [128][16]
+                            const uint32_t cst = sbase + kWsCodeOff + st * kWsCodeBytes;
+                            const size_t tile = (static_cast<size_t>(phys[b]) * Hkv + it.h) * 2048;
+                            pa_tc::bulk_load(cst + b * 2048, static_cast<const unsigned char*>(p.k) + tile, 2048,
+                                             &bars[kKvFull0 + st]);
+                            pa_tc::bulk_load(cst + 8192 + b * 2048, static_cast<const unsigned char*>(p.v) + tile,
+                                             2048, &bars[kKvFull0 + st]);
+                        } else {
+                            const int yk = (phys[b] * Hkv + it.h) * 16, yv = (phys[b] * Hkv + it.h) * kD;
+                            pa_tc::tma_load_2d(kst + b * 2048, &kmap, 0, yk, &bars[kKvFull0 + st]);
+                            pa_tc::tma_load_2d(kst + 8192 + b * 2048, &kmap, 64, yk, &bars[kKvFull0 + st]);
+                            pa_tc::tma_load_2d(kst + 16384 + b * 4096, &vmap, 0, yv, &bars[kKvFull0 + st]);
+                        }
                     }
                 }
                 __syncwarp();
@@ -323,10 +370,10 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         int kk = 0;
         for (int item = blockIdx.x; ok && item < p.n_shared_items; item += gridDim.x, ++kk) {
             const WsItem it = ws_item(p, item);
-            if (!ws_wait(&bars[kQFull], kk & 1, abort_flag)) { ok = false; break; }
+            if (!ws_wait(&bars[F8 ? kQConv : kQFull], kk & 1, abort_flag)) { ok = false; break; }
             for (int j = 0; j < it.nsteps; ++j, ++kv_it, ++s_it) {
                 const int st = kv_it % kWsStages, sb = s_it & 1;
-                if (!ws_wait(&bars[kKvFull0 + st], (kv_it / kWsStages) & 1, abort_flag) ||
+                if (!ws_wait(&bars[(F8 ? kKvConv0 : kKvFull0) + st], (kv_it / kWsStages) & 1, abort_flag) ||
                     ((s_it >> 1) > 0 && !ws_wait(&bars[kSEmpty0 + sb], ((s_it >> 1) - 1) & 1, abort_flag))) {
                     ok = false;
                     break;
@@ -338,7 +385,7 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                     for (int q = 0; q < kD / 16; ++q) {
                         const uint64_t a = pa_tc::sw128_desc(sbase + kQOff + (q >> 2) * 16384 + (q & 3) * 32);
                         const uint64_t b = pa_tc::sw128_desc(kst + (q >> 2) * 8192 + (q & 3) * 32);
-                        pa_tc::mma_bf16(tmem + sb * 64, a, b, kIdescQK, q > 0);
+                        pa_tc::mma_bf16(tmem + sb * 64, a, b, F8 ? kIdescQK16 : kIdescQK, q > 0);
                     }
                     pa_tc::commit(&bars[kSFull0 + sb]);
                     if (j == it.nsteps - 1) pa_tc::commit(&bars[kQEmpty]);   // Q tile free
@@ -363,7 +410,7 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             for (int j = 0; j < it.nsteps; ++j, ++kv_it, ++p_it) {
                 const int st = kv_it % kWsStages, pb = p_it & 1;
                 if (!ws_wait(&bars[kPFull0 + pb], (p_it >> 1) & 1, abort_flag) ||
-                    !ws_wait(&bars[kKvFull0 + st], (kv_it / kWsStages) & 1, abort_flag)) {
+                    !ws_wait(&bars[(F8 ? kKvConv0 : kKvFull0) + st], (kv_it / kWsStages) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -374,8 +421,8 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
                     for (int q = 0; q < kStep / 16; ++q) {
                         const uint64_t b = pa_tc::sw32_desc(kst + 16384 + q * 4096);   // block q's V^T
-                        pa_tc::mma_bf16_ta(od, ph + q * 8, b, kIdescPV, !(j == 0 && q == 0));
-                        pa_tc::mma_bf16_ta(od, pl + q * 8, b, kIdescPV, true);
+                        pa_tc::mma_bf16_ta(od, ph + q * 8, b, F8 ? kIdescPV16 : kIdescPV, !(j == 0 && q == 0));
+                        pa_tc::mma_bf16_ta(od, pl + q * 8, b, F8 ? kIdescPV16 : kIdescPV, true);
                     }
                     pa_tc::commit(&bars[kKvEmpty0 + st]);    // the stage may be refilled
                     pa_tc::commit(&bars[kPEmpty0 + pb]);     // P buffer free, O settled up to here
@@ -387,6 +434,58 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         if (lane == 0) pa_tc::commit(&bars[kMmaDone]);
         __syncwarp();
         pa_tc::mbar_wait(&bars[kMmaDone], 0, kWaitLimit);
+    } else if (F8 && warp >= 7) {
+        // ----------------------------------------------- fp8: converters
+        // thread ct of 128: the item's Q tile re-rounded to f16 in place, then
+        // every step's codes widened into the stage's f16 layouts
+        const int ct = tid - 7 * 32;
+        uint32_t kv_it = 0;
+        int kk = 0;
+        for (int item = blockIdx.x; ok && item < p.n_shared_items; item += gridDim.x, ++kk) {
+            const WsItem it = ws_item(p, item);
+            if (!ws_wait(&bars[kQFull], kk & 1, abort_flag)) { ok = false; break; }
+            for (int i = ct; i < kRows * 16; i += 128) {            // 16-byte chunks of the Q tile
+                uint4* q16 = reinterpret_cast<uint4*>(base + kQOff + i * 16);
+                *q16 = bf16x8_to_f16x8(*q16);
+            }
+            pa_tc::fence_smem_to_async();                           // generic writes -> tensor core reads
+            __syncwarp();
+            if (lane == 0) ws_arrive(&bars[kQConv]);
+            for (int j = 0; j < it.nsteps; ++j, ++kv_it) {
+                const int st = kv_it % kWsStages;
+                if (!ws_wait(&bars[kKvFull0 + st], (kv_it / kWsStages) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int loaded = stage_mask[st];
+                const unsigned char* codes = base + kWsCodeOff + st * kWsCodeBytes;
+                unsigned char* stage = base + kWsStageOff + st * kStageBytes;
+                // K: key row `key` of the step (block key / 16), 8-value chunk c of
+                // its 128 values, into half c / 8 (values 0-63 / 64-127) of the
+                // 128-byte-swizzled tile, at 16-byte chunk c % 8 of the row
+                for (int gi = ct; gi < kStep * 16; gi += 128) {
+                    const int key = gi >> 4, c = gi & 15, b = key >> 4;
+                    uint4 y = make_uint4(0u, 0u, 0u, 0u);
+                    if ((loaded >> b) & 1)
+                        y = e4m3x8_to_f16x8(
+                            *reinterpret_cast<const uint2*>(codes + b * 2048 + (key & 15) * 128 + c * 8));
+                    *reinterpret_cast<uint4*>(stage + (c >> 3) * 8192 + pa_tc::sw128_off(key, c & 7)) = y;
+                }
+                // V^T: block b, value row d, tokens 8k..8k+7, into the 32-byte-swizzled
+                // tile (row d at d * 32, its two halves swapped when bit 2 of d is set);
+                // blocks without keys get zeros (0 * Inf stays out of P.V)
+                for (int gi = ct; gi < (kStep / 16) * kD * 2; gi += 128) {
+                    const int b = gi >> 8, d = (gi >> 1) & (kD - 1), k = gi & 1;
+                    uint4 y = make_uint4(0u, 0u, 0u, 0u);
+                    if ((loaded >> b) & 1)
+                        y = e4m3x8_to_f16x8(*reinterpret_cast<const uint2*>(codes + 8192 + b * 2048 + d * 16 + k * 8));
+                    *reinterpret_cast<uint4*>(stage + 16384 + b * 4096 + d * 32 + ((k ^ ((d >> 2) & 1)) << 4)) = y;
+                }
+                pa_tc::fence_smem_to_async();
+                __syncwarp();
+                if (lane == 0) ws_arrive(&bars[kKvConv0 + st]);
+            }
+        }
     } else {
         // ------------------------------------------------------- softmax
         const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;   // this warp's TMEM lanes
@@ -413,9 +512,11 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                 pa_tc::tmem_ld32(od + cc * 32, o);
                 pa_tc::tmem_wait_ld();
                 if (pend.row_ok) {
+                    const float vs = F8 ? p.v_scale : 1.f;            // fp8: the sums of codes * v_scale
 #pragma unroll
                     for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(acc + cc * 32 + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+                        *reinterpret_cast<float4*>(acc + cc * 32 + i) =
+                            make_float4(o[i] * vs, o[i + 1] * vs, o[i + 2] * vs, o[i + 3] * vs);
                 }
             }
             if (pend.row_ok) {
@@ -514,8 +615,13 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                         const float p0 = exp2_approx(fmaf(x[2 * e], xs, nref));
                         const float p1 = exp2_approx(fmaf(x[2 * e + 1], xs, nref));
                         sum += p0 + p1;
-                        hi[e] = pa_dev::pack_bf16(p0, p1);
-                        lo[e] = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(hi[e]), p1 - pa_dev::bf16_hi(hi[e]));
+                        if constexpr (F8) {
+                            hi[e] = pa_dev::pack_f16(p0, p1);
+                            lo[e] = pa_dev::pack_f16(p0 - pa_dev::f16_lo(hi[e]), p1 - pa_dev::f16_hi(hi[e]));
+                        } else {
+                            hi[e] = pa_dev::pack_bf16(p0, p1);
+                            lo[e] = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(hi[e]), p1 - pa_dev::bf16_hi(hi[e]));
+                        }
                     }
                     pa_tc::tmem_st16u(ph + col, hi);
                     pa_tc::tmem_st16u(pl + col, lo);
@@ -872,10 +978,14 @@ int launch_prefill_tc(pa_pool* pool, const PrefillParams& p, dim3 grid, cudaStre
 }
 
 bool shared_tc_eligible(const pa_pool* pool, int G) {
-    // TMA coordinates are 32-bit: value rows num_blocks * Hkv * D must stay below 2^31
-    return pool->dtype == PA_BF16 && pool->head_dim == kD && G >= 1 && G <= 8 &&
+    // bf16: TMA coordinates are 32-bit, so value rows num_blocks * Hkv * D stay
+    // below 2^31; fp8: bulk copies of codes, and a CTA that needs nearly all of
+    // the opt-in shared memory
+    const bool f8 = pool->dtype == PA_FP8E4M3;
+    return (pool->dtype == PA_BF16 || f8) && pool->head_dim == kD && G >= 1 && G <= 8 &&
            pool->block_size == 16 &&
-           static_cast<long long>(pool->num_blocks) * pool->kv_heads * kD < (1LL << 31);
+           (f8 ? static_cast<uint32_t>(pool->smem_optin) >= ws_smem_bytes(true)
+               : static_cast<long long>(pool->num_blocks) * pool->kv_heads * kD < (1LL << 31));
 }
 
 // TMA descriptors over the pool (16-token blocks): K as
@@ -918,14 +1028,19 @@ int shared_tc_chunk_tokens() { return kChunkBlocks * 16; }
 
 int launch_shared_tc(pa_pool* pool, const DecodeParams& p, cudaStream_t st) {
     if (p.n_shared_items <= 0) return PA_OK;
-    const int rc = ensure_tensor_maps(pool);
-    if (rc != PA_OK) return rc;
-    if (cudaFuncSetAttribute(shared_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kWsSmemBytes)) != cudaSuccess)
+    const bool f8 = pool->dtype == PA_FP8E4M3;
+    if (!f8) {
+        const int rc = ensure_tensor_maps(pool);
+        if (rc != PA_OK) return rc;
+    }
+    auto kernel = f8 ? shared_tc_kernel<true> : shared_tc_kernel<false>;
+    const uint32_t smem = ws_smem_bytes(f8);
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
         return PA_ERR_CUDA;
     // one CTA per SM: the split pass of the private suffixes fills the rest of each SM
     const int grid = p.n_shared_items < pool->num_sms ? p.n_shared_items : pool->num_sms;
-    const cudaError_t e = launch_pdl(shared_tc_kernel, dim3(grid), dim3(kWsThreads), kWsSmemBytes,
+    const cudaError_t e = launch_pdl(kernel, dim3(grid), dim3(f8 ? kWsThreadsF8 : kWsThreads), smem,
                                      st, p, pool->kmap, pool->vmap);
     count_launch();
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -243,14 +243,20 @@ def test_full_size_parity():
     print(f"decode fp8 full size: max-abs over {len(seqs)} sequences {err:.3g} (tol {FP8_TOL})")
 
 
-def test_prefix_full_size_shared_parity():
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync"])
+def test_prefix_full_size_shared_parity(kernel):
     """The prefix workload (256 forks of a 4104-token prompt) on an fp8 pool
-    through pa_decode_shared: the shared span read once per tile of members on
-    the mma.sync form (codes widened to f16), codes bit-exact, attention on
-    sampled sequences."""
+    through pa_decode_shared: the shared span read once per tile of members,
+    on the tcgen05 kernel (codes widened to f16 in shared memory by converter
+    warps) and on the mma.sync form (codes widened at fragment load); codes
+    bit-exact, attention on sampled sequences."""
     wl = wls.make_workload("prefix", dtype="fp8")
     values = wls.generate_values(wl, "cuda")
-    pool, bm, setup_pairs, step = run_library(wl, values, shared=True)
+    pool, bm, setup_pairs = runtime.replay_setup(wl, values, "cuda")
+    pool.set_option("shared_kernel", 1 if kernel == "mma_sync" else 0)
+    step = runtime.prepare_step(wl, values, pool, bm, shared=True)
+    step.run()
+    torch.cuda.synchronize()
     assert step.sharing()
     assert pool.get_error() == 0
     st = orp.replay(wl, values)

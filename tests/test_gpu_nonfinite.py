@@ -102,16 +102,18 @@ def test_decode_ignores_stale_nonfinite(name, kw):
 
 
 @pytest.mark.parametrize("prefix_len", [41, 16 * 21 + 3, 16 * 64 + 5])
-@pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync", "fp8"])
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync", "fp8_tcgen05", "fp8_mma_sync"])
 def test_shared_prefix_ignores_stale_nonfinite(prefix_len, kernel):
     """pa_decode_shared: shared spans of 2, 21 and 64 full blocks (steps of 64
     tokens that leave 2, 3 and 0 block slots unloaded at the span's end), on
-    both bf16 forms and on an fp8 pool (its NaN codes planted)."""
+    both kernel forms, for bf16 pools and for fp8 pools (their NaN codes
+    planted)."""
+    fp8 = kernel.startswith("fp8")
     wl = wls.make_workload("prefix", num_seqs=6, prefix_len=prefix_len, suffix_min=1,
-                           suffix_max=40, **D128, **({"dtype": "fp8"} if kernel == "fp8" else {}))
+                           suffix_max=40, **D128, **({"dtype": "fp8"} if fp8 else {}))
     values = wls.generate_values(wl, "cuda")
     pool, bm, _ = runtime.replay_setup(wl, values, "cuda")
-    pool.set_option("shared_kernel", 1 if kernel == "mma_sync" else 0)
+    pool.set_option("shared_kernel", 1 if kernel.endswith("mma_sync") else 0)
     step = runtime.prepare_step(wl, values, pool, bm, shared=True)
     assert step.sharing()
     step.run()
