@@ -247,11 +247,13 @@ int pa_decode_reserve(pa_pool *pool, int max_seqs, int max_q_heads);
  *                       member's table and lie wholly inside every member's context
  * For each group and KV head, tiles of up to 128 query rows (members x their
  * G heads) attend to 1024-token chunks of the shared span together on the
- * 5th-generation tensor cores (tcgen05: operands staged by TMA, accumulators
- * in tensor memory; bf16 pools with head_dim 128, block_size 16, G <= 8; other
- * tensor-core shapes use 64-row tiles on mma.sync, which the pool's
- * PA_OPT_SHARED_KERNEL option also selects); each member's private suffix goes through
- * the ordinary split path, and the partials are merged by log-sum-exp.  Groups with fewer than two members
+ * 5th-generation tensor cores (tcgen05: operands staged in shared memory,
+ * accumulators in tensor memory; head_dim 128, block_size 16, G <= 8, bf16
+ * pools or fp8 pools, whose codes are widened to f16 in shared memory and
+ * whose queries are re-rounded to f16; other tensor-core shapes use 64-row
+ * tiles on mma.sync, which the pool's PA_OPT_SHARED_KERNEL option also
+ * selects); each member's private suffix goes through the ordinary split
+ * path, and the partials are merged by log-sum-exp.  Groups with fewer than two members
  * or no shared block are ignored; shapes outside the bf16 tensor-core path
  * (see pa_decode) fall back to pa_decode.  The device checks that members'
  * leading entries agree and that their contexts cover the shared span, and
