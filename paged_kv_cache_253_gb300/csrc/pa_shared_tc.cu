@@ -672,6 +672,15 @@ shared_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
 // applied to the scores (a row at position p keeps keys 0 .. p), and each row's
 // normalised output is written directly.  Block ids come from the sequence's
 // table as each step is staged.
+// F8 (fp8 pool): a step's e4m3 codes (K [16][128] and V^T [128][16] per
+// block, 2 KB each) are copied by bulk copy into the V^T half of the stage;
+// once they land every thread reads its 16 groups of 8 codes into registers
+// and, after a block-wide barrier, writes them widened to f16 (exact) into the
+// stage's K and V^T layouts; the Q tile is re-rounded to f16 in place (each
+// thread the chunks it copied), the MMAs are f16, P is an f16 pair, k_scale
+// sits in the score factor and v_scale in the rows' normaliser.  kmap / vmap
+// are unused then.
+template <bool F8>
 __global__ void __launch_bounds__(kThreads, 2)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap) {
@@ -767,7 +776,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
                 if (x < 0 || x >= p.num_blocks) pa_dev::record_error(p.err, PA_ERR_BAD_BLOCK_ID);
                 else phys[b] = x;
             }
-            if (phys[b] >= 0) bytes += 2 * 2048 + 4096;
+            if (phys[b] >= 0) bytes += F8 ? 2 * 2048 : 2 * 2048 + 4096;
             else skip |= 1 << b;
         }
         s_skip[st] = skip;
@@ -775,10 +784,19 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
 #pragma unroll
         for (int b = 0; b < kStep / 16; ++b) {
             if (phys[b] < 0) continue;
-            const int yk = (phys[b] * Hkv + h) * 16, yv = (phys[b] * Hkv + h) * kD;
-            pa_tc::tma_load_2d(kst + b * 2048, &kmap, 0, yk, bar_full + st);
-            pa_tc::tma_load_2d(kst + 8192 + b * 2048, &kmap, 64, yk, bar_full + st);
-            pa_tc::tma_load_2d(kst + 16384 + b * 4096, &vmap, 0, yv, bar_full + st);
+            if constexpr (F8) {
+                // codes: K at 16 KB + 2 KB b, V^T at 24 KB + 2 KB b of the stage
+                const size_t tile = (static_cast<size_t>(phys[b]) * Hkv + h) * 2048;
+                pa_tc::bulk_load(kst + 16384 + b * 2048, static_cast<const unsigned char*>(p.k) + tile, 2048,
+                                 bar_full + st);
+                pa_tc::bulk_load(kst + 24576 + b * 2048, static_cast<const unsigned char*>(p.v) + tile, 2048,
+                                 bar_full + st);
+            } else {
+                const int yk = (phys[b] * Hkv + h) * 16, yv = (phys[b] * Hkv + h) * kD;
+                pa_tc::tma_load_2d(kst + b * 2048, &kmap, 0, yk, bar_full + st);
+                pa_tc::tma_load_2d(kst + 8192 + b * 2048, &kmap, 64, yk, bar_full + st);
+                pa_tc::tma_load_2d(kst + 16384 + b * 4096, &vmap, 0, yv, bar_full + st);
+            }
         }
     };
 
@@ -790,11 +808,47 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
         // behind the previous step's P.V in the tensor pipe: it writes only the
         // S columns (read out before that P.V was issued) and reads this
         // step's stage, so it need not wait for that P.V to finish
-        if (j == 0) pa_tc::cp_wait<0>();
+        if (j == 0) {
+            pa_tc::cp_wait<0>();
+            if constexpr (F8) {
+                // this thread's own Q chunks (those it copied), bf16 -> f16 in place
+                for (int idx = tid; idx < kRows * 16; idx += kThreads) {
+                    const int rr = idx >> 4, c16 = idx & 15;
+                    uint4* q16 = reinterpret_cast<uint4*>(base + kQOff + (c16 >> 3) * 16384 +
+                                                          pa_tc::sw128_off(rr, c16 & 7));
+                    *q16 = bf16x8_to_f16x8(*q16);
+                }
+            }
+        }
         {
             const bool w = pa_tc::mbar_wait(bar_full + st, st ? ph_full1 : ph_full0, kWaitLimit);
             if (st) ph_full1 ^= 1u; else ph_full0 ^= 1u;
             if (!__syncthreads_and(w)) { ok = false; break; }
+        }
+        if constexpr (F8) {
+            // the step's codes into registers (8 K groups, 8 V^T groups of 8 codes),
+            // then, once every thread has read its own, widened into the stage
+            unsigned char* stg = base + kStageOff + st * kStageBytes;
+            uint2 kc[8], vc[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int gi = tid + kThreads * k;
+                const int key = gi >> 4, c = gi & 15, b = key >> 4;
+                kc[k] = *reinterpret_cast<const uint2*>(stg + 16384 + b * 2048 + (key & 15) * 128 + c * 8);
+                const int vb = gi >> 8, d = (gi >> 1) & (kD - 1), kh = gi & 1;
+                vc[k] = *reinterpret_cast<const uint2*>(stg + 24576 + vb * 2048 + d * 16 + kh * 8);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int gi = tid + kThreads * k;
+                const int key = gi >> 4, c = gi & 15;
+                *reinterpret_cast<uint4*>(stg + (c >> 3) * 8192 + pa_tc::sw128_off(key, c & 7)) = e4m3x8_to_f16x8(kc[k]);
+                const int vb = gi >> 8, d = (gi >> 1) & (kD - 1), kh = gi & 1;
+                *reinterpret_cast<uint4*>(stg + 16384 + vb * 4096 + d * 32 + ((kh ^ ((d >> 2) & 1)) << 4)) =
+                    e4m3x8_to_f16x8(vc[k]);
+            }
+            __syncthreads();                               // before the tails are zeroed row by row
         }
         // Keys that no row of the tile may weigh: block slots this step did not
         // load (past the tile's last key, or a block id outside the pool),
@@ -823,7 +877,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
             for (int kk = 0; kk < kD / 16; ++kk) {
                 const uint64_t a = pa_tc::sw128_desc(sbase + kQOff + (kk >> 2) * 16384 + (kk & 3) * 32);
                 const uint64_t b = pa_tc::sw128_desc(kst + (kk >> 2) * 8192 + (kk & 3) * 32);
-                pa_tc::mma_bf16(tS, a, b, kIdescQK, kk > 0);
+                pa_tc::mma_bf16(tS, a, b, F8 ? kIdescQK16 : kIdescQK, kk > 0);
             }
             pa_tc::commit(bar_s);
         }
@@ -891,8 +945,13 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
                 const float p0 = exp2_approx(sc[2 * e] - ref);
                 const float p1 = exp2_approx(sc[2 * e + 1] - ref);
                 sum += p0 + p1;
-                hi[e] = pa_dev::pack_bf16(p0, p1);
-                lo[e] = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(hi[e]), p1 - pa_dev::bf16_hi(hi[e]));
+                if constexpr (F8) {
+                    hi[e] = pa_dev::pack_f16(p0, p1);
+                    lo[e] = pa_dev::pack_f16(p0 - pa_dev::f16_lo(hi[e]), p1 - pa_dev::f16_hi(hi[e]));
+                } else {
+                    hi[e] = pa_dev::pack_bf16(p0, p1);
+                    lo[e] = pa_dev::pack_bf16(p0 - pa_dev::bf16_lo(hi[e]), p1 - pa_dev::bf16_hi(hi[e]));
+                }
             }
             pa_tc::tmem_st32u(tPh + lane_sel, hi);
             pa_tc::tmem_st32u(tPl + lane_sel, lo);
@@ -906,8 +965,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
 #pragma unroll
             for (int kk = 0; kk < kStep / 16; ++kk) {
                 const uint64_t b = pa_tc::sw32_desc(kst + 16384 + kk * 4096);
-                pa_tc::mma_bf16_ta(tO, tPh + kk * 8, b, kIdescPV, j > 0 || kk > 0);
-                pa_tc::mma_bf16_ta(tO, tPl + kk * 8, b, kIdescPV, true);
+                pa_tc::mma_bf16_ta(tO, tPh + kk * 8, b, F8 ? kIdescPV16 : kIdescPV, j > 0 || kk > 0);
+                pa_tc::mma_bf16_ta(tO, tPl + kk * 8, b, F8 ? kIdescPV16 : kIdescPV, true);
             }
             pa_tc::commit(bar_pv);
         }
@@ -919,7 +978,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
     }
     if (ok) {
         pa_tc::fence_after_sync();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? (F8 ? p.v_scale : 1.f) / l : 0.f;
         const size_t orow = row_ok ? (static_cast<size_t>(q0 + qi) * p.Hq +
                                       static_cast<size_t>(h) * G + r % G) * kD : 0;
 #pragma unroll
@@ -959,19 +1018,25 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
 namespace pa_detail {
 
 bool prefill_tc_eligible(const pa_pool* pool) {
-    return pool->dtype == PA_BF16 && pool->head_dim == kD && pool->block_size == 16 &&
-           static_cast<long long>(pool->num_blocks) * pool->kv_heads * kD < (1LL << 31);
+    // bf16: 32-bit TMA coordinates (value rows num_blocks * Hkv * D); fp8: bulk copies of codes
+    return (pool->dtype == PA_BF16 || pool->dtype == PA_FP8E4M3) && pool->head_dim == kD &&
+           pool->block_size == 16 &&
+           (pool->dtype == PA_FP8E4M3 || static_cast<long long>(pool->num_blocks) * pool->kv_heads * kD < (1LL << 31));
 }
 
 int prefill_tc_rows() { return kRows; }
 
 int launch_prefill_tc(pa_pool* pool, const PrefillParams& p, dim3 grid, cudaStream_t st) {
-    const int rc = ensure_tensor_maps(pool);
-    if (rc != PA_OK) return rc;
-    if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool f8 = pool->dtype == PA_FP8E4M3;
+    if (!f8) {
+        const int rc = ensure_tensor_maps(pool);
+        if (rc != PA_OK) return rc;
+    }
+    auto kernel = f8 ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess)
         return PA_ERR_CUDA;
-    const cudaError_t e = launch_pdl(prefill_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, p,
+    const cudaError_t e = launch_pdl(kernel, grid, dim3(kThreads), kSmemBytes, st, p,
                                      pool->kmap, pool->vmap);
     count_launch();
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -190,8 +190,9 @@ PREFILL = [
 ]
 
 
-def _check_prefill(wl, values, seqs=None, threads=1):
+def _check_prefill(wl, values, seqs=None, threads=1, kernel="tcgen05"):
     pool, bm, setup_pairs = runtime.replay_setup(wl, values, "cuda")
+    pool.set_option("prefill_kernel", 1 if kernel == "mma_sync" else 0)
     step = runtime.prepare_prefill(wl, values, pool, bm)
     step.run()
     torch.cuda.synchronize()
@@ -211,25 +212,28 @@ def _check_prefill(wl, values, seqs=None, threads=1):
     return err
 
 
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync"])
 @pytest.mark.parametrize("kw", PREFILL, ids=[f"case{i}" for i in range(len(PREFILL))])
-def test_prefill_parity(kw):
+def test_prefill_parity(kw, kernel):
     """Chunked prefill over an fp8 pool: the chunk's codes (quantizing append)
     bit-exact, every query row within FP8_TOL of float64 attention over the
-    codes' values."""
+    codes' values; the tcgen05 kernel (codes widened to f16 in shared memory,
+    head_dim 128) and the mma.sync form (the other shapes run it either way)."""
     wl = wls.make_workload("prefill", **kw)
     values = wls.generate_values(wl, "cuda")
-    err = _check_prefill(wl, values)
-    print(f"prefill fp8 {kw}: max-abs {err:.3g}")
+    err = _check_prefill(wl, values, kernel=kernel)
+    print(f"prefill fp8 {kw} {kernel}: max-abs {err:.3g}")
 
 
-def test_prefill_full_size_parity():
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync"])
+def test_prefill_full_size_parity(kernel):
     """The prefill workload (16 sequences, cached prefixes up to 4096, chunks of
     128..512) on an fp8 pool: codes bit-exact, attention on sampled sequences."""
     wl = wls.make_workload("prefill", dtype="fp8")
     values = wls.generate_values(wl, "cuda")
     seqs = [0, 7, wl.num_seqs - 1]
-    err = _check_prefill(wl, values, seqs=seqs, threads=16)
-    print(f"prefill fp8 full size: max-abs over sequences {seqs}: {err:.3g}")
+    err = _check_prefill(wl, values, seqs=seqs, threads=16, kernel=kernel)
+    print(f"prefill fp8 full size ({kernel}): max-abs over sequences {seqs}: {err:.3g}")
 
 
 def test_full_size_parity():
