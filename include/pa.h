@@ -322,12 +322,14 @@ int pa_decode_noalloc(pa_pool *pool, const void *q, int num_seqs, int num_q_head
  * and head_dim 64/128/256 (else PA_ERR_UNSUPPORTED).  An fp8 pool's codes are
  * widened exactly to f16 and the bf16 queries re-rounded to f16 (exact for
  * magnitudes 2^-17 .. 65504); products are summed in fp32, k_scale is applied
- * to the scores and v_scale to the outputs (mma.sync kernel).  One kernel launch: one CTA per
- * (query rows, KV head, sequence) streams the keys up to its last row's
- * position through shared memory once for all its rows: 128 rows on the
- * tcgen05 tensor cores (TMA-staged keys/values, TMEM accumulators) for 16-token
- * blocks, head_dim 128 and a 16-byte-aligned out; 64 rows on mma.sync otherwise
- * (or when the pool's PA_OPT_PREFILL_KERNEL option selects it).  Whatever
+ * to the scores and v_scale to the outputs (both kernels).  One kernel launch:
+ * one CTA per (query rows, KV head, sequence) streams the keys up to its last
+ * row's position through shared memory once for all its rows: 128 rows on the
+ * tcgen05 tensor cores (keys/values staged by TMA for bf16 pools, an fp8
+ * pool's codes by bulk copy and widened in shared memory; TMEM accumulators)
+ * for 16-token blocks, head_dim 128 and a 16-byte-aligned out; 64 rows on
+ * mma.sync otherwise (or when the pool's PA_OPT_PREFILL_KERNEL option selects
+ * it).  Whatever
  * bits a block holds at positions at or past the sequence's length (a block
  * recycled from a finished request may hold anything, Inf and NaN included)
  * never reach the output.  A non-finite key or value inside the chunk itself
