@@ -130,6 +130,8 @@ TRAFFIC_PROFILES = {
     ("mixed", "bf16"): "decode_kernel_mixed.md",
     ("prefix", "bf16"): "decode_call_prefix.md",
     ("prefill", "bf16"): "prefill_tc_prefill_batch.md",
+    ("prefill", "fp8"): "prefill_tc_prefill_batch_fp8.md",
+    ("prefix", "fp8"): "decode_call_prefix_fp8.md",
 }
 
 
