@@ -9,13 +9,15 @@
 //
 // How (designed for sm_103a; the pages give no kernel):
 //   * Work item = (sequence, KV head, partition of PT tokens).  PT is chosen
-//     on the device from the batch's total length so that the items number a
-//     few per CTA; long contexts are split over block ranges and merged by
-//     log-sum-exp.  The grid is persistent (a few CTAs per SM); every CTA
-//     builds the same item list from context_lens in shared memory.
+//     on the device from the batch's total length so that the items number
+//     about twelve per SM; long contexts are split over block ranges and
+//     merged by log-sum-exp.  The grid is persistent (a few CTAs per SM);
+//     every CTA builds the same item list from context_lens in shared memory
+//     and takes items by a global ticket.
 //   * Each item is served by the CTA's 4 warps, which take the partition's
-//     blocks round-robin and keep their own online-softmax state; the warps
-//     are merged in shared memory at the end of the item.
+//     blocks round-robin and keep their own online-softmax state; at the end
+//     of the item each head's warp weights are computed once and every thread
+//     writes its merged columns out.
 //   * bf16 pools: a 16-token block tile of one KV head is one tensor-core
 //     M tile.  Scores S^T[16 tokens x 8 heads] = K[16 x D] . Q^T[D x 8] and
 //     O^T[D x 8] += V^T[D x 16] . P^T[16 x 8] with mma.sync m16n8k16 (bf16 in,
@@ -26,12 +28,18 @@
 //     P^T reaches the B-operand layout through movmatrix; P is split into a
 //     bf16 high part and a bf16 low part so the value product keeps ~16 bits
 //     of the fp32 probabilities.
-//   * f32 pools (and bf16 shapes outside the tensor-core tile) use a plain
-//     fp32 CUDA-core item: scores to shared memory, softmax, value mix.
+//   * fp8 (e4m3) pools: the same tiles with half the bytes; each thread's
+//     codes are widened to f16 pairs (exact) just before the MMA that reads
+//     them, queries are re-rounded to f16 and P is an f16 pair.  With G <= 4
+//     the score columns 4..7 repeat heads 0..3 and carry P's remainders, so
+//     one value MMA per m-tile takes both parts.  The walk fits 128 registers,
+//     four CTAs per SM.
+//   * f32 pools (and shapes outside the tensor-core tile) use a plain fp32
+//     CUDA-core item: scores to shared memory, softmax, value mix.
 //   * An item whose sequence has one partition writes the normalised output.
-//     Otherwise it writes (acc, max, sum) to the workspace; the CTA that
-//     completes a (sequence, head)'s last partition (arrival counter, no
-//     waiting) merges them and resets the counter.
+//     Otherwise it writes (acc, max, sum) to the workspace, and the merge
+//     kernel, launched behind the split pass with programmatic dependent
+//     launch, combines each (sequence, head)'s partials by log-sum-exp.
 #include <algorithm>
 #include <cfloat>
 #include <climits>
@@ -661,8 +669,8 @@ __device__ __forceinline__ void fast_item(const DecodeParams& p, int s, int h, i
     // registers, four CTAs (16 warps) per SM: more loads in flight per SM than
     // three CTAs with a one-tile lookahead (on GB300, with the merge below,
     // 48-50 against 52 us on the decode batch, 246-250 against 251 us on long
-    // context).  The shared-prefix kernel runs two CTAs per SM, whose register
-    // budget holds a second tile: it loads one tile ahead (AHEAD).
+    // context).  The mma.sync shared-prefix kernel runs two CTAs per SM, whose
+    // register budget holds a second tile: it loads one tile ahead (AHEAD).
     //
     // Fused append into an fp8 pool: the warp that owns the block holding
     // position L-1 quantizes the new token's bf16 key row and value column

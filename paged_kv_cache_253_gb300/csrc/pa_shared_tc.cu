@@ -7,24 +7,29 @@
 // form a real dense contraction: 128 query rows (members x their G heads) of
 // one KV head against the span's keys, read once per 128 rows.
 //
-// One CTA (4 warps, 128 threads) takes an item = (group, KV head, tile of
-// 128 / G members, chunk of 1024 shared tokens) and walks it in 64-token steps:
-//   S[128 x 64]   = Q[128 x 128] . K^T           tcgen05.mma, fp32 in TMEM cols [0,64)
+// The shared-prefix kernel takes an item = (group, KV head, tile of 128 / G
+// members, chunk of 1024 shared tokens) and walks it in 64-token steps:
+//   S[128 x 64]   = Q[128 x 128] . K^T           tcgen05.mma, fp32 in TMEM
 //   softmax       thread t owns query row t = TMEM lane t (tcgen05.ld), exp2 in
 //                 fp32 with a reference maximum that is raised only when a row's
 //                 maximum grows by more than 2^8 (then O is rescaled in TMEM)
-//   O[128 x 128] += P[128 x 64] . V[64 x 128]    tcgen05.mma, fp32 in TMEM cols [128,256),
-//                 P entering as a bf16 high part plus a bf16 low part
-// Q is staged with cp.async, K (64 tokens x 128 d) and V^T (128 d x 64 tokens)
-// by TMA, into swizzled K-major shared-memory tiles (two K/V stages); value
-// columns that get zero weight (block slots a step did not load) are zeroed
-// before the value product, so stale non-finite bits never reach it; P goes
-// from registers to TMEM (tcgen05.st) and feeds the value product from there, so
-// a CTA needs ~99 KB of shared memory and two fit on an SM; one thread
-// issues the MMAs and commits them to an mbarrier that the others wait on
-// (every wait bounded: on timeout the item records PA_ERR_CUDA and the CTA stops).
-// Each row's (acc, max, sum) goes to the same shared-partial slot the merge
-// kernel reads for the mma.sync variant.
+//   O[128 x 128] += P[128 x 64] . V[64 x 128]    tcgen05.mma, fp32 in TMEM,
+//                 P entering from TMEM as a high part plus a low part
+// with its warps specialised: a producer (Q by cp.async, K and V^T by TMA into
+// four swizzled K-major stages), a Q.K^T issuer, a P.V issuer and four softmax
+// warps, handing work to each other through mbarriers with S, P and O double
+// buffered in TMEM (one CTA per SM).  Each row's (acc, max, sum) goes to the
+// shared-partial slot the merge kernel reads.  fp8 pools: the producer copies
+// the codes and four more warps widen them to f16 (shared_tc_kernel<true>).
+//
+// The chunked-prefill kernel runs the same step on a (128 rows = 128 / G chunk
+// tokens x G heads, KV head, sequence) item with one warpgroup: one thread
+// issues the MMAs and commits them to mbarriers the others wait on, two K/V
+// stages, ~99 KB of shared memory so that two CTAs share an SM, causal masks.
+// Value columns that get zero weight (block slots a step did not load,
+// positions past a context) are zeroed before the value product, so stale
+// non-finite bits never reach it.  Every mbarrier wait is bounded: on timeout
+// the kernel records PA_ERR_CUDA and the CTA stops.
 #include <cstdint>
 
 #include <cuda.h>
