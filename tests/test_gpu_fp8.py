@@ -247,6 +247,43 @@ def test_full_size_parity():
     print(f"decode fp8 full size: max-abs over {len(seqs)} sequences {err:.3g} (tol {FP8_TOL})")
 
 
+SHARED = [
+    dict(num_seqs=6, prefix_len=300, suffix_min=1, suffix_max=40, **D128),               # G = 4
+    dict(num_seqs=70, prefix_len=1100, suffix_min=0, suffix_max=30, **D128),             # 2 chunks, 3 tiles
+    dict(num_seqs=9, prefix_len=700, suffix_min=5, suffix_max=60, num_q_heads=64, num_kv_heads=8,
+         head_dim=128, dtype="fp8"),                                                      # G = 8
+    dict(num_seqs=5, prefix_len=500, suffix_min=1, suffix_max=9, num_q_heads=10, num_kv_heads=2,
+         head_dim=128, dtype="fp8"),                                                      # G = 5
+    dict(num_seqs=7, prefix_len=333, suffix_min=1, suffix_max=20, num_q_heads=8, num_kv_heads=8,
+         head_dim=128, dtype="fp8"),                                                      # G = 1
+]
+
+
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync"])
+@pytest.mark.parametrize("kw", SHARED, ids=[f"case{i}" for i in range(len(SHARED))])
+def test_shared_prefix_parity(kw, kernel):
+    """pa_decode_shared on fp8 pools, on the tcgen05 kernel (codes widened to f16
+    in shared memory by converter warps) and on the mma.sync form: query heads
+    per KV head 1, 4, 5 and 8, a span over two 1024-token chunks, three tiles
+    of members; codes bit-exact, every output row within FP8_TOL of float64
+    attention over the codes' values."""
+    wl = wls.make_workload("prefix", **kw)
+    values = wls.generate_values(wl, "cuda")
+    pool, bm, setup_pairs = runtime.replay_setup(wl, values, "cuda")
+    pool.set_option("shared_kernel", 1 if kernel == "mma_sync" else 0)
+    step = runtime.prepare_step(wl, values, pool, bm, shared=True)
+    step.run()
+    torch.cuda.synchronize()
+    assert step.sharing()
+    assert pool.get_error() == 0
+    st = orp.replay(wl, values)
+    assert setup_pairs == st.setup_pairs
+    assert_pools_equal(pool, st)
+    ref = orp.attention(wl, values, st, threads=4)
+    err = np.abs(step.out.double().cpu().numpy() - ref).max()
+    assert err <= FP8_TOL, f"max-abs {err:.3g} > {FP8_TOL}"
+
+
 @pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync"])
 def test_prefix_full_size_shared_parity(kernel):
     """The prefix workload (256 forks of a 4104-token prompt) on an fp8 pool
