@@ -725,7 +725,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
     uint64_t* bar_full = bar_s + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kMiscOff + 32);
     volatile int* s_skip = reinterpret_cast<volatile int*>(base + kMiscOff + 48);   // [2] per stage
+    // a thread whose bounded wait gave up raises this; the CTA leaves the step
+    // loop together at the next block barrier
+    volatile int* s_abort = reinterpret_cast<volatile int*>(base + kMiscOff + 56);
     if (tid == 0) {
+        *s_abort = 0;
         pa_tc::mbar_init(bar_s, 1);
         pa_tc::mbar_init(bar_pv, 1);
         pa_tc::mbar_init(bar_full, 1);
@@ -740,6 +744,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
     const uint32_t tS = tmem, tO = tmem + 64, tPh = tmem + 192, tPl = tmem + 224;
     const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;
     uint32_t ph_s = 0, ph_pv = 0, ph_full0 = 0, ph_full1 = 0;
+    int pending = 0;                    // thread 0: stages with copies issued and not yet waited for
     bool ok = true;
 
     // this thread's row: TMEM lane tid
@@ -769,6 +774,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
     auto load_step = [&](int j) {
         if (tid != 0) return;
         const int st = j & 1;
+        pending |= 1 << st;
         const uint32_t kst = sbase + kStageOff + st * kStageBytes;
         int phys[kStep / 16], skip = 0;
         uint32_t bytes = 0;
@@ -826,9 +832,12 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
             }
         }
         {
+            // each thread waits for the stage itself (its codes, its V^T rows):
+            // no block barrier here
             const bool w = pa_tc::mbar_wait(bar_full + st, st ? ph_full1 : ph_full0, kWaitLimit);
             if (st) ph_full1 ^= 1u; else ph_full0 ^= 1u;
-            if (!__syncthreads_and(w)) { ok = false; break; }
+            if (w) pending &= ~(1 << st);
+            if (!w) *s_abort = 1;
         }
         if constexpr (F8) {
             // the step's codes into registers (8 K groups, 8 V^T groups of 8 codes),
@@ -874,7 +883,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
         }
         pa_tc::fence_smem_to_async();
         pa_tc::fence_before_sync();
-        __syncthreads();
+        if (__syncthreads_or(*s_abort)) { ok = false; break; }   // Q (every thread's copies) and the stage
         pa_tc::fence_after_sync();
         const uint32_t kst = sbase + kStageOff + st * kStageBytes;
         if (tid == 0) {
@@ -888,15 +897,17 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
         }
         // the previous P.V must be done before its stage is refilled, before P
         // is overwritten and before O is rescaled
+        // (every thread waits for itself: the stage refill, its P columns and
+        // its O row each need only their own view of these phases)
         if (j > 0) {
             const bool w = pa_tc::mbar_wait(bar_pv, ph_pv, kWaitLimit);
-            if (!__syncthreads_and(w)) { ok = false; break; }
+            if (!w) *s_abort = 1;
             ph_pv ^= 1u;
         }
-        if (j + 1 < nsteps) load_step(j + 1);
+        if (j + 1 < nsteps && !*s_abort) load_step(j + 1);
         {
             const bool w = pa_tc::mbar_wait(bar_s, ph_s, kWaitLimit);
-            if (!__syncthreads_and(w)) { ok = false; break; }
+            if (!w) *s_abort = 1;
         }
         ph_s ^= 1u;
         pa_tc::fence_after_sync();
@@ -964,7 +975,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
         }
         l += sum;
         pa_tc::fence_before_sync();
-        __syncthreads();
+        if (__syncthreads_or(*s_abort)) { ok = false; break; }   // every row's P is in TMEM
         pa_tc::fence_after_sync();
         if (tid == 0) {
 #pragma unroll
@@ -1010,7 +1021,13 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
             }
         }
     }
-    if (!ok && tid == 0) pa_dev::record_error(p.err, PA_ERR_CUDA);
+    if (!ok && tid == 0) {
+        pa_dev::record_error(p.err, PA_ERR_CUDA);
+        // copies still in flight land before the CTA's shared memory is released
+        // (bounded again)
+        if (pending & 1) pa_tc::mbar_wait(bar_full, ph_full0, kWaitLimit);
+        if (pending & 2) pa_tc::mbar_wait(bar_full + 1, ph_full1, kWaitLimit);
+    }
     pa_tc::cp_wait<0>();
     pa_tc::fence_before_sync();
     __syncthreads();
