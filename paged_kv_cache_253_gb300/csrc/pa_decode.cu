@@ -58,6 +58,8 @@ constexpr int kWarps = 4;               // warps per CTA sharing one item
 constexpr int kMinCtas = 3;             // resident CTAs per SM the register budget aims at (bf16)
 constexpr int kMinCtasF8 = 4;           // the same for the fp8 walk (one tile in flight per warp)
 constexpr int kPtMax = 2048;            // partition cap in tokens for batches of many sequences
+constexpr int kPtSoftF8 = 256;          // fp8 pools: smallest partition while items allow, tokens
+constexpr size_t kWaveBytes = 1u << 20;  // cache bytes per item that justify another wave of items
 constexpr int kBlockPrefetch = 1;       // L2 prefetch of the block a warp reads this many blocks ahead
 constexpr int kGuideMinPT = 256;        // shortest partition of the guided tail, tokens
 constexpr int kSharedStages = 8;        // staged 16-token tiles per CTA for shared-prefix items
@@ -133,8 +135,33 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
     if (p.pt_fixed > 0) {
         PT = PTs = p.pt_fixed;
     } else {
-        long long need = (total * p.Hkv + p.items_target - 1) / p.items_target;
+        // Item target: whole waves of wave_items (one item per resident CTA),
+        // as many as the token-heads fill at wave_tokens per item, at most
+        // items_target.  Small batches run in one wave: a second, partial wave
+        // of short items costs more in per-item work than it saves in balance
+        // (measured on GB300: 16 sequences 33.3 -> 29.1 us bf16, 28.9 -> 24.6
+        // us fp8; 2 long sequences fp8 80.8 -> 71.5 us); large ones keep
+        // items_target for balance (8 long sequences fp8: 229 us at three
+        // waves, 237 us at one).
+        long long target = p.items_target;
+        if (p.wave_items > 0 && p.wave_tokens > 0) {
+            const long long per_wave = static_cast<long long>(p.wave_items) * p.wave_tokens;
+            const long long waves = (total * p.Hkv + per_wave - 1) / per_wave;
+            target = min(target, max(1LL, waves) * p.wave_items);
+        }
+        long long need = (total * p.Hkv + target - 1) / target;
         need = (need + p.B - 1) / p.B * p.B;
+        // Smallest partition: pt_min, raised towards pt_soft tokens as far as
+        // that still leaves items_floor items.  fp8 pools use it: an item's
+        // fixed work (its queries, the warps' merge, its partial) weighs more
+        // against tiles of half the bytes, and at pt_soft the guided tail
+        // below is allowed again for batches of a few thousand tokens.
+        long long pmin = p.pt_min;
+        if (p.pt_soft > p.pt_min && p.items_floor > 0) {
+            const long long cap = total * p.Hkv / p.items_floor / p.B * p.B;
+            pmin = max(pmin, min(static_cast<long long>(p.pt_soft), cap));
+            if (p.pt_max > 0) pmin = min(pmin, static_cast<long long>(p.pt_max));
+        }
         // cap the partition so the launch's last items are short (long
         // sequences split into more items; the merge combines them), but never
         // below the length that keeps the item count within the workspace:
@@ -145,7 +172,7 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
             lo = (lo + p.B - 1) / p.B * p.B;
             need = min(need, max(static_cast<long long>(p.pt_max), lo));
         }
-        PT = static_cast<int>(max(need, static_cast<long long>(p.pt_min)));
+        PT = static_cast<int>(max(need, pmin));
         // Guided tail: sequences that start in the last quarter of the tokens
         // (they are the last items handed out) use partitions a quarter as long,
         // so the launch ends on short items.  Their tokens are at most a quarter
@@ -153,7 +180,7 @@ __device__ Sched build_schedule(const DecodeParams& p, int* s_start, long long* 
         // only when that fits the workspace, and only when the short partitions
         // still hold kGuideMinPT tokens (shorter items cost more to start than
         // they save at the end: measured on GB300).
-        PTs = max(p.pt_min, (PT / 4 + p.B - 1) / p.B * p.B);
+        PTs = max(static_cast<int>(pmin), (PT / 4 + p.B - 1) / p.B * p.B);
         const long long bound = static_cast<long long>(p.Hkv) *
             ((total + PT - 1) / PT + (total + 4LL * PTs - 1) / (4LL * PTs) + p.S);
         if (PTs < PT && PTs >= kGuideMinPT && bound <= p.max_items) split_at = total - total / 4;
@@ -1518,6 +1545,14 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
         // the mma.sync shared-prefix kernel (two CTAs per SM) keeps four items per
         // CTA (faster on the fp8 prefix batch than twelve per SM, measured on GB300)
         plan->items_target = plan->shared && !plan->tc ? plan->grid * 4 : pool->num_sms * kItemsPerSm;
+        if (fp8 && !(plan->shared && !plan->tc)) {
+            // fp8 pools: partitions of at least kPtSoftF8 tokens while that
+            // leaves two items per SM, so that the guided tail's short
+            // partitions reach kGuideMinPT in a one-wave batch (measured on
+            // GB300, 64 sequences of 128-2048 tokens: 45.2 -> 41.4 us)
+            plan->pt_soft = std::max(plan->pt_min, kPtSoftF8 / B * B);
+            plan->items_floor = pool->num_sms * 2;
+        }
         // items <= Hkv * (total / PT + S); PT >= total * Hkv / items_target keeps
         // that below min_items.  The extra items_target of room lets the
         // partition cap and the guided tail take effect; the kernel never
@@ -1532,12 +1567,22 @@ int plan_decode(pa_pool* pool, int S, int Hq, int max_blocks, DecodePlan* plan) 
     }
     if (static_cast<size_t>(plan->grid) > plan->max_items)
         plan->grid = static_cast<int>(plan->max_items);
+    if (fast && !(plan->shared && !plan->tc)) {
+        // whole waves of one item per resident CTA, one wave per
+        // kWaveBytes of cache each CTA reads
+        plan->wave_items = plan->grid;
+        plan->wave_tokens = static_cast<int>(kWaveBytes / (2 * static_cast<size_t>(D) * (fp8 ? 1 : 2)));
+    }
     return PA_OK;
 }
 
 int launch_decode(const DecodePlan& plan, const DecodeParams& prm, cudaStream_t st) {
     DecodeParams p = prm;
     p.items_target = plan.items_target;
+    p.pt_soft = plan.pt_soft;
+    p.items_floor = plan.items_floor;
+    p.wave_items = plan.wave_items;
+    p.wave_tokens = plan.wave_tokens;
     p.pt_min = plan.pt_min;
     p.pt_max = plan.pt_max;
     p.max_items = static_cast<int>(std::min<size_t>(plan.max_items, 1u << 30));

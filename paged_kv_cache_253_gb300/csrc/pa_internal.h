@@ -59,6 +59,12 @@ struct DecodeParams {
     int out_bf16;
     int items_target;           // wanted number of work items (fast path)
     int pt_min;                 // smallest partition, tokens (multiple of B)
+    int pt_soft;                // > pt_min: the smallest partition grows towards this many
+                                // tokens (multiple of B) while at least items_floor items remain
+    int items_floor;            // (both zero: pt_min alone)
+    int wave_items;             // > 0: the item target is whole waves of this many items,
+    int wave_tokens;            // one wave per wave_tokens token-heads per item, at most
+                                // items_target
     int pt_max;                 // largest partition, tokens (multiple of B; 0: no cap)
     int max_items;              // partial slots the workspace holds (fast path)
     int pt_fixed;               // > 0: use exactly this partition size
@@ -164,6 +170,8 @@ struct DecodePlan {
     int grid, threads;
     size_t smem;
     int items_target, pt_min, pt_max = 0, pt_fixed;
+    int pt_soft = 0, items_floor = 0;
+    int wave_items = 0, wave_tokens = 0;
     size_t max_items;
     size_t min_items;           // fewest partial slots the kernel can work with (fast path)
 };
