@@ -9,9 +9,11 @@
 //
 // How (designed for sm_103a; the pages give no kernel):
 //   * Work item = (sequence, KV head, partition of PT tokens).  PT is chosen
-//     on the device from the batch's total length so that the items number
-//     about twelve per SM; long contexts are split over block ranges and
-//     merged by log-sum-exp.  The grid is persistent (a few CTAs per SM);
+//     on the device from the batch's total length so that the items fill
+//     whole waves of one item per resident CTA: one wave for a small batch,
+//     up to about twelve items per SM for a large one; long contexts are
+//     split over block ranges and merged by log-sum-exp.  The grid is
+//     persistent (a few CTAs per SM);
 //     every CTA builds the same item list from context_lens in shared memory
 //     and takes items by a global ticket.
 //   * Each item is served by the CTA's 4 warps, which take the partition's
@@ -53,7 +55,7 @@
 // Tuning constants (the measured best on GB300).
 namespace {
 
-constexpr int kItemsPerSm = 12;         // target work items per SM (12 beat 9 and 15 on GB300)
+constexpr int kItemsPerSm = 12;         // most work items per SM (12 beat 9 and 15 on GB300)
 constexpr int kWarps = 4;               // warps per CTA sharing one item
 constexpr int kMinCtas = 3;             // resident CTAs per SM the register budget aims at (bf16)
 constexpr int kMinCtasF8 = 4;           // the same for the fp8 walk (one tile in flight per warp)
