@@ -128,6 +128,7 @@ TRAFFIC_PROFILES = {
     ("long", "bf16"): "decode_kernel_long_context.md",
     ("long", "fp8"): "decode_kernel_long_context_fp8.md",
     ("mixed", "bf16"): "decode_kernel_mixed.md",
+    ("mixed", "fp8"): "decode_kernel_mixed_fp8.md",
     ("prefix", "bf16"): "decode_call_prefix.md",
     ("prefill", "bf16"): "prefill_tc_prefill_batch.md",
     ("prefill", "fp8"): "prefill_tc_prefill_batch_fp8.md",
