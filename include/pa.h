@@ -187,7 +187,12 @@ int pa_copy_blocks(pa_pool *pool, const int64_t *pairs, int num_pairs, void *str
  *   out           device [S][num_q_heads][head_dim] of out_dtype
  * Keys/values are read once per (sequence, KV head) for all G query heads;
  * long contexts are split over block ranges and merged by log-sum-exp in a
- * second kernel (two launches per call).  Batches with more sequences than
+ * second kernel (two launches per call).  The partition length is chosen on
+ * the device from the batch's total length, so that the work items fill
+ * whole waves of one item per resident CTA (one wave for a small batch, a
+ * few for a large one; on fp8 pools partitions of at least 256 tokens while
+ * two items per SM remain); the output does not depend on that choice beyond
+ * rounding.  Batches with more sequences than
  * the GPU has SMs use partitions of at most 2048 tokens (the pool's
  * PA_OPT_PARTITION_CAP option overrides); the split never produces more
  * partials than the workspace holds.
