@@ -420,6 +420,11 @@ int pa_bm_block_table(pa_bm *bm, int req, int32_t *out, int cap, int *n);
 int pa_bm_batch_tables(pa_bm *bm, int n, const int32_t *reqs, int width, int32_t *tables,
                        int32_t *lens);
 
+/* *width = the longest block table among reqs[0..n) (0 for n = 0): the width
+ * pa_bm_batch_tables needs for that batch.  PA_ERR_UNKNOWN_REQUEST if a
+ * request is unknown (then *width is unchanged). */
+int pa_bm_batch_width(pa_bm *bm, int n, const int32_t *reqs, int *width);
+
 /* Number of tokens of a request; -1 if unknown. */
 int pa_bm_seq_len(pa_bm *bm, int req);
 

@@ -74,6 +74,7 @@ SIGNATURES = {
     "pa_bm_free_request": (c_int, [c_void_p, c_int]),
     "pa_bm_block_table": (c_int, [c_void_p, c_int, c_i32p, c_int, c_intp]),
     "pa_bm_batch_tables": (c_int, [c_void_p, c_int, c_i32p, c_int, c_i32p, c_i32p]),
+    "pa_bm_batch_width": (c_int, [c_void_p, c_int, c_i32p, c_intp]),
     "pa_bm_seq_len": (c_int, [c_void_p, c_int]),
     "pa_bm_refcount": (c_int, [c_void_p, c_int]),
     "pa_bm_num_free": (c_int, [c_void_p]),

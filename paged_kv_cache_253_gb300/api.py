@@ -317,7 +317,10 @@ class BlockManager:
     def batch_tables(self, reqs, width=None):
         r = np.ascontiguousarray(reqs, dtype=np.int32)
         if width is None:
-            width = max([1] + [len(self.block_table(x)) for x in r.tolist()])
+            w = ctypes.c_int()
+            L.check(L.pa_bm_batch_width(self.handle, len(r), _i32p(r), ctypes.byref(w)),
+                    "pa_bm_batch_width")
+            width = max(1, w.value)
         tables = np.empty((len(r), width), dtype=np.int32)
         lens = np.empty(len(r), dtype=np.int32)
         L.check(L.pa_bm_batch_tables(self.handle, len(r), _i32p(r), int(width), _i32p(tables),

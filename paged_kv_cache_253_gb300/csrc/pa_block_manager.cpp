@@ -312,10 +312,22 @@ int pa_bm_batch_tables(pa_bm* bm, int n, const int32_t* reqs, int width, int32_t
         if (!r) return PA_ERR_UNKNOWN_REQUEST;
         if (static_cast<int>(r->table.size()) > width) return PA_ERR_INVALID_ARG;
         int32_t* row = tables + static_cast<int64_t>(i) * width;
-        for (int j = 0; j < width; ++j)
-            row[j] = j < static_cast<int>(r->table.size()) ? r->table[j] : -1;
+        std::copy(r->table.begin(), r->table.end(), row);
+        std::fill(row + r->table.size(), row + width, -1);
         lens[i] = static_cast<int32_t>(r->tokens.size());
     }
+    return PA_OK;
+}
+
+int pa_bm_batch_width(pa_bm* bm, int n, const int32_t* reqs, int* width) {
+    if (!bm || n < 0 || !width || (n > 0 && !reqs)) return PA_ERR_INVALID_ARG;
+    int w = 0;
+    for (int i = 0; i < n; ++i) {
+        const Request* r = bm->find(reqs[i]);
+        if (!r) return PA_ERR_UNKNOWN_REQUEST;
+        w = std::max(w, static_cast<int>(r->table.size()));
+    }
+    *width = w;
     return PA_OK;
 }
 

@@ -165,6 +165,21 @@ def test_batch_tables_and_errors(lib):
     bm.append_slot(b, 1)
     tables, lens = bm.batch_tables([a, b])
     assert tables.tolist() == [[3, 1, 4], [0, -1, -1]] and lens.tolist() == [9, 1]
+    # the batch's widest table, from one call: 3 blocks for a, 1 for b
+    req = np.array([b, a], dtype=np.int32)
+    w = ctypes.c_int(-7)
+    assert lib.pa_bm_batch_width(bm.handle, 2, req.ctypes.data_as(lib.c_i32p), ctypes.byref(w)) == 0
+    assert w.value == 3
+    assert lib.pa_bm_batch_width(bm.handle, 1, req.ctypes.data_as(lib.c_i32p), ctypes.byref(w)) == 0
+    assert w.value == 1
+    assert lib.pa_bm_batch_width(bm.handle, 0, None, ctypes.byref(w)) == 0 and w.value == 0
+    bad = np.array([a, 99], dtype=np.int32)
+    assert lib.pa_bm_batch_width(bm.handle, 2, bad.ctypes.data_as(lib.c_i32p),
+                                 ctypes.byref(w)) == lib.PA_ERR_UNKNOWN_REQUEST
+    assert w.value == 0                      # unchanged on error
+    assert lib.pa_bm_batch_width(bm.handle, -1, None, ctypes.byref(w)) == lib.PA_ERR_INVALID_ARG
+    tables, _ = bm.batch_tables([b])         # width from the batch: one column
+    assert tables.tolist() == [[0]]
     with pytest.raises(PagedAttnError):
         bm.free_request(99)
     for t in range(11):                      # b fills the last two free blocks
